@@ -1,0 +1,228 @@
+/*
+ * splitkv.h -- split-KV (flash-decoding) attention for the decode step over a
+ * paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes.  For every sequence b, query token t and query
+ * head h (KV head h / G, G = num_q_heads / num_kv_heads), with L = seq_lens[b]
+ * and the keys 0 .. L-T+t visible to token t:
+ *
+ *     s_j  = scale * sum_d q[b][t][h][d] * K_j[d]
+ *     lse  = ln sum_j exp(s_j)                                  (fp32 output)
+ *     out  = sum_j exp(s_j - lse) * V_j                        (bf16 output)
+ *
+ * where K_j / V_j are row j % P of page block_table[b][j / P] (HND layout),
+ * dequantised as code * kv_scale when the cache is FP8-e4m3.  The KV range of
+ * each sequence is cut into num_splits page ranges, each handled by its own
+ * CTA, and the per-split results are merged by their log-sum-exp.  This is the
+ * split-KV scheme of "vLLM 0.30.0 FA4 SplitKV Bug: H100 Decode Can Be 48%
+ * Slower", section "What SplitKV is trying to do" (one query token, few KV
+ * heads, long KV history: split the KV range so more SMs work), with a
+ * partial result per split and a combine step that gives empty splits zero
+ * weight (section "Why the result is still correct").  Unlike the bug that
+ * page dissects ("The actual bug is one missing constructor argument"), the
+ * requested split count is honoured and every launched split CTA owns a
+ * non-empty KV range.  FP8 KV with BF16 queries follows "Xqa decode kernels"
+ * (vLLM pull request #43232), section "Purpose"; the multi-token MLA case
+ * follows "Shipped: 484.5 tok/s on one GB300 ...", table "What shipped".
+ *
+ * Conventions for every entry point.
+ *   - Pointers named *_host are host memory; every other data pointer is
+ *     device memory owned by the caller.  The library never allocates device
+ *     memory and never frees caller memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued asynchronously on it; only
+ *     splitkv_read_stats synchronises (that stream only).
+ *   - Arguments are validated on the host before anything is enqueued; on an
+ *     error nothing is written.  splitkv_last_error() then describes it.
+ *   - Device data pointers must be 16-byte aligned.
+ */
+#ifndef SPLITKV_H
+#define SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum splitkv_status {
+  SPLITKV_OK = 0,
+  SPLITKV_EINVAL = 1,        /* bad argument (null, shape, alignment, range)   */
+  SPLITKV_EUNSUPPORTED = 2,  /* valid shape this build has no kernel for       */
+  SPLITKV_ECUDA = 3,         /* a CUDA runtime call or launch failed           */
+  SPLITKV_EWORKSPACE = 4,    /* workspace missing or too small                 */
+  SPLITKV_EDEVICE = 5        /* a kernel reported an error in the status word  */
+} splitkv_status;
+
+typedef enum splitkv_dtype {
+  SPLITKV_BF16 = 0,          /* K/V pages hold bf16                            */
+  SPLITKV_FP8_E4M3 = 1       /* K/V pages hold OCP e4m3fn codes, x kv_scale    */
+} splitkv_dtype;
+
+typedef enum splitkv_combine_mode {
+  SPLITKV_COMBINE_FUSED = 0,    /* last split CTA of each (b, h_kv) merges      */
+  SPLITKV_COMBINE_SEPARATE = 1  /* a second kernel merges all partials          */
+} splitkv_combine_mode;
+
+/* Shapes and element types of one decode-attention call (no pointers). */
+typedef struct splitkv_desc {
+  int32_t batch;              /* B, >= 1                                        */
+  int32_t q_tokens;           /* T query tokens per sequence, causal among them */
+  int32_t num_q_heads;        /* Hq                                             */
+  int32_t num_kv_heads;       /* Hkv, divides Hq                                */
+  int32_t qk_dim;             /* Dk: 128 (GQA) or 576 (MLA latent + rope)       */
+  int32_t v_dim;              /* Dv: 128 (GQA) or 512 (MLA)                     */
+  int32_t page_size;          /* P tokens per page, multiple of 16              */
+  int32_t max_pages_per_seq;  /* row length of block_table                     */
+  int32_t num_pages_total;    /* pages in k_pages / v_pages                     */
+  int32_t kv_dtype;           /* splitkv_dtype; q and out are always bf16       */
+  int32_t v_shares_k;         /* 1: V_j = first v_dim columns of K_j (MLA)      */
+  int32_t combine_mode;       /* splitkv_combine_mode                           */
+} splitkv_desc_t;
+
+/* Opaque host object holding the split table of one set of sequence lengths. */
+typedef struct splitkv_plan_s splitkv_plan_t;
+
+/* Fields of one work item as returned by splitkv_plan_get_items (int32 each). */
+enum {
+  SPLITKV_ITEM_B = 0,         /* sequence                                        */
+  SPLITKV_ITEM_HKV = 1,       /* KV head                                         */
+  SPLITKV_ITEM_SPLIT = 2,     /* split index s in [0, S_b)                       */
+  SPLITKV_ITEM_NSPLIT = 3,    /* S_b, splits of this sequence                    */
+  SPLITKV_ITEM_PAGE0 = 4,     /* first page (logical, within the sequence)       */
+  SPLITKV_ITEM_PAGE1 = 5,     /* one past the last page                          */
+  SPLITKV_ITEM_SLOT = 6,      /* partial-result slot, -1 when S_b == 1           */
+  SPLITKV_ITEM_GROUP = 7,     /* combine group of (b, h_kv), -1 when S_b == 1    */
+  SPLITKV_ITEM_FIELDS = 8
+};
+
+/*
+ * splitkv_plan -- split planning (host only; no CUDA call unless num_sms == 0).
+ *
+ * For each sequence, n_b = ceil(seq_lens_host[b] / P) pages.  With
+ * num_splits > 0, S_b = min(num_splits, n_b): the request is honoured
+ * whenever the sequence has that many pages.  With num_splits == 0 the
+ * planner picks one chunk size for all sequences by a load-balance cost model
+ * over num_sms SMs (largest-first list scheduling of the work items, plus a
+ * per-split merge cost) and S_b = clamp(ceil(n_b / chunk), 1, min(n_b, 64)).
+ * Split s covers pages [floor(s*n_b/S_b), floor((s+1)*n_b/S_b)), which is
+ * never empty.  Items are ordered longest first.  A sequence with no keys gets
+ * one empty item per KV head that writes out = 0, lse = -inf.
+ *
+ *   desc           shapes; copied into the plan
+ *   seq_lens_host  [B] int32, 0 <= L <= max_pages_per_seq * P, L >= T or L == 0
+ *   num_splits     requested splits per sequence, 0 = planner's choice, <= 64
+ *   num_sms        SMs to plan for; 0 = query the current device
+ *   plan_out       receives a new plan; free with splitkv_plan_destroy
+ */
+splitkv_status splitkv_plan(const splitkv_desc_t* desc, const int32_t* seq_lens_host,
+                            int32_t num_splits, int32_t num_sms, splitkv_plan_t** plan_out);
+
+/* Frees a plan (NULL is ignored). */
+void splitkv_plan_destroy(splitkv_plan_t* plan);
+
+/*
+ * Copies the work list out: items_host receives n * SPLITKV_ITEM_FIELDS int32
+ * in launch order (fields above); capacity is in items.  *n_items always
+ * receives the item count; EINVAL if capacity is smaller (nothing copied).
+ */
+splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items_host,
+                                      int32_t capacity, int32_t* n_items);
+
+/* Number of work items = CTAs of the partial kernel. */
+int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
+
+/* Bytes of device workspace the plan needs (work list, tickets, per-CTA log,
+ * partial outputs).  0 if plan is NULL. */
+size_t splitkv_workspace_size(const splitkv_plan_t* plan);
+
+/*
+ * splitkv_plan_upload -- writes the plan's work list into `workspace` and
+ * zeroes its merge tickets and status word (one host->device copy on
+ * `stream`).  Must be called once per (plan, workspace) pair before
+ * splitkv_decode; the kernels leave the tickets zeroed, so repeated decodes
+ * (including CUDA-graph replays) need no further upload.
+ */
+splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
+ * splitkv_decode -- one split-KV decode-attention call.
+ *
+ *   q            bf16 [B][T][Hq][Dk]
+ *   k_pages      [num_pages_total][Hkv][P][Dk] of bf16 or e4m3 codes
+ *   v_pages      [num_pages_total][Hkv][P][Dv]; ignored (may be NULL) when
+ *                v_shares_k
+ *   block_table  int32 [B][max_pages_per_seq] physical page ids; entries past
+ *                ceil(L/P) are never read
+ *   seq_lens     int32 [B] device copy of the lengths the plan was built from
+ *                (a mismatch is recorded in the status word)
+ *   num_splits   the plan's num_splits, or 0 (= whatever the plan holds)
+ *   scale        softmax scale applied to q.K (e.g. 1/sqrt(Dk))
+ *   kv_scale     dequantisation scale of FP8 K and V (ignored for bf16)
+ *   out          bf16 [B][T][Hq][Dv]
+ *   lse          fp32 [B][T][Hq], natural-log LSE of the scaled scores; may be
+ *                NULL
+ *   workspace    uploaded with splitkv_plan_upload for this plan
+ * Launches one kernel (FUSED) or two (SEPARATE, second with programmatic
+ * dependent launch).
+ */
+splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace,
+                              const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              int32_t num_splits, float scale, float kv_scale,
+                              void* out, float* lse, void* stream);
+
+/*
+ * splitkv_combine -- the log-sum-exp merge on its own, over caller buffers.
+ * For each row r < rows: M = max_s lse_part[s][r]; lse = M + ln sum_s
+ * exp(lse_part[s][r] - M); out[r][:] = sum_s exp(lse_part[s][r] - lse) *
+ * o_part[s][r][:].  Partials with lse = -inf have weight 0; if every partial
+ * of a row is -inf the row gets out = 0, lse = -inf.
+ *   o_part    fp32 [n_parts][rows][dv]      lse_part  fp32 [n_parts][rows]
+ *   out_bf16  bf16 [rows][dv] or NULL       out_f32   fp32 [rows][dv] or NULL
+ *   lse_out   fp32 [rows] or NULL           dv a multiple of 4, <= 1024
+ */
+splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32_t n_parts,
+                               int32_t rows, int32_t dv, void* out_bf16, float* out_f32,
+                               float* lse_out, void* stream);
+
+/*
+ * splitkv_read_stats -- synchronises `stream`, then copies to the host the
+ * per-CTA log of the last decode on `workspace` and the device status word.
+ *   cta_log_host  int32 [n_items][4] or NULL: per launched CTA {first page,
+ *                 one-past-last page it iterated, keys it scored, 1 if it
+ *                 merged its group}, in item order
+ *   status_host   int32 or NULL: 0, or a bit set of SPLITKV_DEVERR_* values
+ */
+splitkv_status splitkv_read_stats(const splitkv_plan_t* plan, const void* workspace,
+                                  int32_t* cta_log_host, int32_t* status_host, void* stream);
+
+enum {
+  SPLITKV_DEVERR_TIMEOUT = 1,    /* a bounded wait on a shared-memory barrier gave up */
+  SPLITKV_DEVERR_SEQLEN = 2,     /* device seq_lens differs from the plan's           */
+  SPLITKV_DEVERR_PAGE = 4        /* a block-table entry was outside [0, num_pages)    */
+};
+
+/*
+ * splitkv_debug_gather -- copies keys [0, n_keys) of sequence b, KV head h_kv
+ * through the block table into dst_host-shaped device memory `dst`
+ * ([n_keys][row_bytes / element size] raw elements), using the same TMA
+ * tensor-map loads and swizzled shared-memory reads as the decode kernel.
+ * `pages` is k_pages or v_pages, `row_elems` its last dimension.  For
+ * checking the paged gather bit for bit.
+ */
+splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* pages,
+                                    int32_t row_elems, const int32_t* block_table,
+                                    int32_t b, int32_t h_kv, int32_t n_keys, void* dst,
+                                    void* stream);
+
+/* Thread-local description of the last error returned on this thread. */
+const char* splitkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITKV_H */

@@ -1,0 +1,318 @@
+// C-ABI layer: argument validation, workspace layout, tensor maps, launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+namespace splitkv {
+
+namespace {
+thread_local char g_err[512] = "";
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over [rows][dim] elements with 16-row boxes, 128-byte swizzle.
+// bf16 boxes are 64 columns wide (two per row), e4m3 boxes 128 columns.
+splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int elt = fp8 ? 1 : 2;
+  CUtensorMap m;
+  cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
+  cuuint64_t gstride[1] = {cuuint64_t(dim) * elt};
+  cuuint32_t box[2] = {cuuint32_t(fp8 ? 128 : 64), 16u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "tensor map size");
+  std::memcpy(out, &m, sizeof(m));
+  return SPLITKV_OK;
+}
+
+splitkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SPLITKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+splitkv_status validate_desc(const splitkv_desc_t* d) {
+  if (!d) return fail(SPLITKV_EINVAL, "desc is NULL");
+  if (d->batch < 1 || d->q_tokens < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1)
+    return fail(SPLITKV_EINVAL, "batch, q_tokens and head counts must be >= 1");
+  if (d->num_q_heads % d->num_kv_heads)
+    return fail(SPLITKV_EINVAL, "num_q_heads (%d) must be a multiple of num_kv_heads (%d)",
+                d->num_q_heads, d->num_kv_heads);
+  if (d->qk_dim < 1 || d->v_dim < 1) return fail(SPLITKV_EINVAL, "dims must be >= 1");
+  if (d->page_size < 16 || d->page_size % 16)
+    return fail(SPLITKV_EINVAL, "page_size (%d) must be a positive multiple of 16", d->page_size);
+  if (d->max_pages_per_seq < 1 || d->num_pages_total < 1)
+    return fail(SPLITKV_EINVAL, "max_pages_per_seq and num_pages_total must be >= 1");
+  if (d->kv_dtype != SPLITKV_BF16 && d->kv_dtype != SPLITKV_FP8_E4M3)
+    return fail(SPLITKV_EINVAL, "unknown kv_dtype %d", d->kv_dtype);
+  if (d->v_shares_k != 0 && d->v_shares_k != 1) return fail(SPLITKV_EINVAL, "v_shares_k must be 0 or 1");
+  if (d->v_shares_k && d->v_dim > d->qk_dim)
+    return fail(SPLITKV_EINVAL, "v_shares_k needs v_dim <= qk_dim");
+  if (d->combine_mode != SPLITKV_COMBINE_FUSED && d->combine_mode != SPLITKV_COMBINE_SEPARATE)
+    return fail(SPLITKV_EINVAL, "unknown combine_mode %d", d->combine_mode);
+  if (int64_t(d->num_pages_total) * d->num_kv_heads * d->page_size >= (int64_t(1) << 31))
+    return fail(SPLITKV_EINVAL, "num_pages_total * num_kv_heads * page_size must be < 2^31");
+  if (family_of(*d) == Family::kNone)
+    return fail(SPLITKV_EUNSUPPORTED,
+                "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
+                "(GQA: qk_dim=v_dim=128, T*G<=8)",
+                d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
+                d->v_shares_k);
+  return SPLITKV_OK;
+}
+
+}  // namespace
+
+splitkv_status fail(splitkv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+Family family_of(const splitkv_desc_t& d) {
+  const int G = d.num_q_heads / d.num_kv_heads;
+  if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 8) return Family::kGqa;
+  return Family::kNone;
+}
+
+int ctas_per_item(const splitkv_desc_t& d) {
+  (void)d;
+  return 1;
+}
+
+}  // namespace splitkv
+
+using namespace splitkv;
+
+extern "C" {
+
+const char* splitkv_last_error(void) { return g_err; }
+
+splitkv_status splitkv_plan(const splitkv_desc_t* desc, const int32_t* seq_lens_host,
+                            int32_t num_splits, int32_t num_sms, splitkv_plan_t** plan_out) {
+  if (!plan_out) return fail(SPLITKV_EINVAL, "plan_out is NULL");
+  *plan_out = nullptr;
+  splitkv_status st = validate_desc(desc);
+  if (st != SPLITKV_OK) return st;
+  if (!seq_lens_host) return fail(SPLITKV_EINVAL, "seq_lens_host is NULL");
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(SPLITKV_EINVAL, "num_splits (%d) must be in [0, %d]", num_splits, kMaxSplits);
+  if (num_sms < 0) return fail(SPLITKV_EINVAL, "num_sms must be >= 0");
+  const int64_t cap = int64_t(desc->max_pages_per_seq) * desc->page_size;
+  for (int b = 0; b < desc->batch; ++b) {
+    const int32_t L = seq_lens_host[b];
+    if (L < 0 || L > cap)
+      return fail(SPLITKV_EINVAL, "seq_lens[%d] = %d outside [0, max_pages_per_seq * page_size = %lld]",
+                  b, L, (long long)cap);
+    if (L > 0 && L < desc->q_tokens)
+      return fail(SPLITKV_EINVAL, "seq_lens[%d] = %d is shorter than q_tokens = %d", b, L,
+                  desc->q_tokens);
+  }
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+  }
+  splitkv_plan_s* p = new (std::nothrow) splitkv_plan_s();
+  if (!p) return fail(SPLITKV_EINVAL, "out of host memory");
+  p->desc = *desc;
+  p->num_splits = num_splits;
+  p->num_sms = num_sms;
+  p->seq_lens.assign(seq_lens_host, seq_lens_host + desc->batch);
+  build_plan(p);
+  *plan_out = p;
+  return SPLITKV_OK;
+}
+
+void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
+
+int32_t splitkv_plan_num_items(const splitkv_plan_t* plan) { return plan ? plan->n_items : 0; }
+
+splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items_host,
+                                      int32_t capacity, int32_t* n_items) {
+  if (!plan || !n_items) return fail(SPLITKV_EINVAL, "plan and n_items must not be NULL");
+  *n_items = plan->n_items;
+  if (!items_host) return capacity == 0 ? SPLITKV_OK : fail(SPLITKV_EINVAL, "items_host is NULL");
+  if (capacity < plan->n_items)
+    return fail(SPLITKV_EINVAL, "capacity %d < %d items", capacity, plan->n_items);
+  std::memcpy(items_host, plan->items.data(), plan->items.size() * sizeof(int32_t));
+  return SPLITKV_OK;
+}
+
+size_t splitkv_workspace_size(const splitkv_plan_t* plan) { return plan ? plan->total : 0; }
+
+splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
+  if (!workspace) return fail(SPLITKV_EWORKSPACE, "workspace is NULL");
+  if (!aligned16(workspace)) return fail(SPLITKV_EINVAL, "workspace must be 16-byte aligned");
+  if (workspace_bytes < plan->total)
+    return fail(SPLITKV_EWORKSPACE, "workspace has %zu bytes, plan needs %zu", workspace_bytes,
+                plan->total);
+  cudaError_t e = cudaMemcpyAsync(workspace, plan->upload.data(), plan->upload_bytes,
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "uploading the plan");
+  return SPLITKV_OK;
+}
+
+splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              int32_t num_splits, float scale, float kv_scale, void* out,
+                              float* lse, void* stream) {
+  if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
+  const splitkv_desc_t& d = plan->desc;
+  if (!workspace) return fail(SPLITKV_EWORKSPACE, "workspace is NULL");
+  if (!q || !k_pages || !block_table || !seq_lens || !out)
+    return fail(SPLITKV_EINVAL, "q, k_pages, block_table, seq_lens and out must not be NULL");
+  if (!d.v_shares_k && !v_pages) return fail(SPLITKV_EINVAL, "v_pages is NULL");
+  const void* ptrs[] = {workspace, q, k_pages, out, block_table, seq_lens};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return fail(SPLITKV_EINVAL, "device pointers must be 16-byte aligned");
+  if (v_pages && !aligned16(v_pages)) return fail(SPLITKV_EINVAL, "v_pages must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SPLITKV_EINVAL, "lse must be 4-byte aligned");
+  if (num_splits != 0 && num_splits != plan->num_splits)
+    return fail(SPLITKV_EINVAL, "num_splits %d differs from the plan's %d", num_splits,
+                plan->num_splits);
+  if (!(scale > 0.f) || !(scale < 1e30f)) return fail(SPLITKV_EINVAL, "scale must be positive and finite");
+  const bool fp8 = d.kv_dtype == SPLITKV_FP8_E4M3;
+  if (fp8 && (!(kv_scale > 0.f) || !(kv_scale < 1e30f)))
+    return fail(SPLITKV_EINVAL, "kv_scale must be positive and finite");
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  DecodeArgs a{};
+  a.items = reinterpret_cast<const int32_t*>(ws + plan->off_items);
+  a.groups = reinterpret_cast<const int32_t*>(ws + plan->off_groups);
+  a.plan_lens = reinterpret_cast<const int32_t*>(ws + plan->off_seqlens);
+  a.tickets = reinterpret_cast<int32_t*>(ws + plan->off_tickets);
+  a.cta_log = reinterpret_cast<int32_t*>(ws + plan->off_log);
+  a.status = reinterpret_cast<int32_t*>(ws + plan->off_status);
+  a.lse_part = reinterpret_cast<float*>(ws + plan->off_lse);
+  a.o_part = reinterpret_cast<float*>(ws + plan->off_o);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.q = q;
+  a.out = out;
+  a.lse = lse;
+  a.n_items = plan->n_items;
+  a.n_groups = plan->n_groups;
+  a.batch = d.batch;
+  a.T = d.q_tokens;
+  a.Hq = d.num_q_heads;
+  a.Hkv = d.num_kv_heads;
+  a.G = d.num_q_heads / d.num_kv_heads;
+  a.P = d.page_size;
+  a.max_pages = d.max_pages_per_seq;
+  a.num_pages = d.num_pages_total;
+  a.rows = plan->rows;
+  a.dv = d.v_dim;
+  const float kLog2e = 1.4426950408889634f;
+  // FP8 tiles are read as f16 values equal to code * 2^-8 (see the kernel), so
+  // both the score scale and the output scale carry an extra 2^8.
+  a.qk_scale_log2 = scale * kLog2e * (fp8 ? kv_scale * 256.f : 1.f);
+  a.o_scale = fp8 ? kv_scale * 256.f : 1.f;
+  a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
+
+  const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
+  TmaDesc tk, tv;
+  splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total);
+  if (st != SPLITKV_OK) return st;
+  st = make_kv_map(&tv, v_pages, fp8, d.v_dim, rows_total);
+  if (st != SPLITKV_OK) return st;
+
+  cudaError_t e = launch_gqa(a, tk, tv, fp8, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the split-KV kernel");
+  if (!a.fused) {
+    e = launch_combine(a, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
+  }
+  return SPLITKV_OK;
+}
+
+splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32_t n_parts,
+                               int32_t rows, int32_t dv, void* out_bf16, float* out_f32,
+                               float* lse_out, void* stream) {
+  if (!o_part || !lse_part) return fail(SPLITKV_EINVAL, "o_part and lse_part must not be NULL");
+  if (n_parts < 1 || rows < 0) return fail(SPLITKV_EINVAL, "n_parts must be >= 1, rows >= 0");
+  if (dv < 4 || dv % 4 || dv > 1024) return fail(SPLITKV_EINVAL, "dv must be a multiple of 4 in [4, 1024]");
+  if (!out_bf16 && !out_f32 && !lse_out) return fail(SPLITKV_EINVAL, "no output given");
+  if (!aligned16(o_part) || (out_f32 && !aligned16(out_f32)) ||
+      (out_bf16 && (reinterpret_cast<uintptr_t>(out_bf16) & 7u)))
+    return fail(SPLITKV_EINVAL, "misaligned buffers");
+  cudaError_t e = launch_combine_raw(o_part, lse_part, n_parts, rows, dv, out_bf16, out_f32,
+                                     lse_out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
+  return SPLITKV_OK;
+}
+
+splitkv_status splitkv_read_stats(const splitkv_plan_t* plan, const void* workspace,
+                                  int32_t* cta_log_host, int32_t* status_host, void* stream) {
+  if (!plan || !workspace) return fail(SPLITKV_EINVAL, "plan and workspace must not be NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned char* ws = static_cast<const unsigned char*>(workspace);
+  cudaError_t e = cudaSuccess;
+  if (cta_log_host && plan->n_ctas)
+    e = cudaMemcpyAsync(cta_log_host, ws + plan->off_log,
+                        size_t(plan->n_ctas) * kLogFields * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && status_host)
+    e = cudaMemcpyAsync(status_host, ws + plan->off_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the statistics");
+  return SPLITKV_OK;
+}
+
+splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* pages,
+                                    int32_t row_elems, const int32_t* block_table, int32_t b,
+                                    int32_t h_kv, int32_t n_keys, void* dst, void* stream) {
+  splitkv_status st = validate_desc(desc);
+  if (st != SPLITKV_OK) return st;
+  if (!pages || !block_table || !dst) return fail(SPLITKV_EINVAL, "NULL pointer");
+  if (row_elems != 128) return fail(SPLITKV_EUNSUPPORTED, "debug gather supports 128-wide rows");
+  if (b < 0 || b >= desc->batch || h_kv < 0 || h_kv >= desc->num_kv_heads)
+    return fail(SPLITKV_EINVAL, "b or h_kv out of range");
+  if (n_keys < 0 || int64_t(n_keys) > int64_t(desc->max_pages_per_seq) * desc->page_size)
+    return fail(SPLITKV_EINVAL, "n_keys out of range");
+  if (!aligned16(pages) || !aligned16(dst)) return fail(SPLITKV_EINVAL, "misaligned buffers");
+  const bool fp8 = desc->kv_dtype == SPLITKV_FP8_E4M3;
+  const int64_t rows_total = int64_t(desc->num_pages_total) * desc->num_kv_heads * desc->page_size;
+  TmaDesc t;
+  st = make_kv_map(&t, pages, fp8, row_elems, rows_total);
+  if (st != SPLITKV_OK) return st;
+  cudaError_t e = launch_debug_gather(t, fp8, row_elems * (fp8 ? 1 : 2),
+                                      block_table + size_t(b) * desc->max_pages_per_seq,
+                                      desc->page_size, desc->num_kv_heads, h_kv, desc->page_size,
+                                      n_keys, dst, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the gather kernel");
+  return SPLITKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,572 @@
+// Split-KV partial attention for thin query groups (GQA), sm_103a.
+//
+// One CTA per work item (b, h_kv, split, page range).  The split's pages are
+// streamed HBM -> shared memory by TMA (one 2-D tiled box per 16-key tile of
+// K and of V, 128-byte swizzle so the ldmatrix reads below are bank-conflict
+// free), through a ring of NST stages guarded by mbarriers.  One producer
+// warp issues the copies; four consumer warps take the tiles round-robin.
+//
+// Per 16-key tile a consumer warp computes, on the warp tensor-core path:
+//   S^T[16 keys x 8 rows] = K_tile[16 x 128] . Q^T      (m16n8k16, keys on M)
+//   online softmax over the keys of each query row (shuffle reductions)
+//   O^T[128 x 8 rows]   += V_tile^T[128 x 16] . P^T     (m16n8k16, dims on M)
+// so a group of up to 8 query rows (T*G <= 8) fills the MMA's N side and the
+// 16-key tile fills M with no padding.  P^T is turned from accumulator layout
+// into operand layout in registers with movmatrix.  FP8 e4m3 tiles are
+// converted to f16 in registers (exact, see ptx::fp8x2_*) and use the f16
+// MMA; BF16 tiles go straight to the bf16 MMA.
+//
+// The four warps' (m, l, O) are merged in shared memory; the item's result is
+// written as the final bf16 output (S_b == 1) or as an fp32 partial with its
+// natural-log LSE.  With the fused combine, the last CTA of a (b, h_kv) group
+// (atomic ticket, no waiting) merges the group's partials.
+//
+// This is the split partial of "vLLM 0.30.0 FA4 SplitKV Bug: H100 Decode Can
+// Be 48% Slower", section "What SplitKV is trying to do"; the merge gives
+// partials with LSE = -inf zero weight (section "Why the result is still
+// correct").  FP8 KV with BF16 queries: "Xqa decode kernels", section
+// "Purpose".
+#include <cuda_runtime.h>
+
+#include <cfloat>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace splitkv {
+namespace {
+
+using namespace ptx;
+
+template <bool FP8>
+struct Gqa {
+  static constexpr int D = 128;
+  static constexpr int TK = 16;                            // keys per tile
+  static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one K (or V) tile
+  static constexpr int STAGE = 2 * KT_BYTES;
+  static constexpr int NST = FP8 ? 16 : 8;  // 64 KB ring either way
+  static constexpr int NCW = 4;             // consumer warps
+  static constexpr int THREADS = (NCW + 1) * 32;
+  static constexpr int RING = NST * STAGE;
+  static constexpr int MERGE = NCW * 8 * D * 4 + NCW * 8 * 2 * 4;
+  static_assert(MERGE <= RING, "merge area aliases the ring");
+  static constexpr int BARS = 2 * NST * 8;
+  static constexpr int SMEM = 1024 + RING + BARS + 64;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a tile stored
+// as 128-byte rows with the TMA 128-byte swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// BF16 tiles are two 64-column halves, each [16 rows][128 B], 2 KB apart.
+__device__ __forceinline__ uint32_t swz_bf16(int row, int d) {
+  return static_cast<uint32_t>((d >> 6) * 2048) + swz(row, (d & 63) >> 3);
+}
+
+// Merges the (m, l, O) of the consumer warps and writes the item's result.
+// Runs on the 128 consumer threads; `mo` is [NCW][8][128] fp32, `mm`/`ml`
+// [NCW][8].  m is in log2 units.
+template <bool FP8>
+__device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, const float* mo,
+                                                const float* mm, const float* ml, int b, int hkv,
+                                                int slot) {
+  constexpr int NCW = Gqa<FP8>::NCW;
+  const int n = tid >> 4;          // query row 0..7
+  const int d0 = (tid & 15) * 8;   // 8 consecutive dims
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) M = fmaxf(M, mm[w * 8 + n]);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float lsum = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) {
+      const float sc = ex2(mm[w * 8 + n] - M);
+      lsum += sc * ml[w * 8 + n];
+      const float4* src = reinterpret_cast<const float4*>(mo + (w * 8 + n) * 128 + d0);
+      const float4 x0 = src[0], x1 = src[1];
+      acc[0] += sc * x0.x; acc[1] += sc * x0.y; acc[2] += sc * x0.z; acc[3] += sc * x0.w;
+      acc[4] += sc * x1.x; acc[5] += sc * x1.y; acc[6] += sc * x1.z; acc[7] += sc * x1.w;
+    }
+  }
+  float lse_n;
+  if (lsum > 0.f) {
+    const float inv = a.o_scale / lsum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= inv;
+    lse_n = (M + lg2(lsum)) * kLn2;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    lse_n = -INFINITY;
+  }
+  if (n >= a.rows) return;
+  if (slot < 0) {
+    const int t = n / a.G, g = n - (n / a.G) * a.G;
+    const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g;
+    uint4 v;
+    v.x = pack_bf16(acc[0], acc[1]);
+    v.y = pack_bf16(acc[2], acc[3]);
+    v.z = pack_bf16(acc[4], acc[5]);
+    v.w = pack_bf16(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0) = v;
+    if (d0 == 0 && a.lse) a.lse[row] = lse_n;
+  } else {
+    float* dst = a.o_part + (size_t(slot) * a.rows + n) * 128 + d0;
+    reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (d0 == 0) a.lse_part[size_t(slot) * a.rows + n] = lse_n;
+  }
+}
+
+// Log-sum-exp merge of the S partials of one (b, h_kv) group, by the CTA that
+// finished last.  128 threads: row n = tid / 16, dims d0 .. d0+7.
+__device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int hkv,
+                                            int slot0, int S) {
+  const int n = tid >> 4;
+  const int d0 = (tid & 15) * 8;
+  if (n >= a.rows) return;
+  const float* lp = a.lse_part + size_t(slot0) * a.rows + n;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(lp + size_t(s) * a.rows));
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float w = ex2((__ldcg(lp + size_t(s) * a.rows) - M) * kLog2e);
+      if (w == 0.f) continue;
+      wsum += w;
+      const float4* src =
+          reinterpret_cast<const float4*>(a.o_part + (size_t(slot0 + s) * a.rows + n) * 128 + d0);
+      const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+      acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+      acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+    }
+  }
+  float lse_n = -INFINITY;
+  if (wsum > 0.f) {
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= inv;
+    lse_n = M + lg2(wsum) * kLn2;
+  }
+  const int t = n / a.G, g = n - (n / a.G) * a.G;
+  const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g;
+  uint4 v;
+  v.x = pack_bf16(acc[0], acc[1]);
+  v.y = pack_bf16(acc[2], acc[3]);
+  v.z = pack_bf16(acc[4], acc[5]);
+  v.w = pack_bf16(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0) = v;
+  if (d0 == 0 && a.lse) a.lse[row] = lse_n;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
+    gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv) {
+  using C = Gqa<FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::RING);
+  uint64_t* empty = full + C::NST;
+  int* misc = reinterpret_cast<int*>(empty + C::NST);  // [0] merge flag, [1] keys scored
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* it = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
+  const int b = it[SPLITKV_ITEM_B], hkv = it[SPLITKV_ITEM_HKV];
+  const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
+  const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
+  const int slot = it[SPLITKV_ITEM_SLOT], group = it[SPLITKV_ITEM_GROUP];
+  const int L = a.seq_lens[b];
+  const int k_begin = p0 * a.P;
+  const int k_end = min(p1 * a.P, L);
+  const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    misc[0] = 0;
+    misc[1] = 0;
+    fence_mbar_init();
+    if (a.plan_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
+  }
+  __syncthreads();
+  launch_dependents();
+
+  if (warp == C::NCW) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+    }
+    const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
+    const int pg_end = (k_end + a.P - 1) / a.P;
+    const int tiles_per_page = a.P >> 4;
+    int tile = 0;
+    bool ok = true;
+    for (int pc = p0; pc < pg_end && ok; pc += 32) {
+      const int my = pc + lane;
+      int phys = 0;
+      if (my < pg_end) {
+        phys = __ldg(trow + my);
+        if (phys < 0 || phys >= a.num_pages) {
+          atomicOr(a.status, SPLITKV_DEVERR_PAGE);
+          phys = 0;
+        }
+      }
+      const int cnt = min(32, pg_end - pc);
+      for (int j = 0; j < cnt && ok; ++j) {
+        const int ph = __shfl_sync(kFull, phys, j);
+        const int key_page = (pc + j) * a.P;
+        for (int sub = 0; sub < tiles_per_page; ++sub) {
+          if (key_page + sub * 16 >= k_end) break;
+          if (lane == 0) {
+            const int st = tile % C::NST;
+            if (tile >= C::NST && !mbar_wait(smem_u32(empty + st), ((tile / C::NST) - 1) & 1)) {
+              atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+              ok = false;
+            }
+            if (ok) {
+              const uint32_t bar = smem_u32(full + st);
+              const uint32_t dk = smem_u32(ring + st * C::STAGE);
+              const uint32_t dv = dk + C::KT_BYTES;
+              const int row = (ph * a.Hkv + hkv) * a.P + sub * 16;
+              mbar_arrive_expect_tx(bar, C::STAGE);
+              if (FP8) {
+                tma_load_2d(dk, &tk, bar, 0, row);
+                tma_load_2d(dv, &tv, bar, 0, row);
+              } else {
+                tma_load_2d(dk, &tk, bar, 0, row);
+                tma_load_2d(dk + 2048, &tk, bar, 64, row);
+                tma_load_2d(dv, &tv, bar, 0, row);
+                tma_load_2d(dv + 2048, &tv, bar, 64, row);
+              }
+            }
+          }
+          ok = __shfl_sync(kFull, ok, 0);
+          if (!ok) break;
+          ++tile;
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int tid = threadIdx.x;  // 0 .. 127
+  const int gi = lane >> 2, ti = lane & 3;
+
+  // Q^T operand fragments: row n = gi, dims by ti (see the layout notes).
+  uint32_t qf[8][2];
+  {
+    const int n = gi;
+    if (n < a.rows) {
+      const int t = n / a.G, g = n - t * a.G;
+      const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) +
+                                ((size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g) * 128;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        if (!FP8) {
+          qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * ti));
+          qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * ti + 8));
+        } else {
+          // k = 2ti, 2ti+1 <-> d = 16ks+4ti, +2 ; k = 2ti+8, 2ti+9 <-> d = 16ks+4ti+1, +3
+          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qp + ks * 16 + 4 * ti));
+          const float f0 = __uint_as_float(raw.x << 16), f1 = __uint_as_float(raw.x & 0xffff0000u);
+          const float f2 = __uint_as_float(raw.y << 16), f3 = __uint_as_float(raw.y & 0xffff0000u);
+          qf[ks][0] = pack_f16(f0, f2);
+          qf[ks][1] = pack_f16(f1, f3);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+    }
+  }
+  // Visible-key limits of the two query rows whose scores this lane holds.
+  int lim0 = -1, lim1 = -1;
+  {
+    const int n0 = 2 * ti, n1 = 2 * ti + 1;
+    if (n0 < a.rows) lim0 = L - a.T + n0 / a.G;
+    if (n1 < a.rows) lim1 = L - a.T + n1 / a.G;
+  }
+  const int min_lim = L - a.T;
+
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int keys_scored = 0;
+
+  for (int i = warp; i < n_tiles; i += C::NCW) {
+    const int st = i % C::NST;
+    const bool arrived = __all_sync(kFull, mbar_wait(smem_u32(full + st), (i / C::NST) & 1));
+    if (!arrived) {
+      if (lane == 0) atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+      break;
+    }
+    uint8_t* kt = ring + st * C::STAGE;
+    uint8_t* vt = kt + C::KT_BYTES;
+    const int key0 = k_begin + i * 16;
+    const int valid = min(16, k_end - key0);
+    keys_scored += valid;
+    if (valid < 16) {
+      // Slots past the last visible key may hold anything (even NaN): zero
+      // those V rows so that 0 * V stays 0 in the PV product.
+      const int rows_bad = 16 - valid;
+      const int halves = FP8 ? 1 : 2;
+      for (int x = lane; x < rows_bad * 8 * halves; x += 32) {
+        const int r = valid + (x >> 3) % rows_bad;
+        const int h = x / (8 * rows_bad);
+        *reinterpret_cast<uint4*>(vt + h * 2048 + r * 128 + (x & 7) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      // order these generic-proxy writes before the stage's next TMA refill
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+
+    // ---- S^T = K . Q^T
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t kbase = smem_u32(kt);
+    const int mi = lane >> 3, mr = lane & 7;
+    if (!FP8) {
+      const int krow = (mi & 1) * 8 + mr;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t af[4];
+        ldsm_x4(kbase + swz_bf16(krow, ks * 16 + (mi >> 1) * 8), af);
+        mma_bf16(sc, af, qf[ks][0], qf[ks][1]);
+      }
+    } else {
+      const int krow = (mi & 1) * 8 + mr;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t x[4];
+        ldsm_x4(kbase + swz(krow, 2 * kk + (mi >> 1)), x);
+        uint32_t af[4] = {fp8x2_lo(x[0]), fp8x2_lo(x[1]), fp8x2_hi(x[0]), fp8x2_hi(x[1])};
+        mma_f16(sc, af, qf[2 * kk][0], qf[2 * kk][1]);
+        uint32_t ag[4] = {fp8x2_lo(x[2]), fp8x2_lo(x[3]), fp8x2_hi(x[2]), fp8x2_hi(x[3])};
+        mma_f16(sc, ag, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+      }
+    }
+
+    // ---- scores in log2 units, masked
+    float s0 = sc[0] * a.qk_scale_log2, s1 = sc[1] * a.qk_scale_log2;
+    float s2 = sc[2] * a.qk_scale_log2, s3 = sc[3] * a.qk_scale_log2;
+    if (key0 + 15 > min_lim) {
+      const int ka = key0 + gi, kb = ka + 8;
+      s0 = ka <= lim0 ? s0 : -INFINITY;
+      s1 = ka <= lim1 ? s1 : -INFINITY;
+      s2 = kb <= lim0 ? s2 : -INFINITY;
+      s3 = kb <= lim1 ? s3 : -INFINITY;
+    }
+    float t0 = fmaxf(s0, s2), t1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, off));
+      t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, off));
+    }
+    const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+    if (__any_sync(kFull, n0 > m0 || n1 > m1)) {
+      const float a0 = ex2(m0 - (n0 == -INFINITY ? 0.f : n0));
+      const float a1 = ex2(m1 - (n1 == -INFINITY ? 0.f : n1));
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+      l0 *= a0;
+      l1 *= a1;
+      m0 = n0;
+      m1 = n1;
+    }
+    const float ms0 = m0 == -INFINITY ? 0.f : m0, ms1 = m1 == -INFINITY ? 0.f : m1;
+    const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1), p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+
+    // ---- P^T into operand layout: keys on K, query rows on N
+    const uint32_t pk0 = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+    const uint32_t pk1 = FP8 ? pack_f16(p2, p3) : pack_bf16(p2, p3);
+    const uint32_t pb0 = movmatrix_t(pk0), pb1 = movmatrix_t(pk1);
+
+    // ---- O^T += V^T . P^T
+    const uint32_t vbase = smem_u32(vt);
+    if (!FP8) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t af[4];
+        ldsm_x4_t(vbase + swz_bf16((mi >> 1) * 8 + mr, mt * 16 + (mi & 1) * 8), af);
+        mma_bf16(o[mt], af, pb0, pb1);
+      }
+    } else {
+      const int vr = (mi & 1) * 8 + mr;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t x[4];
+        ldsm_x4_t(vbase + swz(vr, 2 * cc + (mi >> 1)), x);
+        uint32_t af[4] = {fp8x2_lo(x[0]), fp8x2_hi(x[0]), fp8x2_lo(x[1]), fp8x2_hi(x[1])};
+        mma_f16(o[2 * cc], af, pb0, pb1);
+        uint32_t ag[4] = {fp8x2_lo(x[2]), fp8x2_hi(x[2]), fp8x2_lo(x[3]), fp8x2_hi(x[3])};
+        mma_f16(o[2 * cc + 1], ag, pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(empty + st));
+  }
+
+  // ---- warp totals of l over the 8 lanes sharing each row pair
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, off);
+    l1 += __shfl_xor_sync(kFull, l1, off);
+  }
+  if (lane == 0) atomicAdd(&misc[1], keys_scored);
+
+  // ---- cross-warp merge through shared memory (aliases the drained ring)
+  asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+  float* mo = reinterpret_cast<float*>(ring);
+  float* mm = mo + C::NCW * 8 * 128;
+  float* ml = mm + C::NCW * 8;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    int da, db;
+    if (!FP8) {
+      da = mt * 16 + gi;
+      db = da + 8;
+    } else {
+      da = mt * 16 + 2 * gi;
+      db = da + 1;
+    }
+    float* w0 = mo + (warp * 8 + 2 * ti) * 128;
+    float* w1 = w0 + 128;
+    w0[da] = o[mt][0];
+    w1[da] = o[mt][1];
+    w0[db] = o[mt][2];
+    w1[db] = o[mt][3];
+  }
+  if (gi == 0) {
+    mm[warp * 8 + 2 * ti] = m0;
+    mm[warp * 8 + 2 * ti + 1] = m1;
+    ml[warp * 8 + 2 * ti] = l0;
+    ml[warp * 8 + 2 * ti + 1] = l1;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+  merge_and_store<FP8>(a, tid, mo, mm, ml, b, hkv, slot);
+
+  int merged = 0;
+  if (slot >= 0 && a.fused) {
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+    if (tid == 0) misc[0] = (atomicAdd(a.tickets + group, 1) == nsplit - 1);
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+    if (misc[0]) {
+      __threadfence();
+      merge_group(a, tid, b, hkv, slot - split, nsplit);
+      if (tid == 0) a.tickets[group] = 0;
+      merged = 1;
+    }
+  }
+  if (tid == 0) {
+    int32_t* lg = a.cta_log + size_t(blockIdx.x) * kLogFields;
+    lg[0] = p0;
+    lg[1] = p1;
+    lg[2] = misc[1];
+    lg[3] = merged;
+  }
+}
+
+// Copies keys [0, n_keys) of one KV head through the block table with the
+// same tensor-map boxes and swizzled shared-memory addressing as the decode
+// kernel.  One CTA of 128 threads; tiles are loaded one at a time.
+template <bool FP8>
+__global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant__ CUtensorMap tm,
+                                                           const int32_t* table_row, int Hkv,
+                                                           int h_kv, int P, int n_keys,
+                                                           uint8_t* dst, int32_t* status) {
+  constexpr int KT = Gqa<FP8>::KT_BYTES;
+  __shared__ __align__(1024) uint8_t tile[KT];
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int n_tiles = (n_keys + 15) / 16;
+  for (int i = 0; i < n_tiles; ++i) {
+    const int key0 = i * 16;
+    if (threadIdx.x == 0) {
+      const int ph = table_row[key0 / P];
+      const int row = (ph * Hkv + h_kv) * P + key0 % P;
+      mbar_arrive_expect_tx(smem_u32(&bar), KT);
+      tma_load_2d(smem_u32(tile), &tm, smem_u32(&bar), 0, row);
+      if (!FP8) tma_load_2d(smem_u32(tile) + 2048, &tm, smem_u32(&bar), 64, row);
+    }
+    if (!mbar_wait(smem_u32(&bar), i & 1)) {
+      if (threadIdx.x == 0 && status) atomicOr(status, SPLITKV_DEVERR_TIMEOUT);
+      return;
+    }
+    // 16 rows x 16 chunks (bf16) or 8 chunks (fp8) of 16 bytes each
+    constexpr int CH = FP8 ? 8 : 16;
+    for (int x = threadIdx.x; x < 16 * CH; x += blockDim.x) {
+      const int r = x / CH, c = x % CH;
+      if (key0 + r >= n_keys) continue;
+      const uint32_t off = FP8 ? swz(r, c) : swz_bf16(r, c * 8);
+      *reinterpret_cast<uint4*>(dst + (size_t(key0 + r) * CH + c) * 16) =
+          *reinterpret_cast<const uint4*>(tile + off);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv, bool fp8,
+                       void* stream) {
+  const CUtensorMap& mk = *reinterpret_cast<const CUtensorMap*>(&tk);
+  const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(&tv);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.n_items == 0) return cudaSuccess;
+  if (fp8) {
+    auto k = gqa_splitkv_kernel<true>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<true>::SMEM);
+    if (e != cudaSuccess) return e;
+    k<<<a.n_items, Gqa<true>::THREADS, Gqa<true>::SMEM, s>>>(a, mk, mv);
+  } else {
+    auto k = gqa_splitkv_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<false>::SMEM);
+    if (e != cudaSuccess) return e;
+    k<<<a.n_items, Gqa<false>::THREADS, Gqa<false>::SMEM, s>>>(a, mk, mv);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, int row_bytes, const int32_t* table_row,
+                                int32_t rows_per_page_head, int32_t hkv, int32_t h_kv, int32_t P,
+                                int32_t n_keys, void* dst, void* stream) {
+  (void)row_bytes;
+  (void)rows_per_page_head;
+  const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(&t);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* status = nullptr;
+  if (fp8)
+    gather_debug_kernel<true><<<1, 128, 0, s>>>(m, table_row, hkv, h_kv, P, n_keys,
+                                                static_cast<uint8_t*>(dst), status);
+  else
+    gather_debug_kernel<false><<<1, 128, 0, s>>>(m, table_row, hkv, h_kv, P, n_keys,
+                                                 static_cast<uint8_t*>(dst), status);
+  return cudaGetLastError();
+}
+
+}  // namespace splitkv

@@ -1,0 +1,98 @@
+// Internal declarations shared by the planner, the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime_api.h>
+
+#include "splitkv.h"
+
+namespace splitkv {
+
+constexpr int kMaxSplits = 64;     // cap on splits per sequence
+constexpr int kItemOverhead = 32;  // planner: fixed cost of one split CTA, 1/16-page units
+constexpr int kCombineCost = 2;    // planner: merge cost per split, 1/16-page units
+constexpr int kMaxWaves = 8;       // planner: candidate granularities, 1..8 items per SM
+constexpr int kGroupFields = 4;    // {b, h_kv, S_b, first slot}
+constexpr int kLogFields = 4;      // per-CTA log record
+constexpr size_t kAlign = 256;
+
+// Which kernel family serves a descriptor.
+enum class Family { kGqa, kMla, kNone };
+
+Family family_of(const splitkv_desc_t& d);
+
+// Query rows one work item produces: T * G.
+inline int rows_per_item(const splitkv_desc_t& d) {
+  return d.q_tokens * (d.num_q_heads / d.num_kv_heads);
+}
+
+// CTAs launched per work item (1 for GQA; token tiles x CTA pair for MLA).
+int ctas_per_item(const splitkv_desc_t& d);
+
+}  // namespace splitkv
+
+struct splitkv_plan_s {
+  splitkv_desc_t desc;
+  int32_t num_splits = 0;  // as requested (0 = planner's choice)
+  int32_t num_sms = 0;
+  std::vector<int32_t> seq_lens;
+  std::vector<int32_t> items;   // n_items * SPLITKV_ITEM_FIELDS, launch order
+  std::vector<int32_t> groups;  // n_groups * kGroupFields, (b, h_kv) order
+  int32_t n_items = 0, n_groups = 0, n_slots = 0, rows = 0, n_ctas = 0;
+  // workspace byte offsets
+  size_t off_status = 0, off_items = 0, off_groups = 0, off_seqlens = 0, off_tickets = 0;
+  size_t off_log = 0, off_lse = 0, off_o = 0, upload_bytes = 0, total = 0;
+  std::vector<unsigned char> upload;  // host image of [0, upload_bytes)
+};
+
+namespace splitkv {
+
+// Planner (plan.cpp, host only).  Fills items/groups/offsets of `p` from
+// p->desc, p->seq_lens, p->num_splits, p->num_sms.
+void build_plan(splitkv_plan_s* p);
+
+// Thread-local error text (api.cu).
+splitkv_status fail(splitkv_status s, const char* fmt, ...);
+
+// ----------------------------------------------------------------- kernels
+
+struct DecodeArgs {
+  const int32_t* items;
+  const int32_t* groups;
+  const int32_t* plan_lens;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const void* q;
+  void* out;
+  float* lse;
+  float* o_part;
+  float* lse_part;
+  int32_t* tickets;
+  int32_t* cta_log;
+  int32_t* status;
+  int32_t n_items, n_groups;
+  int32_t batch, T, Hq, Hkv, G, P, max_pages, num_pages, rows, dv;
+  float qk_scale_log2;  // scale * kv_scale * log2(e) (x 256 for FP8, see kernel)
+  float o_scale;        // factor applied to the normalised output (FP8: kv_scale * 256)
+  int32_t fused;        // 1: last CTA of a group merges
+};
+
+// Raw 128-byte tensor map storage (CUtensorMap), built by the API layer.
+struct alignas(64) TmaDesc {
+  unsigned char bytes[128];
+};
+
+cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv, bool fp8,
+                       void* stream);
+cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
+cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
+                               int dv, void* out_bf16, float* out_f32, float* lse_out,
+                               void* stream);
+cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, int row_bytes, const int32_t* table_row,
+                                int32_t rows_per_page_head, int32_t hkv, int32_t h_kv,
+                                int32_t P, int32_t n_keys, void* dst, void* stream);
+
+}  // namespace splitkv

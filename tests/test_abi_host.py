@@ -1,0 +1,164 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+* the library loads and exports every function ``include/splitkv.h`` declares;
+* the planner's work list equals the oracle's restatement, exactly;
+* argument validation returns the documented status codes before any CUDA call.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import __graft_entry__
+
+__graft_entry__.build()
+
+import split_kv_paged_splitkv_gb300 as skv  # noqa: E402
+import oracle  # noqa: E402
+import workloads  # noqa: E402
+
+
+def test_library_exports_every_declared_function():
+    names = skv.header_functions()
+    assert "splitkv_decode" in names and "splitkv_plan" in names
+    lib = ctypes.CDLL(skv.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def _desc(B=1, T=1, Hq=16, Hkv=2, D=128, Dv=128, P=16, maxp=512, N=600, fp8=False, mla=False,
+          mode=0):
+    return skv.make_desc(B, T, Hq, Hkv, D, Dv, P, maxp, N,
+                         skv.SPLITKV_FP8_E4M3 if fp8 else skv.SPLITKV_BF16, int(mla), mode)
+
+
+def _oracle_items(lens, P, Hkv, S, sms):
+    return np.array(oracle.plan_items(list(lens), P, Hkv, S, sms), dtype=np.int32).reshape(-1, 6)
+
+
+def _check_plan(lens, P, Hkv, S, sms, Hq=None):
+    Hq = Hq or Hkv * 8 if Hkv * 8 <= 64 else Hkv
+    maxp = max(1, max(-(-int(L) // P) for L in lens))
+    d = _desc(B=len(lens), Hq=Hkv * (8 if Hq is None else Hq // Hkv), Hkv=Hkv, P=P, maxp=maxp,
+              N=max(1, sum(-(-int(L) // P) for L in lens)))
+    plan = skv.splitkv_plan(d, np.array(lens, np.int32), S, sms)
+    items = skv.splitkv_plan_get_items(plan)
+    ref = _oracle_items(lens, P, Hkv, S, sms)
+    assert items.shape[0] == ref.shape[0]
+    assert np.array_equal(items[:, :6], ref), (lens, S)
+    return items
+
+
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16, 32, 64, 0])
+def test_plan_matches_oracle_gqa_ctx5900(S):
+    items = _check_plan([5900], 16, 2, S, 148)
+    n = 369
+    if S:
+        assert items.shape[0] == 2 * min(S, n)
+    assert (items[:, 5] > items[:, 4]).all()
+
+
+@pytest.mark.parametrize("w", ["tiny_gqa_ctx260", "fp8_batch8_ctx32k", "mixed_batch32_bf16",
+                               "mla_t6_ctx64k"])
+@pytest.mark.parametrize("sms", [148, 152])
+def test_plan_matches_oracle_workloads(w, sms):
+    wl = workloads.WORKLOADS[w]
+    lens = workloads.draw_seq_lens(wl, np.random.default_rng(wl.seed))
+    for S in wl.splits:
+        _check_plan(lens, wl.page_size, wl.num_kv_heads, S, sms)
+
+
+def test_plan_matches_oracle_random_batches():
+    rng = np.random.default_rng(123)
+    for trial in range(40):
+        B = int(rng.integers(1, 12))
+        lens = rng.integers(0, 3000, size=B)
+        lens[rng.random(B) < 0.1] = 0
+        P = int(rng.choice([16, 32, 64]))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        S = int(rng.choice([0, 0, 1, 3, 7, 64]))
+        sms = int(rng.choice([1, 7, 148, 152]))
+        _check_plan(list(lens), P, Hkv, S, sms)
+
+
+def test_plan_slots_and_groups_are_consistent():
+    lens = [260, 5900, 16, 0, 1000]
+    d = _desc(B=5, maxp=400, N=1000)
+    plan = skv.splitkv_plan(d, np.array(lens, np.int32), 4, 148)
+    it = skv.splitkv_plan_get_items(plan)
+    for row in it:
+        b, h, s, S, p0, p1, slot, group = row
+        if S == 1:
+            assert slot == -1 and group == -1
+        else:
+            assert slot >= 0 and group >= 0
+    multi = it[it[:, 3] > 1]
+    # slots of one group are contiguous and start at a multiple... each group owns S slots
+    for g in np.unique(multi[:, 7]):
+        rows = multi[multi[:, 7] == g]
+        slots = np.sort(rows[:, 6])
+        assert np.array_equal(slots, np.arange(slots[0], slots[0] + rows[0, 3]))
+        assert np.array_equal(np.sort(rows[:, 2]), np.arange(rows[0, 3]))
+    assert skv.splitkv_workspace_size(plan) > 0
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(P=8), skv.SPLITKV_EINVAL),
+    (dict(Hq=15), skv.SPLITKV_EINVAL),
+    (dict(D=96, Dv=96), skv.SPLITKV_EUNSUPPORTED),
+    (dict(T=2, Hq=16, Hkv=2), skv.SPLITKV_EUNSUPPORTED),  # 2 * 8 rows > 8
+    (dict(N=0), skv.SPLITKV_EINVAL),
+])
+def test_plan_rejects_bad_descriptors(bad, code):
+    d = _desc(**bad)
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(d, np.array([100], np.int32), 1, 148)
+    assert e.value.status == code
+
+
+def test_plan_rejects_bad_lengths_and_splits():
+    d = _desc(maxp=4)
+    for lens, S in (([65], 1), ([-1], 1), ([10], 65), ([10], -1)):
+        with pytest.raises(skv.SplitKVError) as e:
+            skv.splitkv_plan(d, np.array(lens, np.int32), S, 148)
+        assert e.value.status == skv.SPLITKV_EINVAL
+    d2 = _desc(T=4, Hq=8, Hkv=4, maxp=4)
+    with pytest.raises(skv.SplitKVError):
+        skv.splitkv_plan(d2, np.array([3], np.int32), 1, 148)  # shorter than q_tokens
+
+
+def test_decode_validates_before_any_cuda_call():
+    d = _desc()
+    plan = skv.splitkv_plan(d, np.array([100], np.int32), 2, 148)
+    A = 1 << 20  # 16-byte aligned fake addresses; validation fails before use
+    cases = [
+        dict(workspace=None),
+        dict(q=None),
+        dict(q=A + 8),
+        dict(num_splits=3),
+        dict(scale=0.0),
+    ]
+    base = dict(workspace=A, q=A, k=A, v=A, table=A, lens=A, num_splits=2, scale=0.1,
+                kv_scale=1.0, out=A, lse=A)
+    for c in cases:
+        args = dict(base)
+        args.update(c)
+        st = skv._lib.splitkv_decode(plan.handle, args["workspace"], args["q"], args["k"],
+                                     args["v"], args["table"], args["lens"], args["num_splits"],
+                                     args["scale"], args["kv_scale"], args["out"], args["lse"], None)
+        assert st in (skv.SPLITKV_EINVAL, skv.SPLITKV_EWORKSPACE), (c, st)
+        assert skv.splitkv_last_error()
+
+
+def test_upload_checks_workspace_size():
+    d = _desc()
+    plan = skv.splitkv_plan(d, np.array([5900], np.int32), 8, 148)
+    st = skv._lib.splitkv_plan_upload(plan.handle, 1 << 20, 16, None)
+    assert st == skv.SPLITKV_EWORKSPACE
+
+
+def test_combine_validates():
+    st = skv._lib.splitkv_combine(1 << 20, 1 << 20, 0, 4, 128, 1 << 20, None, None, None)
+    assert st == skv.SPLITKV_EINVAL
+    st = skv._lib.splitkv_combine(1 << 20, 1 << 20, 2, 4, 130, 1 << 20, None, None, None)
+    assert st == skv.SPLITKV_EINVAL

@@ -1,0 +1,227 @@
+"""GPU parity of the GQA split-KV path against the fp64 oracle, through the C-ABI.
+
+Bars: max-abs error <= 1e-2 on bf16 outputs and <= 1e-3 on fp32 LSE; split
+tables, per-CTA page ranges and the paged gather must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import split_kv_paged_splitkv_gb300 as skv
+from _support import LSE_TOL, OUT_TOL, compare, need_gpu, oracle_direct, session
+
+pytestmark = pytest.mark.gpu
+W = workloads.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _custom(lens, G=8, Hkv=2, T=1, P=16, fp8=False, seed=7):
+    return workloads.Workload(
+        "custom", len(lens), T, G * Hkv, Hkv, 128, 128, P, "fp8_e4m3" if fp8 else "bf16",
+        "list:" + ":".join(str(int(x)) for x in lens), pool_slack=0.5, seed=seed)
+
+
+# ------------------------------------------------------------------ gather
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("P", [16, 64])
+def test_paged_gather_is_bit_exact(fp8, P):
+    w = _custom([16 * 7 + 5, 3 * P + 1], P=P, fp8=fp8)
+    x = workloads.make_inputs(w, device="cuda")
+    for b in range(2):
+        L = int(x.seq_lens_host[b])
+        for h in range(w.num_kv_heads):
+            for which, pages in (("k", x.k_pages), ("v", x.v_pages)):
+                dst = torch.zeros((L, 128), dtype=pages.dtype, device="cuda")
+                skv.splitkv_debug_gather(skv.make_desc(2, 1, 16, 2, 128, 128, P, x.max_pages,
+                                                       x.num_pages, int(fp8)),
+                                         pages, 128, x.block_table, b, h, L, dst)
+                torch.cuda.synchronize()
+                ref = oracle.gather_keys(workloads.bits(pages), x.block_table[b].cpu().numpy(), L, h)
+                got = workloads.bits(dst)
+                assert np.array_equal(got, ref), (which, b, h)
+
+
+# ------------------------------------------------------------------ workloads 1 and 2
+
+@pytest.mark.parametrize("mode", [skv.SPLITKV_COMBINE_FUSED, skv.SPLITKV_COMBINE_SEPARATE])
+def test_tiny_gqa_ctx260(mode):
+    x = workloads.make_inputs(W["tiny_gqa_ctx260"], device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in (1, 4):
+        s = session(x, S, mode)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"S={S} mode={mode}")
+        log, status = s.stats()
+        assert status == 0
+
+
+@pytest.mark.parametrize("mode", [skv.SPLITKV_COMBINE_FUSED, skv.SPLITKV_COMBINE_SEPARATE])
+def test_gqa_ctx5900_split_sweep(mode):
+    x = workloads.make_inputs(W["gqa_ctx5900"], device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    outs = []
+    for S in W["gqa_ctx5900"].splits:
+        s = session(x, S, mode)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"S={S}")
+        outs.append(out.float().cpu().numpy())
+        log, status = s.stats()
+        assert status == 0
+    # split invariance on the GPU itself
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= OUT_TOL
+
+
+def test_split_ranges_and_nonempty_ctas():
+    """Every launched CTA iterated exactly its planned page range and scored keys."""
+    x = workloads.make_inputs(W["gqa_ctx5900"], device="cuda")
+    for S in (1, 2, 4, 8, 16, 32, 64, 0):
+        s = session(x, S)
+        s.run()
+        log, status = s.stats()
+        items = skv.splitkv_plan_get_items(s.plan)
+        ref = np.array(oracle.plan_items(list(x.seq_lens_host), 16, 2, S, _sms()), np.int32)
+        assert np.array_equal(items[:, :6], ref)
+        assert np.array_equal(log[:, 0], items[:, 4]) and np.array_equal(log[:, 1], items[:, 5])
+        n_pages = 369
+        expect_keys = np.minimum(items[:, 5] * 16, 5900) - items[:, 4] * 16
+        assert np.array_equal(log[:, 2], expect_keys)
+        assert (log[:, 2] > 0).all()  # non-empty fraction = 1.0
+        if S:
+            assert len(items) == 2 * min(S, n_pages)
+        assert status == 0
+        # exactly one merging CTA per (b, h_kv) group when split
+        if (items[:, 3] > 1).any():
+            assert log[:, 3].sum() == len(np.unique(items[items[:, 3] > 1][:, 7]))
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+# ------------------------------------------------------------------ ragged and edge cases
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("G,Hkv", [(8, 2), (4, 2), (1, 3), (2, 1)])
+@pytest.mark.parametrize("P", [16, 64])
+def test_ragged_lengths(fp8, G, Hkv, P):
+    lens = [1, 15, 16, 17, 255, 257, 1000, 0, 3 * P, 2 * P + 1]
+    w = _custom(lens, G=G, Hkv=Hkv, P=P, fp8=fp8, seed=G * 10 + Hkv + P)
+    x = workloads.make_inputs(w, device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in (1, 3, 0):
+        for mode in (0, 1):
+            s = session(x, S, mode)
+            out, lse = s.run()
+            compare(out, lse, ref_o, ref_l, what=f"S={S} mode={mode}")
+            log, status = s.stats()
+            assert status == 0
+            items = skv.splitkv_plan_get_items(s.plan)
+            nonempty = items[:, 5] > items[:, 4]
+            assert (log[nonempty, 2] > 0).all()
+
+
+@pytest.mark.parametrize("T,G", [(2, 4), (8, 1), (4, 2), (3, 2)])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_multi_token_causal(T, G, fp8):
+    lens = [T, T + 1, 37, 300, 16 * 5]
+    w = _custom(lens, G=G, Hkv=2, T=T, fp8=fp8, seed=T * 7 + G)
+    x = workloads.make_inputs(w, device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in (1, 2, 5):
+        out, lse = session(x, S).run()
+        compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} S={S}")
+
+
+# ------------------------------------------------------------------ workloads 3 and 5
+
+def test_fp8_batch8_ctx32k_full():
+    x = workloads.make_inputs(W["fp8_batch8_ctx32k"], device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for mode in (0, 1):
+        s = session(x, 0, mode)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"mode={mode}")
+        log, status = s.stats()
+        assert status == 0 and (log[:, 2] > 0).all()
+
+
+@pytest.mark.parametrize("name", ["mixed_batch32_bf16", "mixed_batch32_fp8"])
+def test_mixed_batch32_sampled(name):
+    """Full-size run; the oracle checks every head of 5 sequences (longest,
+    shortest and three seeded picks)."""
+    w = W[name]
+    x = workloads.make_inputs(w, device="cuda")
+    s = session(x, 0)
+    out, lse = s.run()
+    log, status = s.stats()
+    assert status == 0 and (log[:, 2] > 0).all()
+    lens = x.seq_lens_host
+    rng = np.random.default_rng(5)
+    picks = sorted({int(np.argmax(lens)), int(np.argmin(lens)), *rng.choice(w.batch, 3, replace=False).tolist()})
+    rows = [(b, 0, h) for b in picks for h in range(w.num_q_heads)]
+    ref_o, ref_l = oracle_direct(x, rows=rows)
+    compare(out, lse, ref_o, ref_l, rows=rows, what=name)
+
+
+# ------------------------------------------------------------------ combine
+
+def test_combine_matches_oracle_and_is_associative():
+    rng = np.random.default_rng(3)
+    S, R, D = 5, 7, 128
+    o = rng.standard_normal((S, R, D)).astype(np.float32)
+    l = (rng.standard_normal((S, R)) * 4).astype(np.float32)
+    l[1, 2] = -np.inf
+    l[:, 5] = -np.inf  # an all-empty row
+    od = torch.from_numpy(o).cuda()
+    ld = torch.from_numpy(l).cuda()
+
+    def comb(o_, l_):
+        n = o_.shape[0]
+        out = torch.empty((R, D), dtype=torch.float32, device="cuda")
+        lo = torch.empty(R, dtype=torch.float32, device="cuda")
+        skv.splitkv_combine(o_.contiguous(), l_.contiguous(), n, R, D, None, out, lo)
+        return out, lo
+
+    full_o, full_l = comb(od, ld)
+    torch.cuda.synchronize()
+    for r in range(R):
+        ro, rl = oracle.combine([(o[s, r].astype(np.float64), float(l[s, r])) for s in range(S)])
+        assert np.abs(full_o[r].cpu().numpy() - ro).max() < 1e-5
+        if np.isfinite(rl):
+            assert abs(full_l[r].item() - rl) < 1e-5
+        else:
+            assert full_l[r].item() == -np.inf and (full_o[r] == 0).all()
+    # ((0,1),2,3,4) == (0,1,2,3,4) and permutation invariance
+    a_o, a_l = comb(od[:2], ld[:2])
+    left_o, left_l = comb(torch.cat([a_o[None], od[2:]]), torch.cat([a_l[None], ld[2:]]))
+    perm = [3, 0, 4, 2, 1]
+    p_o, p_l = comb(od[perm], ld[perm])
+    fin = torch.isfinite(full_l)
+    for oo, ll in ((left_o, left_l), (p_o, p_l)):
+        assert (oo - full_o).abs().max().item() < 1e-5
+        assert (ll[fin] - full_l[fin]).abs().max().item() < 1e-5
+    # -inf partial is the identity
+    e_o, e_l = comb(torch.cat([od[:1], torch.zeros_like(od[:1])]),
+                    torch.cat([ld[:1], torch.full_like(ld[:1], -np.inf)]))
+    one_o, one_l = comb(od[:1], ld[:1])
+    assert (e_o - one_o).abs().max().item() == 0 and torch.equal(e_l, one_l)
+
+
+# ------------------------------------------------------------------ status word
+
+def test_seq_len_mismatch_is_reported():
+    x = workloads.make_inputs(W["tiny_gqa_ctx260"], device="cuda")
+    s = session(x, 4)
+    wrong = x.seq_lens.clone()
+    wrong[0] -= 3
+    s.run(tensors=(x.q, x.k_pages, x.v_pages, x.block_table, wrong))
+    _, status = s.stats()
+    assert status & skv.SPLITKV_DEVERR_SEQLEN
