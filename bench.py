@@ -1,0 +1,421 @@
+"""Benchmark: µs per split-KV decode-attention call on one GB300 (or N replicas).
+
+Default workload: long single-stream GQA decode -- batch 1, one query token,
+16 query / 2 KV heads, head dim 128, context 5,900, BF16 KV in 16-token pages
+behind a shuffled block table, split count chosen by the planner.  ("vLLM
+0.30.0 FA4 SplitKV Bug: H100 Decode Can Be 48% Slower": the ~5.9k-context
+global-layer decode with two KV heads.)
+
+Protocol
+  * One step = one ``splitkv_decode`` call (all kernels of the path) over one
+    batch.  Steps are captured in CUDA graphs and replayed; the timed region
+    is bracketed by a barrier and ``torch.cuda.synchronize()`` and timed with
+    CUDA events on the launching stream.
+  * The KV inputs rotate over R copies of the page pool whose total exceeds 4x
+    the L2 size, so no step starts with its pages in L2.
+  * ``value`` = timed-region time / steps (whole-job: / (steps x ranks)).
+  * ``roofline``: algorithmic bytes of one launch of the split-KV kernel (KV
+    bytes of the visible keys + Q bytes) / its average launch duration,
+    against the measured HBM copy bandwidth.  With the fused combine the
+    kernel is the only launch of a step, so its average duration is taken as
+    timed-region time / launches (this includes inter-launch gaps and so
+    understates the kernel's own bandwidth).
+  * ``e2e``: the same call with host buffers -- pinned-host -> device copies
+    of every input, the decode, and device -> host copies of out and lse,
+    all inside the timed region.
+  * ``cpu_baseline``: the fp64 oracle, single-threaded, on a bounded sample.
+  * Clocks: ``nvidia-smi`` samples every 200 ms while the same work runs
+    (a >= 1 s soak immediately followed by the timed region).
+
+``--impl reference`` times the fp64 CPU oracle on the same workload (the
+reference arm: the pages ship no code of their own).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "µs per decode-attention call; achieved HBM GB/s as fraction of GB300 peak"
+NORTH_STAR_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa_ctx5900", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--splits", type=int, default=0, help="num_splits (0 = planner)")
+    ap.add_argument("--combine", default="fused", choices=["fused", "separate"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- helpers
+
+def algorithmic_bytes(w: workloads.Workload, lens: np.ndarray) -> int:
+    """KV bytes of the visible keys plus Q bytes of one call."""
+    elt = 1 if w.kv_dtype == "fp8_e4m3" else 2
+    row = w.qk_dim * elt + (0 if w.v_shares_k else w.v_dim * elt)
+    kv = int(lens.astype(np.int64).sum()) * w.num_kv_heads * row
+    q = w.batch * w.q_tokens * w.num_q_heads * w.qk_dim * 2
+    return kv + q
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def time_oracle(w, x, seconds, threads=1):
+    """Runs the oracle on the full call repeatedly in a clean single-threaded
+    subprocess; returns (µs per call, calls)."""
+    import pickle
+    payload = dict(q=workloads.bits(x.q), k=workloads.bits(x.k_pages),
+                   v=None if x.v_pages is None else workloads.bits(x.v_pages),
+                   table=x.block_table.cpu().numpy(), lens=x.seq_lens_host, scale=x.scale,
+                   kv_dtype=w.kv_dtype, kv_scale=x.kv_scale, v_dim=w.v_dim,
+                   v_shares_k=w.v_shares_k, seconds=seconds)
+    with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
+        pickle.dump(payload, f)
+        path = f.name
+    code = (
+        "import pickle, sys, time, json\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import oracle\n"
+        f"d = pickle.load(open({path!r}, 'rb'))\n"
+        "n = 0; t0 = time.perf_counter()\n"
+        "while True:\n"
+        "    oracle.attention_direct(d['q'], d['k'], d['v'], d['table'], d['lens'], scale=d['scale'],\n"
+        "        kv_dtype=d['kv_dtype'], kv_scale=d['kv_scale'], v_dim=d['v_dim'], v_shares_k=d['v_shares_k'])\n"
+        "    n += 1\n"
+        "    if time.perf_counter() - t0 >= d['seconds']: break\n"
+        "print(json.dumps({'us': (time.perf_counter() - t0) / n * 1e6, 'n': n}))\n")
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    os.unlink(path)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["us"], d["n"]
+
+
+def oracle_sample_desc(w, n):
+    return (f"fp64 oracle (numpy, 1 thread) on the full {w.name} call "
+            f"({w.batch} seq x {w.num_q_heads} q heads x {w.lens} keys), repeated {n} times")
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w, device="cpu")
+    # Each step is one full oracle call; the run is bounded by --cpu-seconds
+    # (so at most --steps calls, at least one).
+    per_call, _ = time_oracle(w, x, 0.0)
+    steps = max(1, min(args.steps, int(args.cpu_seconds * 1e6 / max(per_call, 1.0))))
+    warm = 1
+    us, n = time_oracle(w, x, steps * per_call / 1e6)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
+        "steps": n, "warmup": warm, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
+                         "sample": oracle_sample_desc(w, n)},
+        "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import split_kv_paged_splitkv_gb300 as skv
+    from split_kv_paged_splitkv_gb300.runner import DecodeSession
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w, device=dev)
+    mode = skv.SPLITKV_COMBINE_FUSED if args.combine == "fused" else skv.SPLITKV_COMBINE_SEPARATE
+    # Everything runs on torch's current stream: graphs are captured on a side
+    # stream by torch.cuda.graph and replayed on the current stream.
+    sess = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
+                         scale=x.scale, kv_scale=x.kv_scale, num_splits=args.splits,
+                         v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode)
+    items = skv.splitkv_plan_get_items(sess.plan)
+    n_groups = len(np.unique(items[items[:, 3] > 1][:, 7])) if len(items) else 0
+    launches_per_step = 1 + (1 if (mode == skv.SPLITKV_COMBINE_SEPARATE and n_groups) else 0)
+
+    # rotating KV pools: total > 4x L2
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    pool_bytes = x.k_pages.numel() * x.k_pages.element_size() + (
+        0 if x.v_pages is None else x.v_pages.numel() * x.v_pages.element_size())
+    R = max(2, min(256, math.ceil(4 * l2 / pool_bytes)))
+    pools = [(x.k_pages.clone(), None if x.v_pages is None else x.v_pages.clone()) for _ in range(R - 1)]
+    pools.insert(0, (x.k_pages, x.v_pages))
+
+    def step(i):
+        k, v = pools[i % R]
+        sess.run(tensors=(x.q, k, v, x.block_table, x.seq_lens))
+
+    # eager warm-up (also sets up per-process kernel attributes before capture)
+    for i in range(max(3, min(args.warmup, R))):
+        step(i)
+    torch.cuda.synchronize()
+    log, status = sess.stats()
+    assert status == 0, f"device status {status}"
+    nonempty = float((log[:, 2] > 0).mean()) if len(log) else 1.0
+
+    def capture(n, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(start + i)
+        return g
+
+    cycle = capture(R, 0)
+    K = args.steps
+    reps, rem = divmod(K, R)
+    tail = capture(rem, 0) if rem else None
+
+    # graph warm-up + clock soak (same work), then the timed region
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(1, math.ceil(args.warmup / R))):
+        cycle.replay()
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + args.soak_seconds
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            cycle.replay()
+        torch.cuda.synchronize()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(reps):
+        cycle.replay()
+    if tail is not None:
+        tail.replay()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms_local, world)
+    us_per_call_local = ms_local * 1e3 / K
+    value = ms * 1e3 / (K * world)
+
+    log, status = sess.stats()
+    assert status == 0, f"device status {status} after the timed region"
+
+    # roofline of the split-KV kernel
+    nbytes = algorithmic_bytes(w, x.seq_lens_host)
+    peak, peak_kind = measured_peaks()
+    if launches_per_step == 1:
+        launch_us = us_per_call_local
+    else:
+        launch_us = None
+    achieved = nbytes / (launch_us * 1e-6) / 1e9 if launch_us else None
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = run_e2e(args, x, sess, dev)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "us", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "q_tokens": w.q_tokens,
+                   "heads_q_kv": [w.num_q_heads, w.num_kv_heads], "head_dim": w.qk_dim,
+                   "context": w.lens, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+                   "num_splits": args.splits, "planned_items": int(len(items)),
+                   "combine": args.combine, "parallelism": f"replicas{world}",
+                   "l2": f"inputs rotate over {R} KV pools ({R * pool_bytes / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA-graph replay of back-to-back calls, CUDA events on the launching stream"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "peak_kind": peak_kind, "algorithmic_bytes": nbytes,
+                     "kernel": "gqa_splitkv_kernel",
+                     "frac_of_8tbs": (achieved / NORTH_STAR_HBM_GBS) if achieved else None},
+        "nonempty_cta_fraction": nonempty,
+        "gpu_launches": K * launches_per_step,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, n = time_oracle(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
+                                "sample": oracle_sample_desc(w, n)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, x, sess, dev):
+    """Pinned host inputs -> device, decode, out/lse -> pinned host, per step."""
+    host_in = [t.cpu().pin_memory() for t in (x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens)
+               if t is not None]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    out_h = torch.empty(sess.out.shape, dtype=sess.out.dtype).pin_memory()
+    lse_h = torch.empty(sess.lse.shape, dtype=sess.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        if x.v_pages is None:
+            q, k, table, lens = dev_in
+            v = None
+        else:
+            q, k, v, table, lens = dev_in
+        out, lse = sess.run(tensors=(q, k, v, table, lens))
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.e2e_steps
+    return {"value": us, "unit": "us", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": args.e2e_steps}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

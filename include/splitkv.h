@@ -182,7 +182,8 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace,
  * of a row is -inf the row gets out = 0, lse = -inf.
  *   o_part    fp32 [n_parts][rows][dv]      lse_part  fp32 [n_parts][rows]
  *   out_bf16  bf16 [rows][dv] or NULL       out_f32   fp32 [rows][dv] or NULL
- *   lse_out   fp32 [rows] or NULL           dv a multiple of 4, <= 1024
+ *   lse_out   fp32 [rows] or NULL
+ *   n_parts in [1, 1024]; dv a power of two in [4, 512]
  */
 splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32_t n_parts,
                                int32_t rows, int32_t dv, void* out_bf16, float* out_f32,

@@ -262,8 +262,10 @@ splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32
                                int32_t rows, int32_t dv, void* out_bf16, float* out_f32,
                                float* lse_out, void* stream) {
   if (!o_part || !lse_part) return fail(SPLITKV_EINVAL, "o_part and lse_part must not be NULL");
-  if (n_parts < 1 || rows < 0) return fail(SPLITKV_EINVAL, "n_parts must be >= 1, rows >= 0");
-  if (dv < 4 || dv % 4 || dv > 1024) return fail(SPLITKV_EINVAL, "dv must be a multiple of 4 in [4, 1024]");
+  if (n_parts < 1 || n_parts > 1024 || rows < 0)
+    return fail(SPLITKV_EINVAL, "n_parts must be in [1, 1024] and rows >= 0");
+  if (dv < 4 || dv > 512 || (dv & (dv - 1)))
+    return fail(SPLITKV_EINVAL, "dv must be a power of two in [4, 512]");
   if (!out_bf16 && !out_f32 && !lse_out) return fail(SPLITKV_EINVAL, "no output given");
   if (!aligned16(o_part) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && (reinterpret_cast<uintptr_t>(out_bf16) & 7u)))

@@ -38,20 +38,36 @@ namespace {
 
 using namespace ptx;
 
+// A tile is 16 keys of one KV head: its K rows then its V rows.  A stage --
+// the unit one mbarrier phase covers -- is TPS tiles (32 KB either way).
+// Measured on GB300, one CTA keeps only about one stage's worth of TMA boxes
+// (~32 KB) in flight however deep its ring is, so per-SM bandwidth comes from
+// several CTAs per SM: a small ring (two stages) and 160 threads let three
+// CTAs share an SM.
 template <bool FP8>
 struct Gqa {
   static constexpr int D = 128;
   static constexpr int TK = 16;                            // keys per tile
   static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one K (or V) tile
-  static constexpr int STAGE = 2 * KT_BYTES;
-  static constexpr int NST = FP8 ? 16 : 8;  // 64 KB ring either way
-  static constexpr int NCW = 4;             // consumer warps
+  static constexpr int TILE = 2 * KT_BYTES;                // K + V of one tile
+  static constexpr int TPS = FP8 ? 8 : 4;                  // tiles per stage
+  static constexpr int STAGE = TPS * TILE;                 // 32 KB
+  static constexpr int NST = 2;                            // stages in the ring
+  static constexpr int NCW = 4;                            // consumer warps
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int RING = NST * STAGE;
   static constexpr int MERGE = NCW * 8 * D * 4 + NCW * 8 * 2 * 4;
-  static_assert(MERGE <= RING, "merge area aliases the ring");
+  static_assert(MERGE + 64 * 8 * 4 <= RING, "merge area and staged LSEs alias the ring");
+  // Warp w takes tiles w, w + NCW, ...: its successive visits to one stage
+  // must be exactly one barrier phase apart (parity waits cannot tell phase k
+  // from k + 2).  That holds when a warp visits every stage in turn (TPS a
+  // multiple of NCW) or steps NCW / TPS stages at a time with that step
+  // dividing NST.
+  static_assert((TPS % NCW == 0) || (NCW % TPS == 0 && NST % (NCW / TPS) == 0),
+                "stage/warp aliasing");
   static constexpr int BARS = 2 * NST * 8;
-  static constexpr int SMEM = 1024 + RING + BARS + 64;
+  static constexpr int PT_CHUNK = 1024;  // block-table entries staged at a time
+  static constexpr int SMEM = 1024 + RING + BARS + 64 + PT_CHUNK * 4;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,106 +84,138 @@ __device__ __forceinline__ uint32_t swz_bf16(int row, int d) {
   return static_cast<uint32_t>((d >> 6) * 2048) + swz(row, (d & 63) >> 3);
 }
 
+// Sums DPT consecutive floats of `x` (DPT a multiple of 4) into `acc` with weight w.
+template <int DPT>
+__device__ __forceinline__ void axpy(float (&acc)[DPT], float w, const float* x) {
+#pragma unroll
+  for (int i = 0; i < DPT; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(x + i);
+    acc[i] += w * v.x; acc[i + 1] += w * v.y; acc[i + 2] += w * v.z; acc[i + 3] += w * v.w;
+  }
+}
+
+// Writes DPT outputs of one query row: bf16 to `out` or fp32 to `dst`.
+template <int DPT>
+__device__ __forceinline__ void store_row(const float (&acc)[DPT], __nv_bfloat16* out, float* dst) {
+#pragma unroll
+  for (int i = 0; i < DPT; i += 4) {
+    if (out) {
+      uint2 v;
+      v.x = pack_bf16(acc[i], acc[i + 1]);
+      v.y = pack_bf16(acc[i + 2], acc[i + 3]);
+      *reinterpret_cast<uint2*>(out + i) = v;
+    } else {
+      *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+    }
+  }
+}
+
 // Merges the (m, l, O) of the consumer warps and writes the item's result.
-// Runs on the 128 consumer threads; `mo` is [NCW][8][128] fp32, `mm`/`ml`
-// [NCW][8].  m is in log2 units.
+// Runs on the NT consumer threads: row n = tid / (NT / 8), DPT = 1024 / NT
+// consecutive dims from d0.  `mo` is [NCW][8][128] fp32, `mm`/`ml` [NCW][8];
+// m is in log2 units.
 template <bool FP8>
 __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, const float* mo,
                                                 const float* mm, const float* ml, int b, int hkv,
                                                 int slot) {
-  constexpr int NCW = Gqa<FP8>::NCW;
-  const int n = tid >> 4;          // query row 0..7
-  const int d0 = (tid & 15) * 8;   // 8 consecutive dims
+  constexpr int NCW = Gqa<FP8>::NCW, NT = NCW * 32, TPR = NT / 8, DPT = 128 / TPR;
+  const int n = tid / TPR;           // query row 0..7
+  const int d0 = (tid % TPR) * DPT;  // first of DPT consecutive dims
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < NCW; ++w) M = fmaxf(M, mm[w * 8 + n]);
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float acc[DPT];
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
   float lsum = 0.f;
   if (M != -INFINITY) {
 #pragma unroll
     for (int w = 0; w < NCW; ++w) {
       const float sc = ex2(mm[w * 8 + n] - M);
       lsum += sc * ml[w * 8 + n];
-      const float4* src = reinterpret_cast<const float4*>(mo + (w * 8 + n) * 128 + d0);
-      const float4 x0 = src[0], x1 = src[1];
-      acc[0] += sc * x0.x; acc[1] += sc * x0.y; acc[2] += sc * x0.z; acc[3] += sc * x0.w;
-      acc[4] += sc * x1.x; acc[5] += sc * x1.y; acc[6] += sc * x1.z; acc[7] += sc * x1.w;
+      axpy<DPT>(acc, sc, mo + (w * 8 + n) * 128 + d0);
     }
   }
-  float lse_n;
-  if (lsum > 0.f) {
-    const float inv = a.o_scale / lsum;
+  float lse_n = -INFINITY;
+  const float inv = lsum > 0.f ? a.o_scale / lsum : 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] *= inv;
-    lse_n = (M + lg2(lsum)) * kLn2;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    lse_n = -INFINITY;
-  }
+  for (int i = 0; i < DPT; ++i) acc[i] *= inv;
+  if (lsum > 0.f) lse_n = (M + lg2(lsum)) * kLn2;
   if (n >= a.rows) return;
   if (slot < 0) {
     const int t = n / a.G, g = n - (n / a.G) * a.G;
     const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g;
-    uint4 v;
-    v.x = pack_bf16(acc[0], acc[1]);
-    v.y = pack_bf16(acc[2], acc[3]);
-    v.z = pack_bf16(acc[4], acc[5]);
-    v.w = pack_bf16(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0) = v;
+    store_row<DPT>(acc, static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0, nullptr);
     if (d0 == 0 && a.lse) a.lse[row] = lse_n;
   } else {
-    float* dst = a.o_part + (size_t(slot) * a.rows + n) * 128 + d0;
-    reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    store_row<DPT>(acc, nullptr, a.o_part + (size_t(slot) * a.rows + n) * 128 + d0);
     if (d0 == 0) a.lse_part[size_t(slot) * a.rows + n] = lse_n;
   }
 }
 
 // Log-sum-exp merge of the S partials of one (b, h_kv) group, by the CTA that
-// finished last.  128 threads: row n = tid / 16, dims d0 .. d0+7.
+// finished last.  NT threads.  The S x rows LSE values are first staged in
+// shared memory (`sl`, [S][8]) by all threads at once; then thread (row n,
+// DPT dims from d0) accumulates the weighted partials with U splits' loads in
+// flight per step, so the L2 round trips overlap instead of serialising one
+// per split.
+template <int NT>
 __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int hkv,
-                                            int slot0, int S) {
-  const int n = tid >> 4;
-  const int d0 = (tid & 15) * 8;
-  if (n >= a.rows) return;
-  const float* lp = a.lse_part + size_t(slot0) * a.rows + n;
+                                            int slot0, int S, float* sl) {
+  constexpr int TPR = NT / 8, DPT = 128 / TPR, U = 8;
+  const int rows = a.rows;
+  for (int i = tid; i < S * 8; i += NT) {
+    const int s = i >> 3, n = i & 7;
+    sl[i] = n < rows ? __ldcg(a.lse_part + size_t(slot0 + s) * rows + n) : -INFINITY;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  const int n = tid / TPR;
+  const int d0 = (tid % TPR) * DPT;
+  if (n >= rows) return;
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(lp + size_t(s) * a.rows));
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int s = 0; s < S; ++s) M = fmaxf(M, sl[s * 8 + n]);
+  float acc[DPT];
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float w = ex2((__ldcg(lp + size_t(s) * a.rows) - M) * kLog2e);
-      if (w == 0.f) continue;
-      wsum += w;
-      const float4* src =
-          reinterpret_cast<const float4*>(a.o_part + (size_t(slot0 + s) * a.rows + n) * 128 + d0);
-      const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-      acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-      acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+    const size_t stride = size_t(rows) * 128;
+    const float* base = a.o_part + (size_t(slot0) * rows + n) * 128 + d0;
+    for (int s0 = 0; s0 < S; s0 += U) {
+      float4 x[U][DPT / 4];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < DPT / 4; ++v)
+          if (s0 + u < S)
+            x[u][v] = __ldcg(reinterpret_cast<const float4*>(base + size_t(s0 + u) * stride) + v);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (s0 + u < S) {
+          const float w = ex2((sl[(s0 + u) * 8 + n] - M) * kLog2e);
+          wsum += w;
+#pragma unroll
+          for (int v = 0; v < DPT / 4; ++v) {
+            acc[4 * v] += w * x[u][v].x; acc[4 * v + 1] += w * x[u][v].y;
+            acc[4 * v + 2] += w * x[u][v].z; acc[4 * v + 3] += w * x[u][v].w;
+          }
+        }
+      }
     }
   }
   float lse_n = -INFINITY;
-  if (wsum > 0.f) {
-    const float inv = 1.f / wsum;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] *= inv;
-    lse_n = M + lg2(wsum) * kLn2;
-  }
+  for (int i = 0; i < DPT; ++i) acc[i] *= inv;
+  if (wsum > 0.f) lse_n = M + lg2(wsum) * kLn2;
   const int t = n / a.G, g = n - (n / a.G) * a.G;
   const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g;
-  uint4 v;
-  v.x = pack_bf16(acc[0], acc[1]);
-  v.y = pack_bf16(acc[2], acc[3]);
-  v.z = pack_bf16(acc[4], acc[5]);
-  v.w = pack_bf16(acc[6], acc[7]);
-  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0) = v;
+  store_row<DPT>(acc, static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0, nullptr);
   if (d0 == 0 && a.lse) a.lse[row] = lse_n;
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
+__global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
     gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
   using C = Gqa<FP8>;
@@ -177,6 +225,7 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::RING);
   uint64_t* empty = full + C::NST;
   int* misc = reinterpret_cast<int*>(empty + C::NST);  // [0] merge flag, [1] keys scored
+  int* pt = misc + 16;                                 // staged block-table entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* it = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
@@ -184,77 +233,101 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
   const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
   const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
   const int slot = it[SPLITKV_ITEM_SLOT], group = it[SPLITKV_ITEM_GROUP];
-  const int L = a.seq_lens[b];
-  const int k_begin = p0 * a.P;
-  const int k_end = min(p1 * a.P, L);
-  const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
 
+  // Prologue: only shared memory, the tensor maps and the uploaded work list,
+  // so it may overlap the previous kernel on the stream (programmatic
+  // dependent launch).  Everything a previous kernel may write -- the caller's
+  // inputs and this workspace's partials and tickets -- is touched only after
+  // griddepcontrol.wait.
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 1);
+      mbar_init(smem_u32(empty + s), C::TPS);  // one arrival per consumed tile
     }
     misc[0] = 0;
     misc[1] = 0;
     fence_mbar_init();
-    if (a.plan_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
+  }
+  if (warp == C::NCW && lane == 0) {
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
   }
   __syncthreads();
   launch_dependents();
+  wait_prerequisites();
+
+  const int L = a.seq_lens[b];
+  const int k_begin = p0 * a.P;
+  const int k_end = min(p1 * a.P, L);
+  const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
+  if (threadIdx.x == 0 && a.plan_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
 
   if (warp == C::NCW) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-    }
+    // The warp stages up to PT_CHUNK physical page ids of this item in shared
+    // memory (coalesced loads); then lane 0 alone walks the tiles, arming each
+    // stage's barrier and issuing the tile boxes.
     const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
     const int pg_end = (k_end + a.P - 1) / a.P;
     const int tiles_per_page = a.P >> 4;
-    int tile = 0;
+    int stages = 0, t = 0;
     bool ok = true;
-    for (int pc = p0; pc < pg_end && ok; pc += 32) {
-      const int my = pc + lane;
-      int phys = 0;
-      if (my < pg_end) {
-        phys = __ldg(trow + my);
-        if (phys < 0 || phys >= a.num_pages) {
+    for (int pc = p0; pc < pg_end && ok; pc += C::PT_CHUNK) {
+      const int cnt = min(C::PT_CHUNK, pg_end - pc);
+      __syncwarp();
+      for (int x = lane; x < cnt; x += 32) {
+        int ph = __ldg(trow + pc + x);
+        if (ph < 0 || ph >= a.num_pages) {
           atomicOr(a.status, SPLITKV_DEVERR_PAGE);
-          phys = 0;
+          ph = 0;
         }
+        pt[x] = ph;
       }
-      const int cnt = min(32, pg_end - pc);
-      for (int j = 0; j < cnt && ok; ++j) {
-        const int ph = __shfl_sync(kFull, phys, j);
-        const int key_page = (pc + j) * a.P;
-        for (int sub = 0; sub < tiles_per_page; ++sub) {
-          if (key_page + sub * 16 >= k_end) break;
-          if (lane == 0) {
-            const int st = tile % C::NST;
-            if (tile >= C::NST && !mbar_wait(smem_u32(empty + st), ((tile / C::NST) - 1) & 1)) {
+      __syncwarp();
+      if (lane == 0) {
+        const int t_end = min(n_tiles, (pc + cnt) * tiles_per_page - p0 * tiles_per_page);
+        for (; t < t_end; ++t) {
+          const int key0 = k_begin + t * 16;
+          const int page = key0 / a.P;
+          const int ph = pt[page - pc];
+          const int j = t / C::TPS, u = t - j * C::TPS, st = j % C::NST;
+          const uint32_t bar = smem_u32(full + st);
+          if (u == 0) {
+            if (j >= C::NST && !mbar_wait(smem_u32(empty + st), ((j / C::NST) - 1) & 1)) {
               atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
               ok = false;
+              break;
             }
-            if (ok) {
-              const uint32_t bar = smem_u32(full + st);
-              const uint32_t dk = smem_u32(ring + st * C::STAGE);
-              const uint32_t dv = dk + C::KT_BYTES;
-              const int row = (ph * a.Hkv + hkv) * a.P + sub * 16;
-              mbar_arrive_expect_tx(bar, C::STAGE);
-              if (FP8) {
-                tma_load_2d(dk, &tk, bar, 0, row);
-                tma_load_2d(dv, &tv, bar, 0, row);
-              } else {
-                tma_load_2d(dk, &tk, bar, 0, row);
-                tma_load_2d(dk + 2048, &tk, bar, 64, row);
-                tma_load_2d(dv, &tv, bar, 0, row);
-                tma_load_2d(dv + 2048, &tv, bar, 64, row);
-              }
-            }
+            mbar_arrive_expect_tx(bar, min(C::TPS, n_tiles - t) * C::TILE);
+            stages = j + 1;
           }
-          ok = __shfl_sync(kFull, ok, 0);
-          if (!ok) break;
-          ++tile;
+          const uint32_t dk = smem_u32(ring + st * C::STAGE + u * C::TILE);
+          const uint32_t dv = dk + C::KT_BYTES;
+          const int row = (ph * a.Hkv + hkv) * a.P + (key0 - page * a.P);
+          if (FP8) {
+            tma_load_2d(dk, &tk, bar, 0, row);
+            tma_load_2d(dv, &tv, bar, 0, row);
+          } else {
+            tma_load_2d(dk, &tk, bar, 0, row);
+            tma_load_2d(dk + 2048, &tk, bar, 64, row);
+            tma_load_2d(dv, &tv, bar, 0, row);
+            tma_load_2d(dv + 2048, &tv, bar, 64, row);
+          }
+        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+      t = __shfl_sync(kFull, t, 0);
+    }
+    // Stay resident until every issued copy has landed: the CTA must not exit
+    // (and free its shared memory) with TMA writes in flight, even when a
+    // consumer gave up on a timed-out wait.  Normally these waits return at
+    // once, since the consumers have already seen the same phases complete.
+    if (lane == 0) {
+      for (int st = 0; st < C::NST && st < stages; ++st) {
+        const int last = st + C::NST * ((stages - 1 - st) / C::NST);
+        if (!mbar_wait(smem_u32(full + st), (last / C::NST) & 1)) {
+          atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+          break;
         }
       }
     }
@@ -262,7 +335,7 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
   }
 
   // ------------------------------------------------------------------ consumers
-  const int tid = threadIdx.x;  // 0 .. 127
+  const int tid = threadIdx.x;  // consumer threads 0 .. NCW*32-1
   const int gi = lane >> 2, ti = lane & 3;
 
   // Q^T operand fragments: row n = gi, dims by ti (see the layout notes).
@@ -308,13 +381,13 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
   int keys_scored = 0;
 
   for (int i = warp; i < n_tiles; i += C::NCW) {
-    const int st = i % C::NST;
-    const bool arrived = __all_sync(kFull, mbar_wait(smem_u32(full + st), (i / C::NST) & 1));
+    const int j = i / C::TPS, st = j % C::NST;
+    const bool arrived = __all_sync(kFull, mbar_wait(smem_u32(full + st), (j / C::NST) & 1));
     if (!arrived) {
       if (lane == 0) atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
       break;
     }
-    uint8_t* kt = ring + st * C::STAGE;
+    uint8_t* kt = ring + st * C::STAGE + (i - j * C::TPS) * C::TILE;
     uint8_t* vt = kt + C::KT_BYTES;
     const int key0 = k_begin + i * 16;
     const int valid = min(16, k_end - key0);
@@ -334,30 +407,35 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
       __syncwarp();
     }
 
-    // ---- S^T = K . Q^T
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T = K . Q^T (two accumulator chains: even and odd k-steps)
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t kbase = smem_u32(kt);
     const int mi = lane >> 3, mr = lane & 7;
     if (!FP8) {
       const int krow = (mi & 1) * 8 + mr;
+      uint32_t af[8][4];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4];
-        ldsm_x4(kbase + swz_bf16(krow, ks * 16 + (mi >> 1) * 8), af);
-        mma_bf16(sc, af, qf[ks][0], qf[ks][1]);
+      for (int ks = 0; ks < 8; ++ks) ldsm_x4(kbase + swz_bf16(krow, ks * 16 + (mi >> 1) * 8), af[ks]);
+#pragma unroll
+      for (int ks = 0; ks < 8; ks += 2) {
+        mma_bf16(sc, af[ks], qf[ks][0], qf[ks][1]);
+        mma_bf16(sd, af[ks + 1], qf[ks + 1][0], qf[ks + 1][1]);
       }
     } else {
       const int krow = (mi & 1) * 8 + mr;
+      uint32_t x[4][4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) ldsm_x4(kbase + swz(krow, 2 * kk + (mi >> 1)), x[kk]);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t x[4];
-        ldsm_x4(kbase + swz(krow, 2 * kk + (mi >> 1)), x);
-        uint32_t af[4] = {fp8x2_lo(x[0]), fp8x2_lo(x[1]), fp8x2_hi(x[0]), fp8x2_hi(x[1])};
+        uint32_t af[4] = {fp8x2_lo(x[kk][0]), fp8x2_lo(x[kk][1]), fp8x2_hi(x[kk][0]), fp8x2_hi(x[kk][1])};
         mma_f16(sc, af, qf[2 * kk][0], qf[2 * kk][1]);
-        uint32_t ag[4] = {fp8x2_lo(x[2]), fp8x2_lo(x[3]), fp8x2_hi(x[2]), fp8x2_hi(x[3])};
-        mma_f16(sc, ag, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+        uint32_t ag[4] = {fp8x2_lo(x[kk][2]), fp8x2_lo(x[kk][3]), fp8x2_hi(x[kk][2]), fp8x2_hi(x[kk][3])};
+        mma_f16(sd, ag, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
       }
     }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) sc[r] += sd[r];
 
     // ---- scores in log2 units, masked
     float s0 = sc[0] * a.qk_scale_log2, s1 = sc[1] * a.qk_scale_log2;
@@ -473,7 +551,9 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 2)
     asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
     if (misc[0]) {
       __threadfence();
-      merge_group(a, tid, b, hkv, slot - split, nsplit);
+      // staged LSE values go past the warp-merge area at the start of the ring
+      merge_group<C::NCW * 32>(a, tid, b, hkv, slot - split, nsplit,
+                               reinterpret_cast<float*>(ring) + C::NCW * 8 * 128 + 2 * C::NCW * 8);
       if (tid == 0) a.tickets[group] = 0;
       merged = 1;
     }
@@ -513,8 +593,11 @@ __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant
       tma_load_2d(smem_u32(tile), &tm, smem_u32(&bar), 0, row);
       if (!FP8) tma_load_2d(smem_u32(tile) + 2048, &tm, smem_u32(&bar), 64, row);
     }
-    if (!mbar_wait(smem_u32(&bar), i & 1)) {
+    if (!__syncthreads_and(mbar_wait(smem_u32(&bar), i & 1))) {
       if (threadIdx.x == 0 && status) atomicOr(status, SPLITKV_DEVERR_TIMEOUT);
+      // one more bounded wait so the copy is not left writing into freed smem
+      if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), i & 1);
+      __syncthreads();
       return;
     }
     // 16 rows x 16 chunks (bf16) or 8 chunks (fp8) of 16 bytes each
@@ -538,18 +621,32 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
   const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(&tv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.n_items == 0) return cudaSuccess;
+  // The shared-memory opt-in is a per-process attribute: set it on first use only.
+  static cudaError_t attr_bf16 = cudaFuncSetAttribute(
+      gqa_splitkv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<false>::SMEM);
+  static cudaError_t attr_fp8 = cudaFuncSetAttribute(
+      gqa_splitkv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<true>::SMEM);
+  // Programmatic dependent launch: the kernel's prologue may overlap the tail
+  // of the previous kernel on the stream; it waits (griddepcontrol.wait)
+  // before touching anything that kernel could have written.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_items, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (fp8) {
-    auto k = gqa_splitkv_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<true>::SMEM);
-    if (e != cudaSuccess) return e;
-    k<<<a.n_items, Gqa<true>::THREADS, Gqa<true>::SMEM, s>>>(a, mk, mv);
-  } else {
-    auto k = gqa_splitkv_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<false>::SMEM);
-    if (e != cudaSuccess) return e;
-    k<<<a.n_items, Gqa<false>::THREADS, Gqa<false>::SMEM, s>>>(a, mk, mv);
+    if (attr_fp8 != cudaSuccess) return attr_fp8;
+    cfg.blockDim = dim3(Gqa<true>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Gqa<true>::SMEM;
+    return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<true>, a, mk, mv);
   }
-  return cudaGetLastError();
+  if (attr_bf16 != cudaSuccess) return attr_bf16;
+  cfg.blockDim = dim3(Gqa<false>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Gqa<false>::SMEM;
+  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<false>, a, mk, mv);
 }
 
 cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, int row_bytes, const int32_t* table_row,

@@ -10,17 +10,9 @@ namespace splitkv {
 namespace ptx {
 
 constexpr unsigned kFull = 0xffffffffu;
-// A bounded shared-memory barrier wait gives up after this long.
-constexpr uint64_t kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ------------------------------------------------------------- mbarrier
@@ -55,14 +47,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of the barrier; false if it did not complete
-// within kWaitTimeoutNs.
+// within kWaitTimeoutCycles SM clock cycles (about 2 s at the 2.07 GHz
+// maximum clock, longer at lower clocks).  A waiter must never be more than
+// one phase ahead of the barrier: parity cannot tell phase k from k + 2.
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const long long t0 = clock64();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if (clock64() - t0 > kWaitTimeoutCycles) return false;
   }
 }
 
