@@ -108,7 +108,7 @@ def _check(status: int):
 
 def make_desc(batch, q_tokens, num_q_heads, num_kv_heads, qk_dim, v_dim, page_size,
               max_pages_per_seq, num_pages_total, kv_dtype=SPLITKV_BF16, v_shares_k=0,
-              combine_mode=SPLITKV_COMBINE_FUSED) -> splitkv_desc_t:
+              combine_mode=SPLITKV_COMBINE_SEPARATE) -> splitkv_desc_t:
     return splitkv_desc_t(batch, q_tokens, num_q_heads, num_kv_heads, qk_dim, v_dim, page_size,
                           max_pages_per_seq, num_pages_total, kv_dtype, int(v_shares_k), combine_mode)
 

@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (SPLITKV_BF16, SPLITKV_COMBINE_FUSED, SPLITKV_FP8_E4M3, make_desc, splitkv_decode,
+from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, make_desc, splitkv_decode,
                splitkv_plan, splitkv_plan_upload, splitkv_read_stats)
 
 
@@ -22,7 +22,7 @@ class DecodeSession:
 
     def __init__(self, q, k_pages, v_pages, block_table, seq_lens, seq_lens_host, *, scale,
                  kv_scale=1.0, num_splits=0, num_sms=0, v_dim=None, v_shares_k=False,
-                 combine_mode=SPLITKV_COMBINE_FUSED, stream=None):
+                 combine_mode=SPLITKV_COMBINE_SEPARATE, stream=None):
         B, T, Hq, Dk = q.shape
         N, Hkv, P, _ = k_pages.shape
         if v_dim is None:

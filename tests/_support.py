@@ -23,7 +23,7 @@ def oracle_direct(x: workloads.Inputs, rows=None):
         kv_scale=x.kv_scale, v_dim=w.v_dim, v_shares_k=w.v_shares_k, rows=rows)
 
 
-def session(x: workloads.Inputs, num_splits=0, combine_mode=0, num_sms=0):
+def session(x: workloads.Inputs, num_splits=0, combine_mode=1, num_sms=0):
     return DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
                          scale=x.scale, kv_scale=x.kv_scale, num_splits=num_splits,
                          num_sms=num_sms, v_dim=x.w.v_dim, v_shares_k=x.w.v_shares_k,
