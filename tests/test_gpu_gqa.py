@@ -83,7 +83,7 @@ def test_split_ranges_and_nonempty_ctas():
     """Every launched CTA iterated exactly its planned page range and scored keys."""
     x = workloads.make_inputs(W["gqa_ctx5900"], device="cuda")
     for S in (1, 2, 4, 8, 16, 32, 64, 0):
-        s = session(x, S)
+        s = session(x, S, skv.SPLITKV_COMBINE_FUSED)  # fused: the merging CTA is logged
         s.run()
         log, status = s.stats()
         items = skv.splitkv_plan_get_items(s.plan)
