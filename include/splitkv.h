@@ -175,6 +175,33 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace,
                               void* out, float* lse, void* stream);
 
 /*
+ * splitkv_decode_noalloc -- splitkv_decode for callers that cannot allocate
+ * device memory (code running inside another framework's memory budget,
+ * plugins whose host forbids device allocations after start-up, real-time
+ * loops that must not risk an allocation stall).  Same arguments and result
+ * as splitkv_decode, minus the workspace: the workspace lives in one 16 MiB
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits.  This entry point has no counterpart on the
+ * pages; it is a packaging convenience.
+ *
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - A plan whose splitkv_workspace_size exceeds 16 MiB is rejected with
+ *     SPLITKV_EWORKSPACE (use splitkv_decode with a caller workspace).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Each call uploads the plan into the array (zeroing its merge tickets and
+ *     status word) and then decodes.  All calls share the one array and it
+ *     keeps the last call's contents, so calls that overlap on the GPU (other
+ *     streams, other threads) race; serialise them on one stream.
+ */
+splitkv_status splitkv_decode_noalloc(const splitkv_plan_t* plan, const void* q,
+                                      const void* k_pages, const void* v_pages,
+                                      const int32_t* block_table, const int32_t* seq_lens,
+                                      int32_t num_splits, float scale, float kv_scale,
+                                      void* out, float* lse, void* stream);
+
+/*
  * splitkv_combine -- the log-sum-exp merge on its own, over caller buffers.
  * For each row r < rows: M = max_s lse_part[s][r]; lse = M + ln sum_s
  * exp(lse_part[s][r] - M); out[r][:] = sum_s exp(lse_part[s][r] - lse) *

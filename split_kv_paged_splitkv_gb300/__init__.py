@@ -51,6 +51,7 @@ _SIGNATURES = {
     "splitkv_workspace_size": (_sz, [_vp]),
     "splitkv_plan_upload": (_i32, [_vp, _vp, _sz, _vp]),
     "splitkv_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
+    "splitkv_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
     "splitkv_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "splitkv_read_stats": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "splitkv_debug_gather": (_i32, [ctypes.POINTER(splitkv_desc_t), _vp, _i32, _vp, _i32, _i32,
@@ -164,6 +165,15 @@ def splitkv_decode(plan: Plan, workspace, q, k_pages, v_pages, block_table, seq_
     _check(_lib.splitkv_decode(plan.handle, _ptr(workspace), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                                _ptr(block_table), _ptr(seq_lens), num_splits, scale, kv_scale,
                                _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def splitkv_decode_noalloc(plan: Plan, q, k_pages, v_pages, block_table, seq_lens,
+                           num_splits: int, scale: float, kv_scale: float, out, lse, stream=None):
+    """splitkv_decode without a caller workspace (the library's 16 MiB device
+    array is used instead); for callers that cannot allocate device memory."""
+    _check(_lib.splitkv_decode_noalloc(plan.handle, _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                       _ptr(block_table), _ptr(seq_lens), num_splits, scale,
+                                       kv_scale, _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def splitkv_combine(o_part, lse_part, n_parts: int, rows: int, dv: int, out_bf16=None,
