@@ -130,8 +130,12 @@ void splitkv_plan_destroy(splitkv_plan_t* plan);
 splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items_host,
                                       int32_t capacity, int32_t* n_items);
 
-/* Number of work items = CTAs of the partial kernel. */
+/* Number of work items. */
 int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
+
+/* CTAs the split-KV kernel launches for this plan (one per item for GQA; a
+ * CTA pair per query token and item for MLA): the rows of the per-CTA log. */
+int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan);
 
 /* Bytes of device workspace the plan needs (work list, tickets, per-CTA log,
  * partial outputs).  0 if plan is NULL. */
@@ -219,13 +223,16 @@ splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32
 /*
  * splitkv_read_stats -- synchronises `stream`, then copies to the host the
  * per-CTA log of the last decode on `workspace` and the device status word.
- *   cta_log_host  int32 [n_items][4] or NULL: per launched CTA {first page,
- *                 one-past-last page it iterated, keys it scored, 1 if it
- *                 merged its group}, in item order
+ *   cta_log_host  int32 [capacity][4] or NULL: per launched CTA {first page,
+ *                 one-past-last page it iterated, keys it scored, flag} in
+ *                 launch order; flag = 1 if the CTA merged its group (GQA,
+ *                 fused mode) or gave up on a timed-out wait (MLA)
+ *   capacity      rows of cta_log_host; EINVAL if below splitkv_plan_num_ctas
  *   status_host   int32 or NULL: 0, or a bit set of SPLITKV_DEVERR_* values
  */
 splitkv_status splitkv_read_stats(const splitkv_plan_t* plan, const void* workspace,
-                                  int32_t* cta_log_host, int32_t* status_host, void* stream);
+                                  int32_t* cta_log_host, int32_t capacity, int32_t* status_host,
+                                  void* stream);
 
 enum {
   SPLITKV_DEVERR_TIMEOUT = 1,    /* a bounded wait on a shared-memory barrier gave up */

@@ -208,7 +208,8 @@ def _makespan(costs: List[int], machines: int) -> int:
     return max(loads)
 
 
-def choose_splits(n_pages: Sequence[int], num_kv_heads: int, num_sms: int) -> List[int]:
+def choose_splits(n_pages: Sequence[int], num_kv_heads: int, num_sms: int,
+                  ctas_per_item: int = 1) -> List[int]:
     """Automatic split count per sequence (``num_splits == 0``).
 
     One chunk size ``c`` (pages per split) is used for all sequences and
@@ -217,8 +218,11 @@ def choose_splits(n_pages: Sequence[int], num_kv_heads: int, num_sms: int) -> Li
     = sum of ``n_b * Hkv``), plus "no split" (``c = max n_b``).  Each candidate
     is scored as the LPT makespan of its items over ``num_sms`` machines, item
     cost ``16 * pages + ITEM_OVERHEAD``, plus ``COMBINE_COST * max_b S_b``.
-    The lowest score wins; ties go to the earlier candidate.
+    The lowest score wins; ties go to the earlier candidate.  When one work
+    item launches several CTAs (the MLA kernel: a CTA pair per query token),
+    the machines are ``max(1, num_sms // ctas_per_item)``.
     """
+    num_sms = max(1, num_sms // ctas_per_item)
     total = sum(int(n) for n in n_pages) * num_kv_heads
     nmax = max([int(n) for n in n_pages] + [1])
     cands = []
@@ -239,7 +243,8 @@ def choose_splits(n_pages: Sequence[int], num_kv_heads: int, num_sms: int) -> Li
 
 
 def plan_items(seq_lens: Sequence[int], page_size: int, num_kv_heads: int,
-               num_splits: int, num_sms: int) -> List[Tuple[int, int, int, int, int, int]]:
+               num_splits: int, num_sms: int,
+               ctas_per_item: int = 1) -> List[Tuple[int, int, int, int, int, int]]:
     """Work list ``[(b, h_kv, s, S_b, p0, p1)]`` in launch order.
 
     ``num_splits > 0``: ``S_b = min(num_splits, n_b)`` -- the requested count
@@ -252,7 +257,7 @@ def plan_items(seq_lens: Sequence[int], page_size: int, num_kv_heads: int,
     if num_splits > 0:
         S = [max(1, min(num_splits, n)) if n > 0 else 1 for n in n_pages]
     else:
-        S = choose_splits(n_pages, num_kv_heads, num_sms)
+        S = choose_splits(n_pages, num_kv_heads, num_sms, ctas_per_item)
     items = []
     for b, (n, s_b) in enumerate(zip(n_pages, S)):
         rngs = split_ranges(n, s_b) if n > 0 else [(0, 0)]

@@ -48,12 +48,13 @@ _SIGNATURES = {
     "splitkv_plan_destroy": (None, [_vp]),
     "splitkv_plan_get_items": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32)]),
     "splitkv_plan_num_items": (_i32, [_vp]),
+    "splitkv_plan_num_ctas": (_i32, [_vp]),
     "splitkv_workspace_size": (_sz, [_vp]),
     "splitkv_plan_upload": (_i32, [_vp, _vp, _sz, _vp]),
     "splitkv_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
     "splitkv_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
     "splitkv_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
-    "splitkv_read_stats": (_i32, [_vp, _vp, _vp, _vp, _vp]),
+    "splitkv_read_stats": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp]),
     "splitkv_debug_gather": (_i32, [ctypes.POINTER(splitkv_desc_t), _vp, _i32, _vp, _i32, _i32,
                                     _i32, _vp, _vp]),
     "splitkv_last_error": (ctypes.c_char_p, []),
@@ -182,13 +183,17 @@ def splitkv_combine(o_part, lse_part, n_parts: int, rows: int, dv: int, out_bf16
                                 _ptr(out_f32), _ptr(lse_out), _stream(stream)))
 
 
+def splitkv_plan_num_ctas(plan: Plan) -> int:
+    return int(_lib.splitkv_plan_num_ctas(plan.handle))
+
+
 def splitkv_read_stats(plan: Plan, workspace, stream=None):
     """Returns (cta_log [n_ctas][4] int32, status int)."""
-    n = plan.num_items
+    n = splitkv_plan_num_ctas(plan)
     log = np.zeros((max(n, 1), 4), dtype=np.int32)
     st = np.zeros(1, dtype=np.int32)
-    _check(_lib.splitkv_read_stats(plan.handle, _ptr(workspace), log.ctypes.data, st.ctypes.data,
-                                   _stream(stream)))
+    _check(_lib.splitkv_read_stats(plan.handle, _ptr(workspace), log.ctypes.data, log.shape[0],
+                                   st.ctypes.data, _stream(stream)))
     return log[:n], int(st[0])
 
 

@@ -53,6 +53,23 @@ splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, in
   return SPLITKV_OK;
 }
 
+// 2-D bf16 map over [rows][dim] with boxes of 64 columns x box_rows rows.
+splitkv_status make_bf16_map(TmaDesc* out, const void* base, int dim, int64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap m;
+  cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
+  cuuint64_t gstride[1] = {cuuint64_t(dim) * 2};
+  cuuint32_t box[2] = {64u, cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  std::memcpy(out, &m, sizeof(m));
+  return SPLITKV_OK;
+}
+
 splitkv_status cuda_fail(cudaError_t e, const char* what) {
   return fail(SPLITKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -81,7 +98,8 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
   if (family_of(*d) == Family::kNone)
     return fail(SPLITKV_EUNSUPPORTED,
                 "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
-                "(GQA: qk_dim=v_dim=128, T*G<=8)",
+                "(GQA: qk_dim=v_dim=128, T*G<=8; MLA: 128 q heads, 1 bf16 latent head, "
+                "qk_dim=576, v_dim=512, v_shares_k, page_size 64, T<=16)",
                 d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
                 d->v_shares_k);
   return SPLITKV_OK;
@@ -100,12 +118,14 @@ splitkv_status fail(splitkv_status s, const char* fmt, ...) {
 Family family_of(const splitkv_desc_t& d) {
   const int G = d.num_q_heads / d.num_kv_heads;
   if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 8) return Family::kGqa;
+  if (d.qk_dim == 576 && d.v_dim == 512 && d.v_shares_k && d.num_kv_heads == 1 &&
+      d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.page_size == 64 && d.q_tokens <= 16)
+    return Family::kMla;
   return Family::kNone;
 }
 
 int ctas_per_item(const splitkv_desc_t& d) {
-  (void)d;
-  return 1;
+  return family_of(d) == Family::kMla ? 2 * d.q_tokens : 1;
 }
 
 }  // namespace splitkv
@@ -156,6 +176,8 @@ splitkv_status splitkv_plan(const splitkv_desc_t* desc, const int32_t* seq_lens_
 void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
 
 int32_t splitkv_plan_num_items(const splitkv_plan_t* plan) { return plan ? plan->n_items : 0; }
+
+int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan) { return plan ? plan->n_ctas : 0; }
 
 splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items_host,
                                       int32_t capacity, int32_t* n_items) {
@@ -243,6 +265,22 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
   a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
+  if (family_of(d) == Family::kMla) {
+    // Latent cache rows of 576 bf16 (64-key boxes = one page); query rows of
+    // 576 bf16 (128-head boxes = one token).  The partials are always merged
+    // by the separate combine kernel.
+    TmaDesc tq, tk;
+    splitkv_status st = make_bf16_map(&tq, q, d.qk_dim, int64_t(d.batch) * d.q_tokens * d.num_q_heads, 128);
+    if (st != SPLITKV_OK) return st;
+    st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, 64);
+    if (st != SPLITKV_OK) return st;
+    a.fused = 0;
+    cudaError_t e = launch_mla(a, tq, tk, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the MLA split-KV kernel");
+    e = launch_combine(a, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
+    return SPLITKV_OK;
+  }
   TmaDesc tk, tv;
   splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total);
   if (st != SPLITKV_OK) return st;
@@ -277,8 +315,11 @@ splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32
 }
 
 splitkv_status splitkv_read_stats(const splitkv_plan_t* plan, const void* workspace,
-                                  int32_t* cta_log_host, int32_t* status_host, void* stream) {
+                                  int32_t* cta_log_host, int32_t capacity, int32_t* status_host,
+                                  void* stream) {
   if (!plan || !workspace) return fail(SPLITKV_EINVAL, "plan and workspace must not be NULL");
+  if (cta_log_host && capacity < plan->n_ctas)
+    return fail(SPLITKV_EINVAL, "cta log capacity %d < %d CTAs", capacity, plan->n_ctas);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned char* ws = static_cast<const unsigned char*>(workspace);
   cudaError_t e = cudaSuccess;

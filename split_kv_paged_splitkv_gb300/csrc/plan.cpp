@@ -62,7 +62,10 @@ inline int32_t split_edge(int64_t s, int64_t n, int64_t S) {
 
 // Automatic choice: one chunk size for the whole batch, scored by the
 // makespan of its items on `sms` SMs plus a per-split merge charge.
-std::vector<int32_t> choose_splits(const std::vector<int32_t>& n_pages, int hkv, int sms) {
+std::vector<int32_t> choose_splits(const std::vector<int32_t>& n_pages, int hkv, int sms_total,
+                                   int ctas_per_item) {
+  // An item that launches several CTAs occupies that many SMs' worth of slots.
+  const int sms = std::max(1, sms_total / ctas_per_item);
   int64_t total = 0, nmax = 1;
   for (int32_t n : n_pages) {
     total += n;
@@ -112,7 +115,7 @@ void build_plan(splitkv_plan_s* p) {
   if (p->num_splits > 0) {
     for (int b = 0; b < B; ++b) S[b] = n_pages[b] > 0 ? std::min(p->num_splits, n_pages[b]) : 1;
   } else {
-    S = choose_splits(n_pages, hkv, p->num_sms);
+    S = choose_splits(n_pages, hkv, p->num_sms, ctas_per_item(d));
   }
 
   // Combine groups and partial slots, in (b, h_kv) order.

@@ -163,3 +163,15 @@ def test_combine_validates():
     for n_parts, dv in ((2, 130), (2, 96), (2, 1024), (1025, 128)):
         st = skv._lib.splitkv_combine(1 << 20, 1 << 20, n_parts, 4, dv, 1 << 20, None, None, None)
         assert st == skv.SPLITKV_EINVAL, (n_parts, dv)
+
+
+def test_plan_matches_oracle_mla_cta_pairs():
+    """MLA items launch a CTA pair per query token; the automatic split count
+    plans over num_sms / (2 T) machines in both the library and the oracle."""
+    for T, L in ((6, 65536), (1, 4096), (2, 300)):
+        d = skv.make_desc(1, T, 128, 1, 576, 512, 64, 1024, 1100, skv.SPLITKV_BF16, 1)
+        for S in (0, 1, 4, 8):
+            plan = skv.splitkv_plan(d, np.array([L], np.int32), S, 148)
+            items = skv.splitkv_plan_get_items(plan)
+            ref = np.array(oracle.plan_items([L], 64, 1, S, 148, ctas_per_item=2 * T), np.int32)
+            assert np.array_equal(items[:, :6], ref), (T, L, S)
