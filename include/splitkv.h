@@ -214,7 +214,7 @@ splitkv_status splitkv_decode_noalloc(const splitkv_plan_t* plan, const void* q,
  *   o_part    fp32 [n_parts][rows][dv]      lse_part  fp32 [n_parts][rows]
  *   out_bf16  bf16 [rows][dv] or NULL       out_f32   fp32 [rows][dv] or NULL
  *   lse_out   fp32 [rows] or NULL
- *   n_parts in [1, 1024]; dv a power of two in [4, 512]
+ *   n_parts >= 1; dv a positive multiple of 4
  */
 splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32_t n_parts,
                                int32_t rows, int32_t dv, void* out_bf16, float* out_f32,

@@ -32,9 +32,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over [rows][dim] elements with 16-row boxes, 128-byte swizzle.
-// bf16 boxes are 64 columns wide (two per row), e4m3 boxes 128 columns.
-splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, int64_t rows) {
+// 2-D map over [rows][dim] K or V elements with 16-row boxes and the 128-byte
+// swizzle: bf16 boxes are 64 columns wide (two per 128-wide row), e4m3 boxes
+// 128 columns.
+splitkv_status make_kv_map_2d(TmaDesc* out, const void* base, bool fp8, int dim, int64_t rows) {
   auto fn = encode_fn();
   if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int elt = fp8 ? 1 : 2;
@@ -51,6 +52,32 @@ splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, in
   static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "tensor map size");
   std::memcpy(out, &m, sizeof(m));
   return SPLITKV_OK;
+}
+
+// As make_kv_map_2d, but for bf16 rows of 128 first tries a 3-D view (64
+// columns, rows, 2 column halves; strides 256 B and 128 B) so that one box
+// brings a whole 16-key tile as [2 halves][16 rows][64] -- the same shared
+// memory layout as two 2-D boxes, in half the TMA transactions.  *box3d
+// reports which form was built.
+splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, int64_t rows,
+                           bool* box3d) {
+  *box3d = false;
+  auto fn = encode_fn();
+  if (fn && !fp8 && dim == 128) {
+    CUtensorMap m;
+    cuuint64_t gdim3[3] = {64u, cuuint64_t(rows), 2u};
+    cuuint64_t gstride3[2] = {256u, 128u};
+    cuuint32_t box3[3] = {64u, 16u, 2u};
+    cuuint32_t estr3[3] = {1u, 1u, 1u};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim3, gstride3, box3,
+           estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      std::memcpy(out, &m, sizeof(m));
+      *box3d = true;
+      return SPLITKV_OK;
+    }
+  }
+  return make_kv_map_2d(out, base, fp8, dim, rows);
 }
 
 // 2-D bf16 map over [rows][dim] with boxes of 64 columns x box_rows rows.
@@ -282,10 +309,18 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
     return SPLITKV_OK;
   }
   TmaDesc tk, tv;
-  splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total);
+  bool k3 = false, v3 = false;
+  splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total, &k3);
   if (st != SPLITKV_OK) return st;
-  st = make_kv_map(&tv, v_pages, fp8, d.v_dim, rows_total);
+  st = make_kv_map(&tv, v_pages, fp8, d.v_dim, rows_total, &v3);
   if (st != SPLITKV_OK) return st;
+  if (k3 != v3) {  // keep both maps in the same form
+    if (k3) st = make_kv_map_2d(&tk, k_pages, fp8, d.qk_dim, rows_total);
+    else st = make_kv_map_2d(&tv, v_pages, fp8, d.v_dim, rows_total);
+    if (st != SPLITKV_OK) return st;
+    k3 = v3 = false;
+  }
+  a.kv_box3d = k3 ? 1 : 0;
 
   cudaError_t e = launch_gqa(a, tk, tv, fp8, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the split-KV kernel");
@@ -300,10 +335,8 @@ splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32
                                int32_t rows, int32_t dv, void* out_bf16, float* out_f32,
                                float* lse_out, void* stream) {
   if (!o_part || !lse_part) return fail(SPLITKV_EINVAL, "o_part and lse_part must not be NULL");
-  if (n_parts < 1 || n_parts > 1024 || rows < 0)
-    return fail(SPLITKV_EINVAL, "n_parts must be in [1, 1024] and rows >= 0");
-  if (dv < 4 || dv > 512 || (dv & (dv - 1)))
-    return fail(SPLITKV_EINVAL, "dv must be a power of two in [4, 512]");
+  if (n_parts < 1 || rows < 0) return fail(SPLITKV_EINVAL, "n_parts must be >= 1 and rows >= 0");
+  if (dv < 4 || dv % 4) return fail(SPLITKV_EINVAL, "dv must be a positive multiple of 4");
   if (!out_bf16 && !out_f32 && !lse_out) return fail(SPLITKV_EINVAL, "no output given");
   if (!aligned16(o_part) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && (reinterpret_cast<uintptr_t>(out_bf16) & 7u)))
@@ -348,12 +381,11 @@ splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* page
   const bool fp8 = desc->kv_dtype == SPLITKV_FP8_E4M3;
   const int64_t rows_total = int64_t(desc->num_pages_total) * desc->num_kv_heads * desc->page_size;
   TmaDesc t;
-  st = make_kv_map(&t, pages, fp8, row_elems, rows_total);
+  bool box3d = false;
+  st = make_kv_map(&t, pages, fp8, row_elems, rows_total, &box3d);
   if (st != SPLITKV_OK) return st;
-  cudaError_t e = launch_debug_gather(t, fp8, row_elems * (fp8 ? 1 : 2),
-                                      block_table + size_t(b) * desc->max_pages_per_seq,
-                                      desc->page_size, desc->num_kv_heads, h_kv, desc->page_size,
-                                      n_keys, dst, stream);
+  cudaError_t e = launch_debug_gather(t, fp8, box3d, block_table + size_t(b) * desc->max_pages_per_seq,
+                                      desc->num_kv_heads, h_kv, desc->page_size, n_keys, dst, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the gather kernel");
   return SPLITKV_OK;
 }

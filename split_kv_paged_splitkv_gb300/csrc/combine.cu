@@ -19,23 +19,24 @@ using namespace ptx;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// One CTA of 128 threads per (group, row).  The row's S LSE values are staged
-// in shared memory by all threads at once.  Each thread owns 4 dims (float4)
-// and 1/W of the splits, W = 128 / (dv / 4) "ways"; it keeps 8 splits' loads
-// in flight per step, and the W ways are summed through shared memory.
+// One CTA of 128 threads per (group, row, 128-dim chunk): 32 lanes x 4 float
+// dims each, and 4 "ways" that take every 4th split.  A thread loads the LSE
+// and the O values of up to 16 of its splits at once (one L2 round trip for
+// up to 64 splits), keeps a running maximum across further chunks of splits,
+// and the 4 ways are merged through shared memory at the end.
 //   plan mode (groups != nullptr): group g = blockIdx.x covers slots
 //     slot0 .. slot0+S-1 with `rows` rows each; row n -> (t, head) of (b, h_kv).
 //   raw mode: one group, S = n_parts, slot0 = 0, output row n.
 constexpr int kCombineThreads = 128;
-constexpr int kCombineMaxParts = 1024;
+constexpr int kWays = 4;
+constexpr int kPerWay = 16;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part,
     const int32_t* __restrict__ groups, int n_parts, int rows, int dv, int T, int Hq, int G,
     void* out_bf16, float* out_f32, float* lse_out, int pdl) {
-  __shared__ float sl[kCombineMaxParts];
   __shared__ float4 red[kCombineThreads];
-  __shared__ float wred[kCombineThreads];
+  __shared__ float red_w[kCombineThreads], red_m[kCombineThreads];
   launch_dependents();
   if (pdl) wait_prerequisites();
   const int n = blockIdx.y;
@@ -49,71 +50,80 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const int t = n / G, gg = n - t * G;
     orow = (size_t(b) * T + t) * Hq + size_t(hkv) * G + gg;
   }
-  const int tid = threadIdx.x;
-  for (int s = tid; s < S; s += kCombineThreads) sl[s] = lse_part[size_t(slot0 + s) * rows + n];
-  __syncthreads();
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, sl[s]);
+  const int tid = threadIdx.x, dl = tid & 31, way = tid >> 5;
+  const int d = blockIdx.z * 128 + dl * 4;
+  const bool dim_ok = d < dv;
+  const float* lp = lse_part + size_t(slot0) * rows + n;
+  const float* op = o_part + (size_t(slot0) * rows + n) * dv + (dim_ok ? d : 0);
+  const size_t ostride = size_t(rows) * dv;
 
-  const int lanes = dv >> 2;                 // threads per row of dims
-  const int ways = kCombineThreads / lanes;  // splits interleaved over this many threads
-  const int dl = tid % lanes, way = tid / lanes;
-  const int d = dl * 4;
+  float m_run = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (M != -INFINITY && way < ways) {
-    const size_t stride = size_t(rows) * dv;
-    const float* base = o_part + (size_t(slot0) * rows + n) * dv + d;
-    for (int s0 = way; s0 < S; s0 += 8 * ways) {
-      float4 x[8];
+  for (int s0 = way; s0 < S; s0 += kWays * kPerWay) {
+    float lv[kPerWay];
+    float4 x[kPerWay];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int s = s0 + u * ways;
-        if (s < S) x[u] = *reinterpret_cast<const float4*>(base + size_t(s) * stride);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int s = s0 + u * ways;
-        if (s < S) {
-          const float w = ex2((sl[s] - M) * kLog2e);
-          wsum += w;
-          acc.x += w * x[u].x;
-          acc.y += w * x[u].y;
-          acc.z += w * x[u].z;
-          acc.w += w * x[u].w;
-        }
+    for (int u = 0; u < kPerWay; ++u) {
+      const int s = s0 + u * kWays;
+      lv[u] = -INFINITY;
+      x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s < S) {
+        lv[u] = lp[size_t(s) * rows];
+        if (dim_ok) x[u] = *reinterpret_cast<const float4*>(op + size_t(s) * ostride);
       }
     }
+    float m_new = m_run;
+#pragma unroll
+    for (int u = 0; u < kPerWay; ++u) m_new = fmaxf(m_new, lv[u]);
+    if (m_new == -INFINITY) continue;  // every split so far is empty
+    const float rs = ex2((m_run - m_new) * kLog2e);  // 0 when m_run is -inf
+    acc.x *= rs; acc.y *= rs; acc.z *= rs; acc.w *= rs;
+    wsum *= rs;
+#pragma unroll
+    for (int u = 0; u < kPerWay; ++u) {
+      const float w = ex2((lv[u] - m_new) * kLog2e);  // 0 for empty splits
+      wsum += w;
+      acc.x += w * x[u].x; acc.y += w * x[u].y; acc.z += w * x[u].z; acc.w += w * x[u].w;
+    }
+    m_run = m_new;
   }
   red[tid] = acc;
-  wred[tid] = wsum;
+  red_w[tid] = wsum;
+  red_m[tid] = m_run;
   __syncthreads();
   if (way != 0) return;
-  for (int k = 1; k < ways; ++k) {
-    const float4 o = red[tid + k * lanes];
-    acc.x += o.x;
-    acc.y += o.y;
-    acc.z += o.z;
-    acc.w += o.w;
-    wsum += wred[tid + k * lanes];
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kWays; ++k) M = fmaxf(M, red_m[dl + 32 * k]);
+  float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wtot = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int k = 0; k < kWays; ++k) {
+      const float mk = red_m[dl + 32 * k];
+      if (mk == -INFINITY) continue;
+      const float sc = ex2((mk - M) * kLog2e);
+      const float4 o = red[dl + 32 * k];
+      tot.x += sc * o.x; tot.y += sc * o.y; tot.z += sc * o.z; tot.w += sc * o.w;
+      wtot += sc * red_w[dl + 32 * k];
+    }
   }
   float lse_n = -INFINITY;
-  if (wsum > 0.f) {
-    const float inv = 1.f / wsum;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
-    lse_n = M + lg2(wsum) * kLn2;
+  if (wtot > 0.f) {
+    const float inv = 1.f / wtot;
+    tot.x *= inv; tot.y *= inv; tot.z *= inv; tot.w *= inv;
+    lse_n = M + lg2(wtot) * kLn2;
   }
-  if (out_bf16) {
-    uint2 v;
-    v.x = pack_bf16(acc.x, acc.y);
-    v.y = pack_bf16(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out_bf16) + orow * dv + d) = v;
+  if (dim_ok) {
+    if (out_bf16) {
+      uint2 v;
+      v.x = pack_bf16(tot.x, tot.y);
+      v.y = pack_bf16(tot.z, tot.w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out_bf16) + orow * dv + d) = v;
+    }
+    if (out_f32) *reinterpret_cast<float4*>(out_f32 + orow * dv + d) = tot;
   }
-  if (out_f32) *reinterpret_cast<float4*>(out_f32 + orow * dv + d) = acc;
-  if (tid == 0 && lse_out) lse_out[orow] = lse_n;
+  if (tid == 0 && blockIdx.z == 0 && lse_out) lse_out[orow] = lse_n;
 }
 
 }  // namespace
@@ -121,7 +131,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream) {
   if (a.n_groups == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_groups, a.rows, 1);
+  cfg.gridDim = dim3(a.n_groups, a.rows, (a.dv + 127) / 128);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -139,7 +149,7 @@ cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n
                                int dv, void* out_bf16, float* out_f32, float* lse_out,
                                void* stream) {
   if (rows == 0) return cudaSuccess;
-  dim3 grid(1, rows, 1), block(kCombineThreads, 1, 1);
+  dim3 grid(1, rows, (dv + 127) / 128), block(kCombineThreads, 1, 1);
   combine_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
       o_part, lse_part, nullptr, n_parts, rows, dv, 1, 1, 1, out_bf16, out_f32, lse_out, 0);
   return cudaGetLastError();

@@ -252,15 +252,17 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
   }
-  __syncthreads();
-  launch_dependents();
-  wait_prerequisites();
-
-  const int L = a.seq_lens[b];
+  // The plan's copy of the sequence length (uploaded with the work list, never
+  // written by a kernel) is read before the wait; the caller's device copy is
+  // only checked against it, off the critical path.
+  const int L = a.plan_lens[b];
   const int k_begin = p0 * a.P;
   const int k_end = min(p1 * a.P, L);
   const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
-  if (threadIdx.x == 0 && a.plan_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
+  __syncthreads();
+  launch_dependents();
+  wait_prerequisites();
+  if (threadIdx.x == 0 && a.seq_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
 
   if (warp == C::NCW) {
     // ---------------------------------------------------------------- producer
@@ -307,6 +309,9 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
           if (FP8) {
             tma_load_2d(dk, &tk, bar, 0, row);
             tma_load_2d(dv, &tv, bar, 0, row);
+          } else if (a.kv_box3d) {  // one [2 halves][16 rows][64] box per tile
+            tma_load_3d(dk, &tk, bar, 0, row, 0);
+            tma_load_3d(dv, &tv, bar, 0, row, 0);
           } else {
             tma_load_2d(dk, &tk, bar, 0, row);
             tma_load_2d(dk + 2048, &tk, bar, 64, row);
@@ -574,7 +579,7 @@ template <bool FP8>
 __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant__ CUtensorMap tm,
                                                            const int32_t* table_row, int Hkv,
                                                            int h_kv, int P, int n_keys,
-                                                           uint8_t* dst, int32_t* status) {
+                                                           uint8_t* dst, int32_t* status, int box3d) {
   constexpr int KT = Gqa<FP8>::KT_BYTES;
   __shared__ __align__(1024) uint8_t tile[KT];
   __shared__ __align__(8) uint64_t bar;
@@ -590,8 +595,12 @@ __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant
       const int ph = table_row[key0 / P];
       const int row = (ph * Hkv + h_kv) * P + key0 % P;
       mbar_arrive_expect_tx(smem_u32(&bar), KT);
-      tma_load_2d(smem_u32(tile), &tm, smem_u32(&bar), 0, row);
-      if (!FP8) tma_load_2d(smem_u32(tile) + 2048, &tm, smem_u32(&bar), 64, row);
+      if (!FP8 && box3d) {
+        tma_load_3d(smem_u32(tile), &tm, smem_u32(&bar), 0, row, 0);
+      } else {
+        tma_load_2d(smem_u32(tile), &tm, smem_u32(&bar), 0, row);
+        if (!FP8) tma_load_2d(smem_u32(tile) + 2048, &tm, smem_u32(&bar), 64, row);
+      }
     }
     if (!__syncthreads_and(mbar_wait(smem_u32(&bar), i & 1))) {
       if (threadIdx.x == 0 && status) atomicOr(status, SPLITKV_DEVERR_TIMEOUT);
@@ -649,20 +658,18 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
   return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<false>, a, mk, mv);
 }
 
-cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, int row_bytes, const int32_t* table_row,
-                                int32_t rows_per_page_head, int32_t hkv, int32_t h_kv, int32_t P,
-                                int32_t n_keys, void* dst, void* stream) {
-  (void)row_bytes;
-  (void)rows_per_page_head;
+cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, bool box3d, const int32_t* table_row,
+                                int32_t hkv, int32_t h_kv, int32_t P, int32_t n_keys, void* dst,
+                                void* stream) {
   const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(&t);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* status = nullptr;
   if (fp8)
     gather_debug_kernel<true><<<1, 128, 0, s>>>(m, table_row, hkv, h_kv, P, n_keys,
-                                                static_cast<uint8_t*>(dst), status);
+                                                static_cast<uint8_t*>(dst), status, 0);
   else
     gather_debug_kernel<false><<<1, 128, 0, s>>>(m, table_row, hkv, h_kv, P, n_keys,
-                                                 static_cast<uint8_t*>(dst), status);
+                                                 static_cast<uint8_t*>(dst), status, box3d ? 1 : 0);
   return cudaGetLastError();
 }
 

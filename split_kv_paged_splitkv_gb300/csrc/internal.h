@@ -78,6 +78,7 @@ struct DecodeArgs {
   float qk_scale_log2;  // scale * kv_scale * log2(e) (x 256 for FP8, see kernel)
   float o_scale;        // factor applied to the normalised output (FP8: kv_scale * 256)
   int32_t fused;        // 1: last CTA of a group merges
+  int32_t kv_box3d;     // bf16 K/V maps are 3-D: one [2][16][64] box per 16-key tile
 };
 
 // Raw 128-byte tensor map storage (CUtensorMap), built by the API layer.
@@ -92,8 +93,8 @@ cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
                                int dv, void* out_bf16, float* out_f32, float* lse_out,
                                void* stream);
-cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, int row_bytes, const int32_t* table_row,
-                                int32_t rows_per_page_head, int32_t hkv, int32_t h_kv,
-                                int32_t P, int32_t n_keys, void* dst, void* stream);
+cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, bool box3d, const int32_t* table_row,
+                                int32_t hkv, int32_t h_kv, int32_t P, int32_t n_keys, void* dst,
+                                void* stream);
 
 }  // namespace splitkv

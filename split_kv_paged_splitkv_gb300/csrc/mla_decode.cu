@@ -132,15 +132,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Mla::THREADS, 1)
   cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  launch_dependents();
-  wait_prerequisites();
-
-  const int L = a.seq_lens[b];
+  // plan's sequence length (uploaded, never written by a kernel): read before the wait
+  const int L = a.plan_lens[b];
   const int k_begin = p0 * C::BK;
   const int k_end = min(p1 * C::BK, L);
   const int nblk = k_end > k_begin ? (k_end - k_begin + C::BK - 1) / C::BK : 0;
   const int lim = L - a.T + t;  // last key visible to this token
-  if (threadIdx.x == 0 && rank == 0 && t == 0 && a.plan_lens[b] != L)
+  launch_dependents();
+  wait_prerequisites();
+  if (threadIdx.x == 0 && rank == 0 && t == 0 && a.seq_lens[b] != L)
     atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
 
   if (warp == 0) {

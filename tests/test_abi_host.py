@@ -160,7 +160,7 @@ def test_upload_checks_workspace_size():
 def test_combine_validates():
     st = skv._lib.splitkv_combine(1 << 20, 1 << 20, 0, 4, 128, 1 << 20, None, None, None)
     assert st == skv.SPLITKV_EINVAL
-    for n_parts, dv in ((2, 130), (2, 96), (2, 1024), (1025, 128)):
+    for n_parts, dv in ((2, 130), (2, 0), (0, 128), (2, 6)):
         st = skv._lib.splitkv_combine(1 << 20, 1 << 20, n_parts, 4, dv, 1 << 20, None, None, None)
         assert st == skv.SPLITKV_EINVAL, (n_parts, dv)
 

@@ -225,3 +225,25 @@ def test_seq_len_mismatch_is_reported():
     s.run(tensors=(x.q, x.k_pages, x.v_pages, x.block_table, wrong))
     _, status = s.stats()
     assert status & skv.SPLITKV_DEVERR_SEQLEN
+
+
+@pytest.mark.parametrize("S,R,D", [(200, 3, 512), (70, 2, 96), (1, 4, 128), (64, 5, 128)])
+def test_combine_many_parts_and_widths(S, R, D):
+    """More splits than one load round covers (running maximum across chunks),
+    V widths that are not a multiple of 128, a single part, and -inf rows."""
+    rng = np.random.default_rng(S * 7 + D)
+    o = rng.standard_normal((S, R, D)).astype(np.float32)
+    l = (rng.standard_normal((S, R)) * 6).astype(np.float32)
+    l[rng.random((S, R)) < 0.2] = -np.inf
+    l[:, 0] = -np.inf if S > 1 else l[:, 0]
+    out = torch.empty((R, D), dtype=torch.float32, device="cuda")
+    lo = torch.empty(R, dtype=torch.float32, device="cuda")
+    skv.splitkv_combine(torch.from_numpy(o).cuda(), torch.from_numpy(l).cuda(), S, R, D, None, out, lo)
+    torch.cuda.synchronize()
+    for r in range(R):
+        ro, rl = oracle.combine([(o[s, r].astype(np.float64), float(l[s, r])) for s in range(S)])
+        assert np.abs(out[r].cpu().numpy() - ro).max() < 1e-5
+        if np.isfinite(rl):
+            assert abs(lo[r].item() - rl) < 1e-5
+        else:
+            assert lo[r].item() == -np.inf
