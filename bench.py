@@ -256,7 +256,7 @@ def run_ours(args, rank, world, local):
                          v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode)
     items = skv.splitkv_plan_get_items(sess.plan)
     n_groups = len(np.unique(items[items[:, 3] > 1][:, 7])) if len(items) else 0
-    launches_per_step = 1 + (1 if (mode == skv.SPLITKV_COMBINE_SEPARATE and n_groups) else 0)
+    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan)
 
     # rotating KV pools: total > 4x L2
     props = torch.cuda.get_device_properties(dev)

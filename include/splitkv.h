@@ -137,6 +137,11 @@ int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
  * CTA pair per query token and item for MLA): the rows of the per-CTA log. */
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan);
 
+/* Kernel launches one splitkv_decode of this plan makes (1 or 2: the split
+ * kernel, plus the combine kernel when splits must be merged and the merge
+ * does not run inside the split kernel). */
+int32_t splitkv_plan_launches_per_call(const splitkv_plan_t* plan);
+
 /* Bytes of device workspace the plan needs (work list, tickets, per-CTA log,
  * partial outputs).  0 if plan is NULL. */
 size_t splitkv_workspace_size(const splitkv_plan_t* plan);

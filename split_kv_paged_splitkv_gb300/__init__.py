@@ -49,6 +49,7 @@ _SIGNATURES = {
     "splitkv_plan_get_items": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32)]),
     "splitkv_plan_num_items": (_i32, [_vp]),
     "splitkv_plan_num_ctas": (_i32, [_vp]),
+    "splitkv_plan_launches_per_call": (_i32, [_vp]),
     "splitkv_workspace_size": (_sz, [_vp]),
     "splitkv_plan_upload": (_i32, [_vp, _vp, _sz, _vp]),
     "splitkv_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
@@ -181,6 +182,10 @@ def splitkv_combine(o_part, lse_part, n_parts: int, rows: int, dv: int, out_bf16
                     out_f32=None, lse_out=None, stream=None):
     _check(_lib.splitkv_combine(_ptr(o_part), _ptr(lse_part), n_parts, rows, dv, _ptr(out_bf16),
                                 _ptr(out_f32), _ptr(lse_out), _stream(stream)))
+
+
+def splitkv_plan_launches_per_call(plan: Plan) -> int:
+    return int(_lib.splitkv_plan_launches_per_call(plan.handle))
 
 
 def splitkv_plan_num_ctas(plan: Plan) -> int:

@@ -206,6 +206,14 @@ int32_t splitkv_plan_num_items(const splitkv_plan_t* plan) { return plan ? plan-
 
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan) { return plan ? plan->n_ctas : 0; }
 
+int32_t splitkv_plan_launches_per_call(const splitkv_plan_t* plan) {
+  if (!plan) return 0;
+  if (plan->n_groups == 0) return 1;
+  const bool fused = plan->desc.combine_mode == SPLITKV_COMBINE_FUSED &&
+                     family_of(plan->desc) == Family::kGqa;
+  return fused ? 1 : 2;
+}
+
 splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items_host,
                                       int32_t capacity, int32_t* n_items) {
   if (!plan || !n_items) return fail(SPLITKV_EINVAL, "plan and n_items must not be NULL");

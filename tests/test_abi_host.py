@@ -175,3 +175,12 @@ def test_plan_matches_oracle_mla_cta_pairs():
             items = skv.splitkv_plan_get_items(plan)
             ref = np.array(oracle.plan_items([L], 64, 1, S, 148, ctas_per_item=2 * T), np.int32)
             assert np.array_equal(items[:, :6], ref), (T, L, S)
+
+
+def test_launches_per_call():
+    d_sep = _desc(mode=skv.SPLITKV_COMBINE_SEPARATE)
+    d_fus = _desc(mode=skv.SPLITKV_COMBINE_FUSED)
+    lens = np.array([5900], np.int32)
+    assert skv.splitkv_plan_launches_per_call(skv.splitkv_plan(d_sep, lens, 8, 148)) == 2
+    assert skv.splitkv_plan_launches_per_call(skv.splitkv_plan(d_fus, lens, 8, 148)) == 1
+    assert skv.splitkv_plan_launches_per_call(skv.splitkv_plan(d_sep, lens, 1, 148)) == 1  # nothing to merge
