@@ -293,10 +293,10 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
   a.rows = plan->rows;
   a.dv = d.v_dim;
   const float kLog2e = 1.4426950408889634f;
-  // FP8 tiles are read as f16 values equal to code * 2^-8 (see the kernel), so
-  // both the score scale and the output scale carry an extra 2^8.
-  a.qk_scale_log2 = scale * kLog2e * (fp8 ? kv_scale * 256.f : 1.f);
-  a.o_scale = fp8 ? kv_scale * 256.f : 1.f;
+  // FP8 tiles are converted to their e4m3 values; the per-tensor kv_scale is
+  // applied once to the scores and once to the output.
+  a.qk_scale_log2 = scale * kLog2e * (fp8 ? kv_scale : 1.f);
+  a.o_scale = fp8 ? kv_scale : 1.f;
   a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;

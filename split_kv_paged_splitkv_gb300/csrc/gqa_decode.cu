@@ -13,7 +13,7 @@
 // so a group of up to 8 query rows (T*G <= 8) fills the MMA's N side and the
 // 16-key tile fills M with no padding.  P^T is turned from accumulator layout
 // into operand layout in registers with movmatrix.  FP8 e4m3 tiles are
-// converted to f16 in registers (exact, see ptx::fp8x2_*) and use the f16
+// converted to f16 in registers (exact, ptx::e4m3x2_*) and use the f16
 // MMA; BF16 tiles go straight to the bf16 MMA.
 //
 // The four warps' (m, l, O) are merged in shared memory; the item's result is
@@ -357,12 +357,13 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
           qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * ti));
           qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * ti + 8));
         } else {
-          // k = 2ti, 2ti+1 <-> d = 16ks+4ti, +2 ; k = 2ti+8, 2ti+9 <-> d = 16ks+4ti+1, +3
+          // k = 2ti, 2ti+1 <-> d = 16ks+4ti, +1 ; k = 2ti+8, 2ti+9 <-> d = 16ks+4ti+2, +3
+          // (the byte order of the e4m3 K operand, see the QK product below)
           const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qp + ks * 16 + 4 * ti));
           const float f0 = __uint_as_float(raw.x << 16), f1 = __uint_as_float(raw.x & 0xffff0000u);
           const float f2 = __uint_as_float(raw.y << 16), f3 = __uint_as_float(raw.y & 0xffff0000u);
-          qf[ks][0] = pack_f16(f0, f2);
-          qf[ks][1] = pack_f16(f1, f3);
+          qf[ks][0] = pack_f16(f0, f1);
+          qf[ks][1] = pack_f16(f2, f3);
         }
       }
     } else {
@@ -431,11 +432,13 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
       uint32_t x[4][4];
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) ldsm_x4(kbase + swz(krow, 2 * kk + (mi >> 1)), x[kk]);
+      // a lane holds dims 4ti..4ti+3 of one key row per word: dims (4ti, 4ti+1)
+      // feed k = (2ti, 2ti+1) and dims (4ti+2, 4ti+3) feed k = (2ti+8, 2ti+9)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t af[4] = {fp8x2_lo(x[kk][0]), fp8x2_lo(x[kk][1]), fp8x2_hi(x[kk][0]), fp8x2_hi(x[kk][1])};
+        uint32_t af[4] = {e4m3x2_lo(x[kk][0]), e4m3x2_lo(x[kk][1]), e4m3x2_hi(x[kk][0]), e4m3x2_hi(x[kk][1])};
         mma_f16(sc, af, qf[2 * kk][0], qf[2 * kk][1]);
-        uint32_t ag[4] = {fp8x2_lo(x[kk][2]), fp8x2_lo(x[kk][3]), fp8x2_hi(x[kk][2]), fp8x2_hi(x[kk][3])};
+        uint32_t ag[4] = {e4m3x2_lo(x[kk][2]), e4m3x2_lo(x[kk][3]), e4m3x2_hi(x[kk][2]), e4m3x2_hi(x[kk][3])};
         mma_f16(sd, ag, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
       }
     }
@@ -495,13 +498,18 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
       }
     } else {
       const int vr = (mi & 1) * 8 + mr;
+      // a lane's word holds keys (2ti, 2ti+1) x dims (2gi, 2gi+1) as bytes
+      // (k, d), (k, d+1), (k+1, d), (k+1, d+1): regroup into one key pair per
+      // dim, so MMA row gi <-> dim 2gi and row gi + 8 <-> dim 2gi + 1
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t x[4];
         ldsm_x4_t(vbase + swz(vr, 2 * cc + (mi >> 1)), x);
-        uint32_t af[4] = {fp8x2_lo(x[0]), fp8x2_hi(x[0]), fp8x2_lo(x[1]), fp8x2_hi(x[1])};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = prmt(x[q], 0u, 0x3120u);
+        uint32_t af[4] = {e4m3x2_lo(x[0]), e4m3x2_hi(x[0]), e4m3x2_lo(x[1]), e4m3x2_hi(x[1])};
         mma_f16(o[2 * cc], af, pb0, pb1);
-        uint32_t ag[4] = {fp8x2_lo(x[2]), fp8x2_hi(x[2]), fp8x2_lo(x[3]), fp8x2_hi(x[3])};
+        uint32_t ag[4] = {e4m3x2_lo(x[2]), e4m3x2_hi(x[2]), e4m3x2_lo(x[3]), e4m3x2_hi(x[3])};
         mma_f16(o[2 * cc + 1], ag, pb0, pb1);
       }
     }

@@ -75,8 +75,8 @@ struct DecodeArgs {
   int32_t* status;
   int32_t n_items, n_groups;
   int32_t batch, T, Hq, Hkv, G, P, max_pages, num_pages, rows, dv;
-  float qk_scale_log2;  // scale * kv_scale * log2(e) (x 256 for FP8, see kernel)
-  float o_scale;        // factor applied to the normalised output (FP8: kv_scale * 256)
+  float qk_scale_log2;  // scale * kv_scale (FP8 only) * log2(e)
+  float o_scale;        // factor applied to the normalised output (FP8: kv_scale)
   int32_t fused;        // 1: last CTA of a group merges
   int32_t kv_box3d;     // bf16 K/V maps are 3-D: one [2][16][64] box per 16-key tile
 };

@@ -164,21 +164,26 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return r;
 }
 
-// e4m3fn -> f16, two at a time, exactly scaled by 2^-8.
-//
-// An e4m3 byte s.eeee.mmm (bias 7) placed in the upper byte of a 16-bit lane
-// and shifted right by one becomes the f16 pattern s.0eeee.mmm0000000 (bias
-// 15): the same bits read as f16 equal the e4m3 value times 2^(7-15).
-// Subnormals map to subnormals (2^-6 * m/8 -> 2^-14 * m/8), so every finite
-// code converts exactly; the 2^8 is folded into the caller's scales.  Codes
-// 0x7F/0xFF (NaN) are not special-cased (they read as +-480 * 2^-8).
-//
-// fp8x2_hi: bytes 1 and 3 of x -> (lo lane, hi lane)
-// fp8x2_lo: bytes 0 and 2 of x -> (lo lane, hi lane)
-__device__ __forceinline__ uint32_t fp8x2_hi(uint32_t x) {
-  return (x & 0x80008000u) | ((x >> 1) & 0x3F803F80u);
+// e4m3fn -> f16, two at a time (the hardware conversion; exact, since every
+// e4m3 value, subnormals included, is an f16 value).  The two codes sit in a
+// 16-bit half of `x`: e4m3x2_lo converts bytes 0 (-> lo lane) and 1 (-> hi
+// lane), e4m3x2_hi bytes 2 and 3.  NaN codes (0x7F/0xFF) become f16 NaN.
+__device__ __forceinline__ uint32_t e4m3x2_lo(uint32_t x) {
+  uint32_t r;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, l;\n}" : "=r"(r) : "r"(x));
+  return r;
 }
-__device__ __forceinline__ uint32_t fp8x2_lo(uint32_t x) { return fp8x2_hi(x << 8); }
+__device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t x) {
+  uint32_t r;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(r) : "r"(x));
+  return r;
+}
+// Byte permutation: result byte i = byte (sel >> 4i) & 7 of the pair (x, y).
+__device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(y), "r"(sel));
+  return r;
+}
 
 
 // ------------------------------------------------------------- clusters
