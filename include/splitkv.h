@@ -87,13 +87,14 @@ typedef struct splitkv_plan_s splitkv_plan_t;
 /* Fields of one work item as returned by splitkv_plan_get_items (int32 each). */
 enum {
   SPLITKV_ITEM_B = 0,         /* sequence                                        */
-  SPLITKV_ITEM_HKV = 1,       /* KV head                                         */
+  SPLITKV_ITEM_HKV = 1,       /* first KV head; the item covers heads [HKV,
+                                 HKV + splitkv_plan_heads_per_item)              */
   SPLITKV_ITEM_SPLIT = 2,     /* split index s in [0, S_b)                       */
   SPLITKV_ITEM_NSPLIT = 3,    /* S_b, splits of this sequence                    */
   SPLITKV_ITEM_PAGE0 = 4,     /* first page (logical, within the sequence)       */
   SPLITKV_ITEM_PAGE1 = 5,     /* one past the last page                          */
   SPLITKV_ITEM_SLOT = 6,      /* partial-result slot, -1 when S_b == 1           */
-  SPLITKV_ITEM_GROUP = 7,     /* combine group of (b, h_kv), -1 when S_b == 1    */
+  SPLITKV_ITEM_GROUP = 7,     /* combine group of (b, HKV), -1 when S_b == 1     */
   SPLITKV_ITEM_FIELDS = 8
 };
 
@@ -104,11 +105,14 @@ enum {
  * num_splits > 0, S_b = min(num_splits, n_b): the request is honoured
  * whenever the sequence has that many pages.  With num_splits == 0 the
  * planner picks one chunk size for all sequences by a load-balance cost model
- * over num_sms SMs (largest-first list scheduling of the work items, plus a
- * per-split merge cost) and S_b = clamp(ceil(n_b / chunk), 1, min(n_b, 64)).
- * Split s covers pages [floor(s*n_b/S_b), floor((s+1)*n_b/S_b)), which is
- * never empty.  Items are ordered longest first.  A sequence with no keys gets
- * one empty item per KV head that writes out = 0, lse = -inf.
+ * (largest-first list scheduling of the work items over the kernel's resident
+ * slots -- 3 CTAs per SM for GQA, one CTA pair per query token for MLA --
+ * plus a fixed cost per item and a per-split merge cost) and S_b = n_b / chunk
+ * rounded up or down, clamped to [1, min(n_b, 64)].  Split s covers pages
+ * [floor(s*n_b/S_b), floor((s+1)*n_b/S_b)), which is never empty.  One work
+ * item covers splitkv_plan_heads_per_item consecutive KV heads of one split.
+ * Items are ordered longest first.  A sequence with no keys gets one empty
+ * item per head group that writes out = 0, lse = -inf.
  *
  *   desc           shapes; copied into the plan
  *   seq_lens_host  [B] int32, 0 <= L <= max_pages_per_seq * P, L >= T or L == 0
@@ -136,6 +140,12 @@ int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
 /* CTAs the split-KV kernel launches for this plan (one per item for GQA; a
  * CTA pair per query token and item for MLA): the rows of the per-CTA log. */
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan);
+
+/* KV heads one work item covers: 4, 2 or 1 (the largest dividing Hkv) for the
+ * e4m3 GQA path, where one TMA box then brings a 16-key tile of all of them;
+ * 1 otherwise.  Partial-result rows of an item are numbered
+ * head_slot * T * G + t * G + g. */
+int32_t splitkv_plan_heads_per_item(const splitkv_plan_t* plan);
 
 /* Kernel launches one splitkv_decode of this plan makes (1 or 2: the split
  * kernel, plus the combine kernel when splits must be merged and the merge

@@ -177,9 +177,9 @@ def attention_direct(q, k_pages, v_pages, block_table, seq_lens, *, scale,
 # --------------------------------------------------------------------------
 
 MAX_SPLITS = 64          # cap on splits per sequence
-ITEM_OVERHEAD = 32       # fixed cost of one split CTA, in 1/16-page units
+ITEM_OVERHEAD = 96       # fixed cost of one work item, in 1/16-page units (6 pages)
 COMBINE_COST = 2         # cost per split of the merge, in 1/16-page units
-MAX_WAVES = 8            # candidate granularities: 1 .. MAX_WAVES items per SM
+MAX_WAVES = 8            # candidate granularities: 1 .. MAX_WAVES items per machine
 
 
 def pages_of(L: int, P: int) -> int:
@@ -195,8 +195,16 @@ def split_ranges(n: int, S: int) -> List[Tuple[int, int]]:
     return [((s * n) // S, ((s + 1) * n) // S) for s in range(S)]
 
 
-def _splits_for(n_pages: Sequence[int], chunk: int) -> List[int]:
-    return [max(1, min(MAX_SPLITS, n, -(-n // chunk))) if n > 0 else 1 for n in n_pages]
+def _splits_for(n_pages: Sequence[int], chunk: int, round_up: bool) -> List[int]:
+    """``S_b = clamp(n_b / chunk rounded up or down, 1, min(n_b, MAX_SPLITS))``."""
+    out = []
+    for n in n_pages:
+        if n <= 0:
+            out.append(1)
+            continue
+        q = -(-n // chunk) if round_up else n // chunk
+        out.append(max(1, min(MAX_SPLITS, n, q)))
+    return out
 
 
 def _makespan(costs: List[int], machines: int) -> int:
@@ -209,59 +217,70 @@ def _makespan(costs: List[int], machines: int) -> int:
 
 
 def choose_splits(n_pages: Sequence[int], num_kv_heads: int, num_sms: int,
-                  ctas_per_item: int = 1) -> List[int]:
+                  ctas_per_item: int = 1, ctas_per_sm: int = 1,
+                  heads_per_item: int = 1) -> List[int]:
     """Automatic split count per sequence (``num_splits == 0``).
 
-    One chunk size ``c`` (pages per split) is used for all sequences and
-    ``S_b = clamp(ceil(n_b / c), 1, min(n_b, MAX_SPLITS))``.  Candidates are
-    ``c_k = ceil(total / (k * num_sms))`` for ``k = 1 .. MAX_WAVES`` (``total``
-    = sum of ``n_b * Hkv``), plus "no split" (``c = max n_b``).  Each candidate
-    is scored as the LPT makespan of its items over ``num_sms`` machines, item
-    cost ``16 * pages + ITEM_OVERHEAD``, plus ``COMBINE_COST * max_b S_b``.
-    The lowest score wins; ties go to the earlier candidate.  When one work
-    item launches several CTAs (the MLA kernel: a CTA pair per query token),
-    the machines are ``max(1, num_sms // ctas_per_item)``.
+    The machine model: ``M = max(1, num_sms * ctas_per_sm // ctas_per_item)``
+    work items run at once (a kernel with several resident CTAs per SM offers
+    that many slots per SM; an item that launches several CTAs takes that many).
+    A split of sequence b is ``U = Hkv / heads_per_item`` items (each covers
+    ``heads_per_item`` KV heads), an item over ``p`` pages costs
+    ``16 * p * heads_per_item + ITEM_OVERHEAD``.
+
+    One chunk size ``c`` (pages per split) is used for all sequences.
+    Candidates are ``c_k = ceil(total / (k * M))`` for ``k = 1 .. MAX_WAVES``
+    (``total = U * sum n_b``), each with ``S_b = n_b / c_k`` rounded up and
+    rounded down (then clamped to ``[1, min(n_b, MAX_SPLITS)]``), and last
+    "no split".  A candidate scores the LPT makespan of its items over ``M``
+    machines plus ``COMBINE_COST * max_b S_b``; the lowest score wins and ties
+    go to the earlier candidate.
     """
-    num_sms = max(1, num_sms // ctas_per_item)
-    total = sum(int(n) for n in n_pages) * num_kv_heads
+    machines = max(1, (num_sms * ctas_per_sm) // ctas_per_item)
+    units = num_kv_heads // heads_per_item
+    total = sum(int(n) for n in n_pages) * units
     nmax = max([int(n) for n in n_pages] + [1])
     cands = []
     for k in range(1, MAX_WAVES + 1):
-        cands.append(max(1, -(-total // (k * num_sms))))
-    cands.append(nmax)
+        c = max(1, -(-total // (k * machines)))
+        cands += [(c, True), (c, False)]
+    cands.append((nmax, True))
     best, best_S = None, None
-    for c in cands:
-        S = _splits_for(n_pages, c)
+    for c, up in cands:
+        S = _splits_for(n_pages, c, up)
         costs = []
         for n, s_b in zip(n_pages, S):
             for (p0, p1) in split_ranges(n, s_b) if n > 0 else [(0, 0)]:
-                costs.extend([16 * (p1 - p0) + ITEM_OVERHEAD] * num_kv_heads)
-        score = _makespan(costs, num_sms) + COMBINE_COST * max(S)
+                costs.extend([16 * (p1 - p0) * heads_per_item + ITEM_OVERHEAD] * units)
+        score = _makespan(costs, machines) + COMBINE_COST * max(S)
         if best is None or score < best:
             best, best_S = score, S
     return best_S
 
 
 def plan_items(seq_lens: Sequence[int], page_size: int, num_kv_heads: int,
-               num_splits: int, num_sms: int,
-               ctas_per_item: int = 1) -> List[Tuple[int, int, int, int, int, int]]:
-    """Work list ``[(b, h_kv, s, S_b, p0, p1)]`` in launch order.
+               num_splits: int, num_sms: int, ctas_per_item: int = 1,
+               ctas_per_sm: int = 1,
+               heads_per_item: int = 1) -> List[Tuple[int, int, int, int, int, int]]:
+    """Work list ``[(b, h0, s, S_b, p0, p1)]`` in launch order.
 
-    ``num_splits > 0``: ``S_b = min(num_splits, n_b)`` -- the requested count
-    is honoured whenever the sequence has that many pages.  ``num_splits ==
-    0``: ``choose_splits``.  A sequence with no keys gets one empty item per KV
-    head (it only writes out = 0, lse = -inf).  Launch order: longest range
-    first, ties by ``(b, h_kv, s)``.
+    An item covers KV heads ``[h0, h0 + heads_per_item)`` of sequence b over
+    pages ``[p0, p1)``.  ``num_splits > 0``: ``S_b = min(num_splits, n_b)`` --
+    the requested count is honoured whenever the sequence has that many pages.
+    ``num_splits == 0``: ``choose_splits``.  A sequence with no keys gets one
+    empty item per head group (it only writes out = 0, lse = -inf).  Launch
+    order: longest range first, ties by ``(b, h0, s)``.
     """
     n_pages = [pages_of(L, page_size) for L in seq_lens]
     if num_splits > 0:
         S = [max(1, min(num_splits, n)) if n > 0 else 1 for n in n_pages]
     else:
-        S = choose_splits(n_pages, num_kv_heads, num_sms, ctas_per_item)
+        S = choose_splits(n_pages, num_kv_heads, num_sms, ctas_per_item, ctas_per_sm,
+                          heads_per_item)
     items = []
     for b, (n, s_b) in enumerate(zip(n_pages, S)):
         rngs = split_ranges(n, s_b) if n > 0 else [(0, 0)]
-        for h in range(num_kv_heads):
+        for h in range(0, num_kv_heads, heads_per_item):
             for s, (p0, p1) in enumerate(rngs):
                 items.append((b, h, s, s_b, p0, p1))
     items.sort(key=lambda it: (-(it[5] - it[4]), it[0], it[1], it[2]))

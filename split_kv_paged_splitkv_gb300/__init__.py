@@ -49,6 +49,7 @@ _SIGNATURES = {
     "splitkv_plan_get_items": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32)]),
     "splitkv_plan_num_items": (_i32, [_vp]),
     "splitkv_plan_num_ctas": (_i32, [_vp]),
+    "splitkv_plan_heads_per_item": (_i32, [_vp]),
     "splitkv_plan_launches_per_call": (_i32, [_vp]),
     "splitkv_workspace_size": (_sz, [_vp]),
     "splitkv_plan_upload": (_i32, [_vp, _vp, _sz, _vp]),
@@ -190,6 +191,10 @@ def splitkv_plan_launches_per_call(plan: Plan) -> int:
 
 def splitkv_plan_num_ctas(plan: Plan) -> int:
     return int(_lib.splitkv_plan_num_ctas(plan.handle))
+
+
+def splitkv_plan_heads_per_item(plan: Plan) -> int:
+    return int(_lib.splitkv_plan_heads_per_item(plan.handle))
 
 
 def splitkv_read_stats(plan: Plan, workspace, stream=None):

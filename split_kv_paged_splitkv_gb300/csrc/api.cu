@@ -80,6 +80,26 @@ splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, in
   return make_kv_map_2d(out, base, fp8, dim, rows);
 }
 
+// 3-D map over e4m3 pages viewed as (dim, key in page, page * Hkv + head),
+// 128-byte swizzle, boxes of [hpi heads][16 keys][128]: one box brings a
+// 16-key tile of hpi consecutive KV heads of one page (2 KB per head).
+splitkv_status make_fp8_map(TmaDesc* out, const void* base, int dim, int P, int64_t page_heads,
+                            int hpi) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap m;
+  cuuint64_t gdim[3] = {cuuint64_t(dim), cuuint64_t(P), cuuint64_t(page_heads)};
+  cuuint64_t gstride[2] = {cuuint64_t(dim), cuuint64_t(dim) * P};
+  cuuint32_t box[3] = {128u, 16u, cuuint32_t(hpi)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  std::memcpy(out, &m, sizeof(m));
+  return SPLITKV_OK;
+}
+
 // 2-D bf16 map over [rows][dim] with boxes of 64 columns x box_rows rows.
 splitkv_status make_bf16_map(TmaDesc* out, const void* base, int dim, int64_t rows, int box_rows) {
   auto fn = encode_fn();
@@ -155,6 +175,17 @@ int ctas_per_item(const splitkv_desc_t& d) {
   return family_of(d) == Family::kMla ? 2 * d.q_tokens : 1;
 }
 
+int ctas_per_sm(const splitkv_desc_t& d) {
+  return family_of(d) == Family::kGqa ? kGqaCtasPerSm : 1;
+}
+
+int heads_per_item(const splitkv_desc_t& d) {
+  if (family_of(d) != Family::kGqa || d.kv_dtype != SPLITKV_FP8_E4M3) return 1;
+  for (int h : {4, 2})
+    if (d.num_kv_heads % h == 0) return h;
+  return 1;
+}
+
 }  // namespace splitkv
 
 using namespace splitkv;
@@ -205,6 +236,10 @@ void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
 int32_t splitkv_plan_num_items(const splitkv_plan_t* plan) { return plan ? plan->n_items : 0; }
 
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan) { return plan ? plan->n_ctas : 0; }
+
+int32_t splitkv_plan_heads_per_item(const splitkv_plan_t* plan) {
+  return plan ? heads_per_item(plan->desc) : 0;
+}
 
 int32_t splitkv_plan_launches_per_call(const splitkv_plan_t* plan) {
   if (!plan) return 0;
@@ -317,18 +352,28 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
     return SPLITKV_OK;
   }
   TmaDesc tk, tv;
-  bool k3 = false, v3 = false;
-  splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total, &k3);
-  if (st != SPLITKV_OK) return st;
-  st = make_kv_map(&tv, v_pages, fp8, d.v_dim, rows_total, &v3);
-  if (st != SPLITKV_OK) return st;
-  if (k3 != v3) {  // keep both maps in the same form
-    if (k3) st = make_kv_map_2d(&tk, k_pages, fp8, d.qk_dim, rows_total);
-    else st = make_kv_map_2d(&tv, v_pages, fp8, d.v_dim, rows_total);
+  a.hpi = heads_per_item(d);
+  a.kv_box3d = 0;
+  if (fp8) {
+    const int64_t page_heads = int64_t(d.num_pages_total) * d.num_kv_heads;
+    splitkv_status st = make_fp8_map(&tk, k_pages, d.qk_dim, d.page_size, page_heads, a.hpi);
     if (st != SPLITKV_OK) return st;
-    k3 = v3 = false;
+    st = make_fp8_map(&tv, v_pages, d.v_dim, d.page_size, page_heads, a.hpi);
+    if (st != SPLITKV_OK) return st;
+  } else {
+    bool k3 = false, v3 = false;
+    splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total, &k3);
+    if (st != SPLITKV_OK) return st;
+    st = make_kv_map(&tv, v_pages, fp8, d.v_dim, rows_total, &v3);
+    if (st != SPLITKV_OK) return st;
+    if (k3 != v3) {  // keep both maps in the same form
+      if (k3) st = make_kv_map_2d(&tk, k_pages, fp8, d.qk_dim, rows_total);
+      else st = make_kv_map_2d(&tv, v_pages, fp8, d.v_dim, rows_total);
+      if (st != SPLITKV_OK) return st;
+      k3 = v3 = false;
+    }
+    a.kv_box3d = k3 ? 1 : 0;
   }
-  a.kv_box3d = k3 ? 1 : 0;
 
   cudaError_t e = launch_gqa(a, tk, tv, fp8, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the split-KV kernel");
@@ -390,7 +435,11 @@ splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* page
   const int64_t rows_total = int64_t(desc->num_pages_total) * desc->num_kv_heads * desc->page_size;
   TmaDesc t;
   bool box3d = false;
-  st = make_kv_map(&t, pages, fp8, row_elems, rows_total, &box3d);
+  if (fp8)
+    st = make_fp8_map(&t, pages, row_elems, desc->page_size,
+                      int64_t(desc->num_pages_total) * desc->num_kv_heads, 1);
+  else
+    st = make_kv_map(&t, pages, fp8, row_elems, rows_total, &box3d);
   if (st != SPLITKV_OK) return st;
   cudaError_t e = launch_debug_gather(t, fp8, box3d, block_table + size_t(b) * desc->max_pages_per_seq,
                                       desc->num_kv_heads, h_kv, desc->page_size, n_keys, dst, stream);

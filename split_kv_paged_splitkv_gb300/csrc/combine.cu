@@ -25,7 +25,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // up to 64 splits), keeps a running maximum across further chunks of splits,
 // and the 4 ways are merged through shared memory at the end.
 //   plan mode (groups != nullptr): group g = blockIdx.x covers slots
-//     slot0 .. slot0+S-1 with `rows` rows each; row n -> (t, head) of (b, h_kv).
+//     slot0 .. slot0+S-1 with `rows` rows each; row n -> (t, head) of (b, the
+//     group's KV heads).
 //   raw mode: one group, S = n_parts, slot0 = 0, output row n.
 constexpr int kCombineThreads = 128;
 constexpr int kWays = 4;
@@ -47,8 +48,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const int b = g[0], hkv = g[1];
     S = g[2];
     slot0 = g[3];
-    const int t = n / G, gg = n - t * G;
-    orow = (size_t(b) * T + t) * Hq + size_t(hkv) * G + gg;
+    // rows are numbered hs * T*G + t * G + gg over the group's heads hkv + hs
+    const int hs = n / (T * G), r = n - hs * (T * G);
+    const int t = r / G, gg = r - t * G;
+    orow = (size_t(b) * T + t) * Hq + size_t(hkv + hs) * G + gg;
   }
   const int tid = threadIdx.x, dl = tid & 31, way = tid >> 5;
   const int d = blockIdx.z * 128 + dl * 4;

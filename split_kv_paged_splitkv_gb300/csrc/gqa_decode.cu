@@ -1,10 +1,12 @@
 // Split-KV partial attention for thin query groups (GQA), sm_103a.
 //
-// One CTA per work item (b, h_kv, split, page range).  The split's pages are
-// streamed HBM -> shared memory by TMA (one 2-D tiled box per 16-key tile of
-// K and of V, 128-byte swizzle so the ldmatrix reads below are bank-conflict
-// free), through a ring of NST stages guarded by mbarriers.  One producer
-// warp issues the copies; four consumer warps take the tiles round-robin.
+// One CTA per work item (b, HPI consecutive KV heads, split, page range).
+// The split's pages are streamed HBM -> shared memory by TMA (one tiled box
+// per 16-key tile of K and of V covering the item's HPI heads, 128-byte
+// swizzle so the ldmatrix reads below are bank-conflict free), through a
+// ring of NST stages guarded by mbarriers.  One producer warp issues the
+// copies.  Consumer warp w serves head slot w % HPI and takes every
+// (NCW / HPI)-th tile: with HPI = 4 each warp owns one head and every tile.
 //
 // Per 16-key tile a consumer warp computes, on the warp tensor-core path:
 //   S^T[16 keys x 8 rows] = K_tile[16 x 128] . Q^T      (m16n8k16, keys on M)
@@ -16,7 +18,8 @@
 // converted to f16 in registers (exact, ptx::e4m3x2_*) and use the f16
 // MMA; BF16 tiles go straight to the bf16 MMA.
 //
-// The four warps' (m, l, O) are merged in shared memory; the item's result is
+// The (m, l, O) of the warps sharing a head are merged in shared memory; the
+// item's result is
 // written as the final bf16 output (S_b == 1) or as an fp32 partial with its
 // natural-log LSE.  With the fused combine, the last CTA of a (b, h_kv) group
 // (atomic ticket, no waiting) merges the group's partials.
@@ -38,32 +41,38 @@ namespace {
 
 using namespace ptx;
 
-// A tile is 16 keys of one KV head: its K rows then its V rows.  A stage --
-// the unit one mbarrier phase covers -- is TPS tiles (32 KB either way).
-// Measured on GB300, one CTA keeps only about one stage's worth of TMA boxes
-// (~32 KB) in flight however deep its ring is, so per-SM bandwidth comes from
-// several CTAs per SM: a small ring (two stages) and 160 threads let three
-// CTAs share an SM.
-template <bool FP8>
+// A tile is 16 keys of the item's HPI KV heads: its K box ([HPI][16 rows])
+// then its V box.  A stage -- the unit one mbarrier phase covers -- is TPS
+// tiles (32 KB).  Measured on GB300, one CTA keeps only about one stage's
+// worth of TMA boxes in flight however deep its ring is, and small boxes
+// stream more slowly than large ones, so per-SM bandwidth comes from several
+// CTAs per SM (a two-stage ring and 160 threads let three CTAs share an SM)
+// and from boxes that span several heads (HPI > 1, e4m3 only).
+template <bool FP8, int HPI>
 struct Gqa {
+  static_assert(HPI == 1 || (FP8 && (HPI == 2 || HPI == 4)), "heads per item");
   static constexpr int D = 128;
   static constexpr int TK = 16;                            // keys per tile
-  static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one K (or V) tile
-  static constexpr int TILE = 2 * KT_BYTES;                // K + V of one tile
-  static constexpr int TPS = FP8 ? 8 : 4;                  // tiles per stage
-  static constexpr int STAGE = TPS * TILE;                 // 32 KB
+  static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one head's K (or V) rows
+  static constexpr int TILE = 2 * HPI * KT_BYTES;          // K + V boxes of one tile
+  static constexpr int STAGE = 32768;
+  static constexpr int TPS = STAGE / TILE;                 // tiles per stage
   static constexpr int NST = 2;                            // stages in the ring
   static constexpr int NCW = 4;                            // consumer warps
+  static constexpr int WPH = NCW / HPI;                    // warps per head slot
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int RING = NST * STAGE;
+  static constexpr int ROWS = 8 * HPI;                     // merge rows (8 per head)
   static constexpr int MERGE = NCW * 8 * D * 4 + NCW * 8 * 2 * 4;
-  static_assert(MERGE + 64 * 8 * 4 <= RING, "merge area and staged LSEs alias the ring");
-  // Warp w takes tiles w, w + NCW, ...: its successive visits to one stage
-  // must be exactly one barrier phase apart (parity waits cannot tell phase k
-  // from k + 2).  That holds when a warp visits every stage in turn (TPS a
-  // multiple of NCW) or steps NCW / TPS stages at a time with that step
-  // dividing NST.
-  static_assert((TPS % NCW == 0) || (NCW % TPS == 0 && NST % (NCW / TPS) == 0),
+  static_assert(MERGE + 64 * ROWS * 4 <= RING, "merge area and staged LSEs alias the ring");
+  // Warp w takes tiles w / HPI, w / HPI + WPH, ...: its successive visits to
+  // one stage must be exactly one barrier phase apart (parity waits cannot
+  // tell phase k from k + 2).  That holds when a warp visits every stage in
+  // turn (TPS a multiple of WPH) or steps WPH / TPS stages at a time with that
+  // step dividing NST.
+  static constexpr bool kVisitsEveryStage = TPS % WPH == 0;
+  static constexpr int kStageStep = WPH >= TPS ? WPH / TPS : 1;
+  static_assert(kVisitsEveryStage || (WPH % TPS == 0 && NST % kStageStep == 0),
                 "stage/warp aliasing");
   static constexpr int BARS = 2 * NST * 8;
   static constexpr int PT_CHUNK = 1024;  // block-table entries staged at a time
@@ -110,30 +119,34 @@ __device__ __forceinline__ void store_row(const float (&acc)[DPT], __nv_bfloat16
   }
 }
 
-// Merges the (m, l, O) of the consumer warps and writes the item's result.
-// Runs on the NT consumer threads: row n = tid / (NT / 8), DPT = 1024 / NT
-// consecutive dims from d0.  `mo` is [NCW][8][128] fp32, `mm`/`ml` [NCW][8];
-// m is in log2 units.
-template <bool FP8>
+// Merges the (m, l, O) of the warps sharing each head slot and writes the
+// item's result.  Runs on the NT = NCW * 32 consumer threads: merge row
+// n = tid / TPR (head slot n / 8, query row n % 8 of that head), DPT =
+// 128 / TPR consecutive dims from d0.  `mo` is [NCW][8][128] fp32, `mm`/`ml`
+// [NCW][8]; m is in log2 units.  Partial rows are numbered hs * T*G + row.
+template <bool FP8, int HPI>
 __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, const float* mo,
-                                                const float* mm, const float* ml, int b, int hkv,
+                                                const float* mm, const float* ml, int b, int h0,
                                                 int slot) {
-  constexpr int NCW = Gqa<FP8>::NCW, NT = NCW * 32, TPR = NT / 8, DPT = 128 / TPR;
-  const int n = tid / TPR;           // query row 0..7
+  using C = Gqa<FP8, HPI>;
+  constexpr int NT = C::NCW * 32, TPR = NT / C::ROWS, DPT = 128 / TPR;
+  const int n = tid / TPR;           // merge row
+  const int hs = n >> 3, r = n & 7;  // head slot, query row of that head
   const int d0 = (tid % TPR) * DPT;  // first of DPT consecutive dims
   float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < NCW; ++w) M = fmaxf(M, mm[w * 8 + n]);
+  for (int j = 0; j < C::WPH; ++j) M = fmaxf(M, mm[(hs + HPI * j) * 8 + r]);
   float acc[DPT];
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
   float lsum = 0.f;
   if (M != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < NCW; ++w) {
-      const float sc = ex2(mm[w * 8 + n] - M);
-      lsum += sc * ml[w * 8 + n];
-      axpy<DPT>(acc, sc, mo + (w * 8 + n) * 128 + d0);
+    for (int j = 0; j < C::WPH; ++j) {
+      const int w = hs + HPI * j;
+      const float sc = ex2(mm[w * 8 + r] - M);
+      lsum += sc * ml[w * 8 + r];
+      axpy<DPT>(acc, sc, mo + (w * 8 + r) * 128 + d0);
     }
   }
   float lse_n = -INFINITY;
@@ -141,46 +154,49 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] *= inv;
   if (lsum > 0.f) lse_n = (M + lg2(lsum)) * kLn2;
-  if (n >= a.rows) return;
+  const int rph = a.T * a.G;  // query rows per head
+  if (r >= rph) return;
   if (slot < 0) {
-    const int t = n / a.G, g = n - (n / a.G) * a.G;
-    const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g;
+    const int t = r / a.G, g = r - (r / a.G) * a.G;
+    const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(h0 + hs) * a.G + g;
     store_row<DPT>(acc, static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0, nullptr);
     if (d0 == 0 && a.lse) a.lse[row] = lse_n;
   } else {
-    store_row<DPT>(acc, nullptr, a.o_part + (size_t(slot) * a.rows + n) * 128 + d0);
-    if (d0 == 0) a.lse_part[size_t(slot) * a.rows + n] = lse_n;
+    const int pr = hs * rph + r;
+    store_row<DPT>(acc, nullptr, a.o_part + (size_t(slot) * a.rows + pr) * 128 + d0);
+    if (d0 == 0) a.lse_part[size_t(slot) * a.rows + pr] = lse_n;
   }
 }
 
-// Log-sum-exp merge of the S partials of one (b, h_kv) group, by the CTA that
-// finished last.  NT threads.  The S x rows LSE values are first staged in
-// shared memory (`sl`, [S][8]) by all threads at once; then thread (row n,
-// DPT dims from d0) accumulates the weighted partials with U splits' loads in
-// flight per step, so the L2 round trips overlap instead of serialising one
-// per split.
-template <int NT>
-__device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int hkv,
+// Log-sum-exp merge of the S partials of one (b, head group) group, by the
+// CTA that finished last.  NT threads over ROWS = 8 * HPI merge rows.  The
+// S x rows LSE values are first staged in shared memory (`sl`, [S][ROWS]) by
+// all threads at once; then thread (row n, DPT dims from d0) accumulates the
+// weighted partials with U splits' loads in flight per step, so the L2 round
+// trips overlap instead of serialising one per split.
+template <int NT, int HPI>
+__device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int h0,
                                             int slot0, int S, float* sl) {
-  constexpr int TPR = NT / 8, DPT = 128 / TPR, U = 8;
-  const int rows = a.rows;
-  for (int i = tid; i < S * 8; i += NT) {
-    const int s = i >> 3, n = i & 7;
-    sl[i] = n < rows ? __ldcg(a.lse_part + size_t(slot0 + s) * rows + n) : -INFINITY;
+  constexpr int ROWS = 8 * HPI, TPR = NT / ROWS, DPT = 128 / TPR, U = 64 / DPT;
+  const int rows = a.rows, rph = a.T * a.G;
+  for (int i = tid; i < S * ROWS; i += NT) {
+    const int s = i / ROWS, n = i % ROWS, hs = n >> 3, r = n & 7;
+    sl[i] = r < rph ? __ldcg(a.lse_part + size_t(slot0 + s) * rows + hs * rph + r) : -INFINITY;
   }
   asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
   const int n = tid / TPR;
+  const int hs = n >> 3, r = n & 7;
   const int d0 = (tid % TPR) * DPT;
-  if (n >= rows) return;
+  if (r >= rph) return;
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, sl[s * 8 + n]);
+  for (int s = 0; s < S; ++s) M = fmaxf(M, sl[s * ROWS + n]);
   float acc[DPT];
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
     const size_t stride = size_t(rows) * 128;
-    const float* base = a.o_part + (size_t(slot0) * rows + n) * 128 + d0;
+    const float* base = a.o_part + (size_t(slot0) * rows + hs * rph + r) * 128 + d0;
     for (int s0 = 0; s0 < S; s0 += U) {
       float4 x[U][DPT / 4];
 #pragma unroll
@@ -192,7 +208,7 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (s0 + u < S) {
-          const float w = ex2((sl[(s0 + u) * 8 + n] - M) * kLog2e);
+          const float w = ex2((sl[(s0 + u) * ROWS + n] - M) * kLog2e);
           wsum += w;
 #pragma unroll
           for (int v = 0; v < DPT / 4; ++v) {
@@ -208,17 +224,17 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] *= inv;
   if (wsum > 0.f) lse_n = M + lg2(wsum) * kLn2;
-  const int t = n / a.G, g = n - (n / a.G) * a.G;
-  const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g;
+  const int t = r / a.G, g = r - (r / a.G) * a.G;
+  const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(h0 + hs) * a.G + g;
   store_row<DPT>(acc, static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0, nullptr);
   if (d0 == 0 && a.lse) a.lse[row] = lse_n;
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
+template <bool FP8, int HPI>
+__global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
     gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
-  using C = Gqa<FP8>;
+  using C = Gqa<FP8, HPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* it = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
-  const int b = it[SPLITKV_ITEM_B], hkv = it[SPLITKV_ITEM_HKV];
+  const int b = it[SPLITKV_ITEM_B], h0 = it[SPLITKV_ITEM_HKV];  // heads h0 .. h0+HPI-1
   const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
   const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
   const int slot = it[SPLITKV_ITEM_SLOT], group = it[SPLITKV_ITEM_GROUP];
@@ -242,7 +258,7 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), C::TPS);  // one arrival per consumed tile
+      mbar_init(smem_u32(empty + s), C::TPS * HPI);  // one arrival per tile and head
     }
     misc[0] = 0;
     misc[1] = 0;
@@ -304,12 +320,14 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
             stages = j + 1;
           }
           const uint32_t dk = smem_u32(ring + st * C::STAGE + u * C::TILE);
-          const uint32_t dv = dk + C::KT_BYTES;
-          const int row = (ph * a.Hkv + hkv) * a.P + (key0 - page * a.P);
-          if (FP8) {
-            tma_load_2d(dk, &tk, bar, 0, row);
-            tma_load_2d(dv, &tv, bar, 0, row);
-          } else if (a.kv_box3d) {  // one [2 halves][16 rows][64] box per tile
+          const uint32_t dv = dk + HPI * C::KT_BYTES;
+          if (FP8) {  // [HPI heads][16 rows][128] of the map (dim, key in page, page*Hkv + head)
+            tma_load_3d(dk, &tk, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
+            tma_load_3d(dv, &tv, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
+            continue;
+          }
+          const int row = (ph * a.Hkv + h0) * a.P + (key0 - page * a.P);
+          if (a.kv_box3d) {  // one [2 halves][16 rows][64] box per tile
             tma_load_3d(dk, &tk, bar, 0, row, 0);
             tma_load_3d(dv, &tv, bar, 0, row, 0);
           } else {
@@ -342,6 +360,8 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
   // ------------------------------------------------------------------ consumers
   const int tid = threadIdx.x;  // consumer threads 0 .. NCW*32-1
   const int gi = lane >> 2, ti = lane & 3;
+  const int hs = warp % HPI;    // head slot: this warp serves KV head h0 + hs
+  const int hkv = h0 + hs;
 
   // Q^T operand fragments: row n = gi, dims by ti (see the layout notes).
   uint32_t qf[8][2];
@@ -386,18 +406,18 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int keys_scored = 0;
 
-  for (int i = warp; i < n_tiles; i += C::NCW) {
+  for (int i = warp / HPI; i < n_tiles; i += C::WPH) {
     const int j = i / C::TPS, st = j % C::NST;
     const bool arrived = __all_sync(kFull, mbar_wait(smem_u32(full + st), (j / C::NST) & 1));
     if (!arrived) {
       if (lane == 0) atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
       break;
     }
-    uint8_t* kt = ring + st * C::STAGE + (i - j * C::TPS) * C::TILE;
-    uint8_t* vt = kt + C::KT_BYTES;
+    uint8_t* kt = ring + st * C::STAGE + (i - j * C::TPS) * C::TILE + hs * C::KT_BYTES;
+    uint8_t* vt = kt + HPI * C::KT_BYTES;
     const int key0 = k_begin + i * 16;
     const int valid = min(16, k_end - key0);
-    keys_scored += valid;
+    if (hs == 0) keys_scored += valid;
     if (valid < 16) {
       // Slots past the last visible key may hold anything (even NaN): zero
       // those V rows so that 0 * V stays 0 in the PV product.
@@ -554,7 +574,7 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
     ml[warp * 8 + 2 * ti + 1] = l1;
   }
   asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-  merge_and_store<FP8>(a, tid, mo, mm, ml, b, hkv, slot);
+  merge_and_store<FP8, HPI>(a, tid, mo, mm, ml, b, h0, slot);
 
   int merged = 0;
   if (slot >= 0 && a.fused) {
@@ -565,8 +585,9 @@ __global__ void __launch_bounds__(Gqa<FP8>::THREADS, 3)
     if (misc[0]) {
       __threadfence();
       // staged LSE values go past the warp-merge area at the start of the ring
-      merge_group<C::NCW * 32>(a, tid, b, hkv, slot - split, nsplit,
-                               reinterpret_cast<float*>(ring) + C::NCW * 8 * 128 + 2 * C::NCW * 8);
+      merge_group<C::NCW * 32, HPI>(a, tid, b, h0, slot - split, nsplit,
+                                    reinterpret_cast<float*>(ring) + C::NCW * 8 * 128 +
+                                        2 * C::NCW * 8);
       if (tid == 0) a.tickets[group] = 0;
       merged = 1;
     }
@@ -588,7 +609,7 @@ __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant
                                                            const int32_t* table_row, int Hkv,
                                                            int h_kv, int P, int n_keys,
                                                            uint8_t* dst, int32_t* status, int box3d) {
-  constexpr int KT = Gqa<FP8>::KT_BYTES;
+  constexpr int KT = Gqa<FP8, 1>::KT_BYTES;
   __shared__ __align__(1024) uint8_t tile[KT];
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
@@ -603,7 +624,9 @@ __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant
       const int ph = table_row[key0 / P];
       const int row = (ph * Hkv + h_kv) * P + key0 % P;
       mbar_arrive_expect_tx(smem_u32(&bar), KT);
-      if (!FP8 && box3d) {
+      if (FP8) {  // the decode kernel's e4m3 map: (dim, key in page, page * Hkv + head)
+        tma_load_3d(smem_u32(tile), &tm, smem_u32(&bar), 0, key0 % P, ph * Hkv + h_kv);
+      } else if (box3d) {
         tma_load_3d(smem_u32(tile), &tm, smem_u32(&bar), 0, row, 0);
       } else {
         tma_load_2d(smem_u32(tile), &tm, smem_u32(&bar), 0, row);
@@ -632,38 +655,48 @@ __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant
 
 }  // namespace
 
+namespace {
+
+// One-time shared-memory opt-in of an instantiation, then a launch with
+// programmatic dependent launch: the kernel's prologue may overlap the tail
+// of the previous kernel on the stream; it waits (griddepcontrol.wait)
+// before touching anything that kernel could have written.
+template <bool FP8, int HPI>
+cudaError_t launch_gqa_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                         cudaStream_t s) {
+  using C = Gqa<FP8, HPI>;
+  // The shared-memory opt-in is a per-process attribute: set it on first use only.
+  static cudaError_t attr = cudaFuncSetAttribute(
+      gqa_splitkv_kernel<FP8, HPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (attr != cudaSuccess) return attr;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_items, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = la;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<FP8, HPI>, a, mk, mv);
+}
+
+}  // namespace
+
 cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv, bool fp8,
                        void* stream) {
   const CUtensorMap& mk = *reinterpret_cast<const CUtensorMap*>(&tk);
   const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(&tv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.n_items == 0) return cudaSuccess;
-  // The shared-memory opt-in is a per-process attribute: set it on first use only.
-  static cudaError_t attr_bf16 = cudaFuncSetAttribute(
-      gqa_splitkv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<false>::SMEM);
-  static cudaError_t attr_fp8 = cudaFuncSetAttribute(
-      gqa_splitkv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gqa<true>::SMEM);
-  // Programmatic dependent launch: the kernel's prologue may overlap the tail
-  // of the previous kernel on the stream; it waits (griddepcontrol.wait)
-  // before touching anything that kernel could have written.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_items, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (fp8) {
-    if (attr_fp8 != cudaSuccess) return attr_fp8;
-    cfg.blockDim = dim3(Gqa<true>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Gqa<true>::SMEM;
-    return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<true>, a, mk, mv);
+  if (!fp8) return a.hpi == 1 ? launch_gqa_t<false, 1>(a, mk, mv, s) : cudaErrorInvalidValue;
+  switch (a.hpi) {
+    case 1: return launch_gqa_t<true, 1>(a, mk, mv, s);
+    case 2: return launch_gqa_t<true, 2>(a, mk, mv, s);
+    case 4: return launch_gqa_t<true, 4>(a, mk, mv, s);
+    default: return cudaErrorInvalidValue;
   }
-  if (attr_bf16 != cudaSuccess) return attr_bf16;
-  cfg.blockDim = dim3(Gqa<false>::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Gqa<false>::SMEM;
-  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<false>, a, mk, mv);
 }
 
 cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, bool box3d, const int32_t* table_row,

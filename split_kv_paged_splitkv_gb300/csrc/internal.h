@@ -12,10 +12,11 @@
 namespace splitkv {
 
 constexpr int kMaxSplits = 64;     // cap on splits per sequence
-constexpr int kItemOverhead = 32;  // planner: fixed cost of one split CTA, 1/16-page units
+constexpr int kItemOverhead = 96;  // planner: fixed cost of one work item, 1/16-page units
 constexpr int kCombineCost = 2;    // planner: merge cost per split, 1/16-page units
-constexpr int kMaxWaves = 8;       // planner: candidate granularities, 1..8 items per SM
-constexpr int kGroupFields = 4;    // {b, h_kv, S_b, first slot}
+constexpr int kMaxWaves = 8;       // planner: candidate granularities, 1..8 items per slot
+constexpr int kGqaCtasPerSm = 3;   // resident CTAs per SM of the GQA kernel
+constexpr int kGroupFields = 4;    // {b, first h_kv, S_b, first slot}
 constexpr int kLogFields = 4;      // per-CTA log record
 constexpr size_t kAlign = 256;
 
@@ -24,13 +25,21 @@ enum class Family { kGqa, kMla, kNone };
 
 Family family_of(const splitkv_desc_t& d);
 
-// Query rows one work item produces: T * G.
+// KV heads one work item covers (consecutive, from the item's h_kv): for the
+// e4m3 GQA path the largest of 4, 2, 1 dividing Hkv, so that one TMA box
+// brings a 16-key tile of all of them; otherwise 1.
+int heads_per_item(const splitkv_desc_t& d);
+
+// Query rows one work item produces: heads_per_item * T * G.
 inline int rows_per_item(const splitkv_desc_t& d) {
-  return d.q_tokens * (d.num_q_heads / d.num_kv_heads);
+  return heads_per_item(d) * d.q_tokens * (d.num_q_heads / d.num_kv_heads);
 }
 
 // CTAs launched per work item (1 for GQA; token tiles x CTA pair for MLA).
 int ctas_per_item(const splitkv_desc_t& d);
+
+// Resident CTAs per SM the planner counts on (kGqaCtasPerSm for GQA, 1 for MLA).
+int ctas_per_sm(const splitkv_desc_t& d);
 
 }  // namespace splitkv
 
@@ -79,6 +88,7 @@ struct DecodeArgs {
   float o_scale;        // factor applied to the normalised output (FP8: kv_scale)
   int32_t fused;        // 1: last CTA of a group merges
   int32_t kv_box3d;     // bf16 K/V maps are 3-D: one [2][16][64] box per 16-key tile
+  int32_t hpi;          // KV heads per item (e4m3 boxes are [hpi][16][128])
 };
 
 // Raw 128-byte tensor map storage (CUtensorMap), built by the API layer.

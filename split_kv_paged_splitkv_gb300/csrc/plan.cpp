@@ -23,8 +23,10 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-// Splits per sequence for one chunk size (pages per split).
-std::vector<int32_t> splits_for_chunk(const std::vector<int32_t>& n_pages, int64_t chunk) {
+// Splits per sequence for one chunk size (pages per split), n_b / chunk
+// rounded up or down, clamped to [1, min(n_b, kMaxSplits)].
+std::vector<int32_t> splits_for_chunk(const std::vector<int32_t>& n_pages, int64_t chunk,
+                                      bool round_up) {
   std::vector<int32_t> S(n_pages.size());
   for (size_t b = 0; b < n_pages.size(); ++b) {
     const int64_t n = n_pages[b];
@@ -32,7 +34,7 @@ std::vector<int32_t> splits_for_chunk(const std::vector<int32_t>& n_pages, int64
       S[b] = 1;
       continue;
     }
-    int64_t s = ceil_div(n, chunk);
+    int64_t s = round_up ? ceil_div(n, chunk) : n / chunk;
     s = std::min<int64_t>(s, std::min<int64_t>(n, kMaxSplits));
     S[b] = static_cast<int32_t>(std::max<int64_t>(s, 1));
   }
@@ -61,40 +63,44 @@ inline int32_t split_edge(int64_t s, int64_t n, int64_t S) {
 }
 
 // Automatic choice: one chunk size for the whole batch, scored by the
-// makespan of its items on `sms` SMs plus a per-split merge charge.
-std::vector<int32_t> choose_splits(const std::vector<int32_t>& n_pages, int hkv, int sms_total,
-                                   int ctas_per_item) {
-  // An item that launches several CTAs occupies that many SMs' worth of slots.
-  const int sms = std::max(1, sms_total / ctas_per_item);
+// makespan of its items on the machine's work-item slots plus a per-split
+// merge charge.  `slots` = items that run at once; a split is `units` items
+// of `hpi` KV heads each.
+std::vector<int32_t> choose_splits(const std::vector<int32_t>& n_pages, int units, int hpi,
+                                   int slots) {
   int64_t total = 0, nmax = 1;
   for (int32_t n : n_pages) {
     total += n;
     nmax = std::max<int64_t>(nmax, n);
   }
-  total *= hkv;
-  std::vector<int64_t> cands;
-  for (int k = 1; k <= kMaxWaves; ++k) cands.push_back(std::max<int64_t>(1, ceil_div(total, int64_t(k) * sms)));
-  cands.push_back(nmax);
+  total *= units;
+  std::vector<std::pair<int64_t, bool>> cands;
+  for (int k = 1; k <= kMaxWaves; ++k) {
+    const int64_t c = std::max<int64_t>(1, ceil_div(total, int64_t(k) * slots));
+    cands.push_back({c, true});
+    cands.push_back({c, false});
+  }
+  cands.push_back({nmax, true});
 
   std::vector<int32_t> best_S;
   int64_t best = -1;
-  for (int64_t chunk : cands) {
-    std::vector<int32_t> S = splits_for_chunk(n_pages, chunk);
+  for (const auto& cand : cands) {
+    std::vector<int32_t> S = splits_for_chunk(n_pages, cand.first, cand.second);
     std::vector<int64_t> costs;
     int32_t smax = 1;
     for (size_t b = 0; b < n_pages.size(); ++b) {
       const int64_t n = n_pages[b];
       smax = std::max(smax, S[b]);
       if (n <= 0) {
-        for (int h = 0; h < hkv; ++h) costs.push_back(kItemOverhead);
+        for (int u = 0; u < units; ++u) costs.push_back(kItemOverhead);
         continue;
       }
       for (int32_t s = 0; s < S[b]; ++s) {
         const int64_t pages = split_edge(s + 1, n, S[b]) - split_edge(s, n, S[b]);
-        for (int h = 0; h < hkv; ++h) costs.push_back(16 * pages + kItemOverhead);
+        for (int u = 0; u < units; ++u) costs.push_back(16 * pages * hpi + kItemOverhead);
       }
     }
-    const int64_t score = lpt_makespan(costs, sms) + int64_t(kCombineCost) * smax;
+    const int64_t score = lpt_makespan(costs, slots) + int64_t(kCombineCost) * smax;
     if (best < 0 || score < best) {
       best = score;
       best_S = S;
@@ -108,6 +114,7 @@ std::vector<int32_t> choose_splits(const std::vector<int32_t>& n_pages, int hkv,
 void build_plan(splitkv_plan_s* p) {
   const splitkv_desc_t& d = p->desc;
   const int B = d.batch, hkv = d.num_kv_heads, P = d.page_size;
+  const int hpi = heads_per_item(d);  // an item covers KV heads [h0, h0 + hpi)
   std::vector<int32_t> n_pages(B);
   for (int b = 0; b < B; ++b) n_pages[b] = static_cast<int32_t>(ceil_div(p->seq_lens[b], P));
 
@@ -115,7 +122,9 @@ void build_plan(splitkv_plan_s* p) {
   if (p->num_splits > 0) {
     for (int b = 0; b < B; ++b) S[b] = n_pages[b] > 0 ? std::min(p->num_splits, n_pages[b]) : 1;
   } else {
-    S = choose_splits(n_pages, hkv, p->num_sms, ctas_per_item(d));
+    // An item that launches several CTAs takes that many of the resident slots.
+    const int slots = std::max(1, p->num_sms * ctas_per_sm(d) / ctas_per_item(d));
+    S = choose_splits(n_pages, hkv / hpi, hpi, slots);
   }
 
   // Combine groups and partial slots, in (b, h_kv) order.
@@ -124,7 +133,7 @@ void build_plan(splitkv_plan_s* p) {
   int32_t slots = 0;
   for (int b = 0; b < B; ++b) {
     if (n_pages[b] <= 0 || S[b] <= 1) continue;
-    for (int h = 0; h < hkv; ++h) {
+    for (int h = 0; h < hkv; h += hpi) {
       group_of[size_t(b) * hkv + h] = static_cast<int32_t>(p->groups.size() / kGroupFields);
       slot_of[size_t(b) * hkv + h] = slots;
       p->groups.insert(p->groups.end(), {b, h, S[b], slots});
@@ -140,7 +149,7 @@ void build_plan(splitkv_plan_s* p) {
   std::vector<Item> items;
   for (int b = 0; b < B; ++b) {
     const int64_t n = n_pages[b];
-    for (int h = 0; h < hkv; ++h) {
+    for (int h = 0; h < hkv; h += hpi) {
       const int32_t g = group_of[size_t(b) * hkv + h];
       const int32_t slot0 = slot_of[size_t(b) * hkv + h];
       if (n <= 0) {

@@ -32,18 +32,31 @@ def _desc(B=1, T=1, Hq=16, Hkv=2, D=128, Dv=128, P=16, maxp=512, N=600, fp8=Fals
                          skv.SPLITKV_FP8_E4M3 if fp8 else skv.SPLITKV_BF16, int(mla), mode)
 
 
-def _oracle_items(lens, P, Hkv, S, sms):
-    return np.array(oracle.plan_items(list(lens), P, Hkv, S, sms), dtype=np.int32).reshape(-1, 6)
+# Resident CTAs per SM the library's planner counts on for the GQA kernel
+# (launch bounds and shared memory of the kernel allow three).
+GQA_CTAS_PER_SM = 3
 
 
-def _check_plan(lens, P, Hkv, S, sms, Hq=None):
-    Hq = Hq or Hkv * 8 if Hkv * 8 <= 64 else Hkv
+def _expected_hpi(Hkv, fp8):
+    if not fp8:
+        return 1
+    return next(h for h in (4, 2, 1) if Hkv % h == 0)
+
+
+def _oracle_items(lens, P, Hkv, S, sms, hpi=1):
+    return np.array(oracle.plan_items(list(lens), P, Hkv, S, sms, ctas_per_sm=GQA_CTAS_PER_SM,
+                                      heads_per_item=hpi), dtype=np.int32).reshape(-1, 6)
+
+
+def _check_plan(lens, P, Hkv, S, sms, Hq=None, fp8=False):
     maxp = max(1, max(-(-int(L) // P) for L in lens))
     d = _desc(B=len(lens), Hq=Hkv * (8 if Hq is None else Hq // Hkv), Hkv=Hkv, P=P, maxp=maxp,
-              N=max(1, sum(-(-int(L) // P) for L in lens)))
+              N=max(1, sum(-(-int(L) // P) for L in lens)), fp8=fp8)
     plan = skv.splitkv_plan(d, np.array(lens, np.int32), S, sms)
+    hpi = skv.splitkv_plan_heads_per_item(plan)
+    assert hpi == _expected_hpi(Hkv, fp8)
     items = skv.splitkv_plan_get_items(plan)
-    ref = _oracle_items(lens, P, Hkv, S, sms)
+    ref = _oracle_items(lens, P, Hkv, S, sms, hpi)
     assert items.shape[0] == ref.shape[0]
     assert np.array_equal(items[:, :6], ref), (lens, S)
     return items
@@ -59,13 +72,13 @@ def test_plan_matches_oracle_gqa_ctx5900(S):
 
 
 @pytest.mark.parametrize("w", ["tiny_gqa_ctx260", "fp8_batch8_ctx32k", "mixed_batch32_bf16",
-                               "mla_t6_ctx64k"])
+                               "mixed_batch32_fp8"])
 @pytest.mark.parametrize("sms", [148, 152])
 def test_plan_matches_oracle_workloads(w, sms):
     wl = workloads.WORKLOADS[w]
     lens = workloads.draw_seq_lens(wl, np.random.default_rng(wl.seed))
     for S in wl.splits:
-        _check_plan(lens, wl.page_size, wl.num_kv_heads, S, sms)
+        _check_plan(lens, wl.page_size, wl.num_kv_heads, S, sms, fp8=wl.kv_dtype == "fp8_e4m3")
 
 
 def test_plan_matches_oracle_random_batches():
@@ -78,7 +91,7 @@ def test_plan_matches_oracle_random_batches():
         Hkv = int(rng.choice([1, 2, 4, 8]))
         S = int(rng.choice([0, 0, 1, 3, 7, 64]))
         sms = int(rng.choice([1, 7, 148, 152]))
-        _check_plan(list(lens), P, Hkv, S, sms)
+        _check_plan(list(lens), P, Hkv, S, sms, fp8=bool(rng.random() < 0.5))
 
 
 def test_plan_slots_and_groups_are_consistent():

@@ -87,7 +87,8 @@ def test_split_ranges_and_nonempty_ctas():
         s.run()
         log, status = s.stats()
         items = skv.splitkv_plan_get_items(s.plan)
-        ref = np.array(oracle.plan_items(list(x.seq_lens_host), 16, 2, S, _sms()), np.int32)
+        ref = np.array(oracle.plan_items(list(x.seq_lens_host), 16, 2, S, _sms(), ctas_per_sm=3),
+                       np.int32)
         assert np.array_equal(items[:, :6], ref)
         assert np.array_equal(log[:, 0], items[:, 4]) and np.array_equal(log[:, 1], items[:, 5])
         n_pages = 369

@@ -371,6 +371,36 @@ def test_auto_splits_fill_the_machine_for_few_heads():
     assert all(it[5] > it[4] for it in items1)
 
 
+def test_auto_splits_count_resident_slots():
+    """One 100-page sequence, one KV head, 4 SMs.  Worked by hand with the
+    cost model (item = 16 * pages + ITEM_OVERHEAD, plus COMBINE_COST * S):
+    one resident CTA per SM -> 4 splits of 25 pages (504 beats 608 for 8
+    splits); two per SM -> 8 machines, 8 splits of 12-13 pages (320)."""
+    assert O.choose_splits([100], 1, 4, ctas_per_sm=1) == [4]
+    assert O.choose_splits([100], 1, 4, ctas_per_sm=2) == [8]
+    # an item that needs two CTAs halves the machines again
+    assert O.choose_splits([100], 1, 4, ctas_per_item=2, ctas_per_sm=2) == [4]
+
+
+def test_head_groups_share_the_sequence_ranges():
+    lens = [5900, 300, 0]
+    for S in (0, 1, 4):
+        items = O.plan_items(lens, 16, 8, S, 152, ctas_per_sm=3, heads_per_item=4)
+        assert sorted(set(it[1] for it in items)) == [0, 4]
+        for b, L in enumerate(lens):
+            n = O.pages_of(L, 16)
+            rr = {h: sorted((it[4], it[5]) for it in items if it[0] == b and it[1] == h)
+                  for h in (0, 4)}
+            assert rr[0] == rr[4]
+            if n:
+                assert rr[0][0][0] == 0 and rr[0][-1][1] == n
+                assert all(p1 > p0 for p0, p1 in rr[0])
+                if S:
+                    assert len(rr[0]) == min(S, n)
+            else:
+                assert rr[0] == [(0, 0)]
+
+
 # ---------------------------------------------------------------- pin strength
 
 def _pins_on_direct():
