@@ -111,12 +111,29 @@ def algorithmic_bytes(w: workloads.Workload, lens: np.ndarray) -> int:
     return kv + q
 
 
+def algorithmic_flops(w: workloads.Workload, lens: np.ndarray) -> float:
+    """Multiply-add FLOPs of QK^T and PV over the visible keys of one call
+    (query token t of a sequence of length L sees L - T + 1 + t keys)."""
+    vis = 0
+    for L in lens.astype(np.int64):
+        for t in range(w.q_tokens):
+            vis += max(0, int(L) - w.q_tokens + 1 + t)
+    return 2.0 * w.num_q_heads * vis * (w.qk_dim + w.v_dim)
+
+
+def is_tensor_bound(w: workloads.Workload) -> bool:
+    """The MLA shape (128 heads x T tokens on one latent head) is a dense
+    contraction (about 1,450 FLOP per KV byte); the GQA shapes stream KV."""
+    return w.num_kv_heads == 1 and w.num_q_heads >= 64 and w.qk_dim > w.v_dim
+
+
 def measured_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, kind)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -328,11 +345,22 @@ def run_ours(args, rank, world, local):
 
     # roofline of the split-KV kernel
     nbytes = algorithmic_bytes(w, x.seq_lens_host)
-    peak, peak_kind = measured_peaks()
+    nflops = algorithmic_flops(w, x.seq_lens_host)
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
     # The split-KV kernel's average launch duration: timed-region time per call
     # (an upper bound when the combine kernel shares the step; see profiles/).
     launch_us = us_per_call_local
-    achieved = nbytes / (launch_us * 1e-6) / 1e9
+    if is_tensor_bound(w):
+        roof = {"bound": "tensor", "achieved": nflops / (launch_us * 1e-6) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "algorithmic_flops": nflops,
+                "hbm_gbs": nbytes / (launch_us * 1e-6) / 1e9, "kernel": "mla_splitkv_kernel"}
+    else:
+        achieved = nbytes / (launch_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "kernel": "gqa_splitkv_kernel"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": None, "duration_basis": "timed-region time per call (all launches of a step)",
+                 "peak_kind": peak_kind, "algorithmic_bytes": nbytes})
 
     # end to end: host buffers, copies inside the timed region
     e2e = run_e2e(args, x, sess, dev)
@@ -349,12 +377,7 @@ def run_ours(args, rank, world, local):
                    "combine": args.combine, "parallelism": f"replicas{world}",
                    "l2": f"inputs rotate over {R} KV pools ({R * pool_bytes / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
                    "timing": "CUDA-graph replay of back-to-back calls, CUDA events on the launching stream"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "duration_basis": "timed-region time per call (all launches of a step)",
-                     "peak_kind": peak_kind, "algorithmic_bytes": nbytes,
-                     "kernel": "gqa_splitkv_kernel",
-                     "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS},
+        "roofline": roof,
         "nonempty_cta_fraction": nonempty,
         "gpu_launches": K * launches_per_step,
         "e2e": e2e,

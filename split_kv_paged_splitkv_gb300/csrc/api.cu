@@ -336,16 +336,14 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
   if (family_of(d) == Family::kMla) {
-    // Latent cache rows of 576 bf16 (64-key boxes = one page); query rows of
-    // 576 bf16 (128-head boxes = one token).  The partials are always merged
-    // by the separate combine kernel.
-    TmaDesc tq, tk;
-    splitkv_status st = make_bf16_map(&tq, q, d.qk_dim, int64_t(d.batch) * d.q_tokens * d.num_q_heads, 128);
-    if (st != SPLITKV_OK) return st;
-    st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, 64);
+    // Latent cache rows of 576 bf16 (64-key boxes = one page); the query rows
+    // are read by the kernel's threads.  The partials are always merged by
+    // the separate combine kernel.
+    TmaDesc tk;
+    splitkv_status st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, 64);
     if (st != SPLITKV_OK) return st;
     a.fused = 0;
-    cudaError_t e = launch_mla(a, tq, tk, stream);
+    cudaError_t e = launch_mla(a, tk, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the MLA split-KV kernel");
     e = launch_combine(a, true, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");

@@ -98,7 +98,7 @@ struct alignas(64) TmaDesc {
 
 cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv, bool fp8,
                        void* stream);
-cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tq, const TmaDesc& tk, void* stream);
+cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, void* stream);
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
                                int dv, void* out_bf16, float* out_f32, float* lse_out,
