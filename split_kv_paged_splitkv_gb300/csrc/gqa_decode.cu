@@ -283,8 +283,10 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
   if (warp == C::NCW) {
     // ---------------------------------------------------------------- producer
     // The warp stages up to PT_CHUNK physical page ids of this item in shared
-    // memory (coalesced loads); then lane 0 alone walks the tiles, arming each
-    // stage's barrier and issuing the tile boxes.
+    // memory (coalesced loads); then the whole warp walks the tiles, arming
+    // each stage's barrier and issuing the tile boxes from one elected lane
+    // (copies issued by a converged warp cost a fraction of the issue cycles
+    // of copies issued by a lane that branched away from its warp).
     const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
     const int pg_end = (k_end + a.P - 1) / a.P;
     const int tiles_per_page = a.P >> 4;
@@ -302,44 +304,42 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
         pt[x] = ph;
       }
       __syncwarp();
-      if (lane == 0) {
-        const int t_end = min(n_tiles, (pc + cnt) * tiles_per_page - p0 * tiles_per_page);
-        for (; t < t_end; ++t) {
-          const int key0 = k_begin + t * 16;
-          const int page = key0 / a.P;
-          const int ph = pt[page - pc];
-          const int j = t / C::TPS, u = t - j * C::TPS, st = j % C::NST;
-          const uint32_t bar = smem_u32(full + st);
-          if (u == 0) {
-            if (j >= C::NST && !mbar_wait(smem_u32(empty + st), ((j / C::NST) - 1) & 1)) {
-              atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
-              ok = false;
+      const int t_end = min(n_tiles, (pc + cnt) * tiles_per_page - p0 * tiles_per_page);
+      for (; t < t_end; ++t) {
+        const int key0 = k_begin + t * 16;
+        const int page = key0 / a.P;
+        const int ph = pt[page - pc];
+        const int j = t / C::TPS, u = t - j * C::TPS, st = j % C::NST;
+        const uint32_t bar = smem_u32(full + st);
+        if (u == 0) {
+          if (j >= C::NST) {
+            ok = __all_sync(kFull, mbar_wait(smem_u32(empty + st), ((j / C::NST) - 1) & 1));
+            if (!ok) {
+              if (lane == 0) atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
               break;
             }
-            mbar_arrive_expect_tx(bar, min(C::TPS, n_tiles - t) * C::TILE);
-            stages = j + 1;
           }
-          const uint32_t dk = smem_u32(ring + st * C::STAGE + u * C::TILE);
-          const uint32_t dv = dk + HPI * C::KT_BYTES;
-          if (FP8) {  // [HPI heads][16 rows][128] of the map (dim, key in page, page*Hkv + head)
-            tma_load_3d(dk, &tk, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
-            tma_load_3d(dv, &tv, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
-            continue;
-          }
-          const int row = (ph * a.Hkv + h0) * a.P + (key0 - page * a.P);
-          if (a.kv_box3d) {  // one [2 halves][16 rows][64] box per tile
-            tma_load_3d(dk, &tk, bar, 0, row, 0);
-            tma_load_3d(dv, &tv, bar, 0, row, 0);
-          } else {
-            tma_load_2d(dk, &tk, bar, 0, row);
-            tma_load_2d(dk + 2048, &tk, bar, 64, row);
-            tma_load_2d(dv, &tv, bar, 0, row);
-            tma_load_2d(dv + 2048, &tv, bar, 64, row);
-          }
+          mbar_arrive_expect_tx_warp(bar, min(C::TPS, n_tiles - t) * C::TILE);
+          stages = j + 1;
+        }
+        const uint32_t dk = smem_u32(ring + st * C::STAGE + u * C::TILE);
+        const uint32_t dv = dk + HPI * C::KT_BYTES;
+        if (FP8) {  // [HPI heads][16 rows][128] of the map (dim, key in page, page*Hkv + head)
+          tma_load_3d_warp(dk, &tk, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
+          tma_load_3d_warp(dv, &tv, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
+          continue;
+        }
+        const int row = (ph * a.Hkv + h0) * a.P + (key0 - page * a.P);
+        if (a.kv_box3d) {  // one [2 halves][16 rows][64] box per tile
+          tma_load_3d_warp(dk, &tk, bar, 0, row, 0);
+          tma_load_3d_warp(dv, &tv, bar, 0, row, 0);
+        } else {
+          tma_load_2d_warp(dk, &tk, bar, 0, row);
+          tma_load_2d_warp(dk + 2048, &tk, bar, 64, row);
+          tma_load_2d_warp(dv, &tv, bar, 0, row);
+          tma_load_2d_warp(dv + 2048, &tv, bar, 64, row);
         }
       }
-      ok = __shfl_sync(kFull, ok, 0);
-      t = __shfl_sync(kFull, t, 0);
     }
     // Stay resident until every issued copy has landed: the CTA must not exit
     // (and free its shared memory) with TMA writes in flight, even when a
