@@ -53,6 +53,15 @@ import workloads  # noqa: E402
 METRIC = "µs per decode-attention call; achieved HBM GB/s as fraction of GB300 peak"
 NORTH_STAR_HBM_GBS = 8000.0
 
+# DRAM bytes (read + write) of one launch of each workload's dominant kernel,
+# from the ncu captures summarised under profiles/.  An entry is removed
+# whenever that kernel changes after its capture.
+PROFILED_TRAFFIC = {
+    "gqa_ctx5900": (6094080, "profiles/gqa_splitkv_kernel_gqa_ctx5900.md"),
+    "fp8_batch8_ctx32k": (253586944, "profiles/gqa_splitkv_kernel_fp8_batch8_ctx32k.md"),
+    "mla_t6_ctx64k": (79378176, "profiles/mla_splitkv_kernel_mla_t6_ctx64k.md"),
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -359,7 +368,9 @@ def run_ours(args, rank, world, local):
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "kernel": "gqa_splitkv_kernel"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof.update({"traffic": None, "duration_basis": "timed-region time per call (all launches of a step)",
+    traffic, traffic_src = PROFILED_TRAFFIC.get(w.name, (None, None))
+    roof.update({"traffic": traffic, "traffic_source": traffic_src,
+                 "duration_basis": "timed-region time per call (all launches of a step)",
                  "peak_kind": peak_kind, "algorithmic_bytes": nbytes})
 
     # end to end: host buffers, copies inside the timed region
