@@ -61,7 +61,11 @@ typedef enum splitkv_dtype {
 } splitkv_dtype;
 
 typedef enum splitkv_combine_mode {
-  SPLITKV_COMBINE_FUSED = 0,    /* last split CTA of each (b, h_kv) merges      */
+  SPLITKV_COMBINE_FUSED = 0,    /* the split kernel merges: the last CTA of each
+                                   (b, h_kv) group, or with more than 8 splits the
+                                   last CTA of each bundle of 8 and then the last
+                                   bundle of the group (GQA; MLA always merges
+                                   with the combine kernel)                    */
   SPLITKV_COMBINE_SEPARATE = 1  /* a second kernel merges all partials          */
 } splitkv_combine_mode;
 
@@ -240,8 +244,10 @@ splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32
  * per-CTA log of the last decode on `workspace` and the device status word.
  *   cta_log_host  int32 [capacity][4] or NULL: per launched CTA {first page,
  *                 one-past-last page it iterated, keys it scored, flag} in
- *                 launch order; flag = 1 if the CTA merged its group (GQA,
- *                 fused mode) or gave up on a timed-out wait (MLA)
+ *                 launch order; flag (GQA, fused mode): bit 0 set if the CTA
+ *                 wrote its group's merged output, bit 1 set if it merged a
+ *                 bundle of up to 8 splits; flag (MLA): 1 if the CTA gave up
+ *                 on a timed-out wait
  *   capacity      rows of cta_log_host; EINVAL if below splitkv_plan_num_ctas
  *   status_host   int32 or NULL: 0, or a bit set of SPLITKV_DEVERR_* values
  */

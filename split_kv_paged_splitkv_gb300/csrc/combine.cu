@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   __shared__ float4 red[kCombineThreads];
   __shared__ float red_w[kCombineThreads], red_m[kCombineThreads];
   launch_dependents();
-  if (pdl) wait_prerequisites();
+  // The group table is uploaded with the plan and never written by a kernel:
+  // it is read before waiting for the split kernel, off the critical path.
   const int n = blockIdx.y;
   int S = n_parts, slot0 = 0;
   size_t orow = n;
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const int t = r / G, gg = r - t * G;
     orow = (size_t(b) * T + t) * Hq + size_t(hkv + hs) * G + gg;
   }
+  if (pdl) wait_prerequisites();
   const int tid = threadIdx.x, dl = tid & 31, way = tid >> 5;
   const int d = blockIdx.z * 128 + dl * 4;
   const bool dim_ok = d < dv;

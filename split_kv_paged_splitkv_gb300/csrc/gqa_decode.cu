@@ -168,20 +168,24 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
   }
 }
 
-// Log-sum-exp merge of the S partials of one (b, head group) group, by the
-// CTA that finished last.  NT threads over ROWS = 8 * HPI merge rows.  The
-// S x rows LSE values are first staged in shared memory (`sl`, [S][ROWS]) by
-// all threads at once; then thread (row n, DPT dims from d0) accumulates the
-// weighted partials with U splits' loads in flight per step, so the L2 round
-// trips overlap instead of serialising one per split.
+// Log-sum-exp merge of `count` partials of one (b, head group) group -- the
+// slots first, first + stride, ... -- by one CTA.  NT threads over ROWS =
+// 8 * HPI merge rows.  The count x rows LSE values are first staged in shared
+// memory (`sl`, [count][ROWS]) by all threads at once; then thread (row n,
+// DPT dims from d0) accumulates the weighted partials with U partials' loads
+// in flight per step, so the L2 round trips overlap instead of serialising.
+// out_slot < 0: the result is the final bf16 output and LSE; otherwise it is
+// written as a partial (fp32 O, natural-log LSE) into slot out_slot, which may
+// be one of the slots read (each thread reads its own elements before writing
+// them, and the LSEs were staged before any is written).
 template <int NT, int HPI>
-__device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int h0,
-                                            int slot0, int S, float* sl) {
+__device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int h0, int first,
+                                            int count, int stride, int out_slot, float* sl) {
   constexpr int ROWS = 8 * HPI, TPR = NT / ROWS, DPT = 128 / TPR, U = 64 / DPT;
   const int rows = a.rows, rph = a.T * a.G;
-  for (int i = tid; i < S * ROWS; i += NT) {
+  for (int i = tid; i < count * ROWS; i += NT) {
     const int s = i / ROWS, n = i % ROWS, hs = n >> 3, r = n & 7;
-    sl[i] = r < rph ? __ldcg(a.lse_part + size_t(slot0 + s) * rows + hs * rph + r) : -INFINITY;
+    sl[i] = r < rph ? __ldcg(a.lse_part + size_t(first + s * stride) * rows + hs * rph + r) : -INFINITY;
   }
   asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
   const int n = tid / TPR;
@@ -189,25 +193,25 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
   const int d0 = (tid % TPR) * DPT;
   if (r >= rph) return;
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, sl[s * ROWS + n]);
+  for (int s = 0; s < count; ++s) M = fmaxf(M, sl[s * ROWS + n]);
   float acc[DPT];
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
-    const size_t stride = size_t(rows) * 128;
-    const float* base = a.o_part + (size_t(slot0) * rows + hs * rph + r) * 128 + d0;
-    for (int s0 = 0; s0 < S; s0 += U) {
+    const size_t sstride = size_t(stride) * rows * 128;
+    const float* base = a.o_part + (size_t(first) * rows + hs * rph + r) * 128 + d0;
+    for (int s0 = 0; s0 < count; s0 += U) {
       float4 x[U][DPT / 4];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int v = 0; v < DPT / 4; ++v)
-          if (s0 + u < S)
-            x[u][v] = __ldcg(reinterpret_cast<const float4*>(base + size_t(s0 + u) * stride) + v);
+          if (s0 + u < count)
+            x[u][v] = __ldcg(reinterpret_cast<const float4*>(base + size_t(s0 + u) * sstride) + v);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (s0 + u < S) {
+        if (s0 + u < count) {
           const float w = ex2((sl[(s0 + u) * ROWS + n] - M) * kLog2e);
           wsum += w;
 #pragma unroll
@@ -224,6 +228,12 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] *= inv;
   if (wsum > 0.f) lse_n = M + lg2(wsum) * kLn2;
+  if (out_slot >= 0) {
+    const int pr = hs * rph + r;
+    store_row<DPT>(acc, nullptr, a.o_part + (size_t(out_slot) * rows + pr) * 128 + d0);
+    if (d0 == 0) a.lse_part[size_t(out_slot) * rows + pr] = lse_n;
+    return;
+  }
   const int t = r / a.G, g = r - (r / a.G) * a.G;
   const size_t row = (size_t(b) * a.T + t) * a.Hq + size_t(h0 + hs) * a.G + g;
   store_row<DPT>(acc, static_cast<__nv_bfloat16*>(a.out) + row * 128 + d0, nullptr);
@@ -576,20 +586,43 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
   asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
   merge_and_store<FP8, HPI>(a, tid, mo, mm, ml, b, h0, slot);
 
+  // Fused combine: last-arriver merges, no waiting.  With S <= kBundle splits
+  // the CTA that finishes last merges the group's S partials into the output.
+  // With more, the splits form bundles of kBundle consecutive splits: the
+  // last CTA of a bundle merges it in place into the bundle's first slot,
+  // and the last bundle to finish merges the bundle partials into the output
+  // (two reads of at most kBundle partials instead of one read of S).
+  // Bundle tickets live after the group tickets, indexed by slot.
   int merged = 0;
   if (slot >= 0 && a.fused) {
-    __threadfence();
+    constexpr int kBundle = 8;
+    float* sl = reinterpret_cast<float*>(ring) + C::NCW * 8 * 128 + 2 * C::NCW * 8;
+    const int slot0 = slot - split;
+    const bool two_level = nsplit > kBundle;
+    const int bslot = slot0 + (split / kBundle) * kBundle;
+    const int bcount = min(kBundle, nsplit - (bslot - slot0));
     asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-    if (tid == 0) misc[0] = (atomicAdd(a.tickets + group, 1) == nsplit - 1);
+    if (tid == 0)
+      misc[0] = two_level ? (atom_add_acq_rel_gpu(a.tickets + a.n_groups + bslot, 1) == bcount - 1)
+                          : (atom_add_acq_rel_gpu(a.tickets + group, 1) == nsplit - 1);
     asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-    if (misc[0]) {
-      __threadfence();
-      // staged LSE values go past the warp-merge area at the start of the ring
-      merge_group<C::NCW * 32, HPI>(a, tid, b, h0, slot - split, nsplit,
-                                    reinterpret_cast<float*>(ring) + C::NCW * 8 * 128 +
-                                        2 * C::NCW * 8);
+    if (misc[0] && !two_level) {
+      merge_group<C::NCW * 32, HPI>(a, tid, b, h0, slot0, nsplit, 1, -1, sl);
       if (tid == 0) a.tickets[group] = 0;
       merged = 1;
+    } else if (misc[0]) {
+      merge_group<C::NCW * 32, HPI>(a, tid, b, h0, bslot, bcount, 1, bslot, sl);
+      if (tid == 0) a.tickets[a.n_groups + bslot] = 0;
+      merged = 2;
+      const int nb = (nsplit + kBundle - 1) / kBundle;
+      asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+      if (tid == 0) misc[0] = (atom_add_acq_rel_gpu(a.tickets + group, 1) == nb - 1);
+      asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+      if (misc[0]) {
+        merge_group<C::NCW * 32, HPI>(a, tid, b, h0, slot0, nb, kBundle, -1, sl);
+        if (tid == 0) a.tickets[group] = 0;
+        merged = 3;
+      }
     }
   }
   if (tid == 0) {

@@ -188,8 +188,8 @@ void build_plan(splitkv_plan_s* p) {
   off = align_up(off + p->groups.size() * sizeof(int32_t));
   p->off_seqlens = off;
   off = align_up(off + size_t(B) * sizeof(int32_t));
-  p->off_tickets = off;
-  off = align_up(off + size_t(p->n_groups) * sizeof(int32_t));
+  p->off_tickets = off;  // group tickets, then one bundle ticket per slot
+  off = align_up(off + size_t(p->n_groups + p->n_slots) * sizeof(int32_t));
   p->upload_bytes = off;
   p->off_log = off;
   off = align_up(off + size_t(p->n_ctas) * kLogFields * sizeof(int32_t));

@@ -132,6 +132,19 @@ __device__ __forceinline__ void tma_load_3d_warp(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// ------------------------------------------------------------- tickets
+
+// Atomic add with acquire-release semantics at GPU scope.  Issued by one
+// thread after a CTA barrier, it publishes the CTA's earlier global writes
+// (release) and, for the caller that sees the final count, makes the writes
+// published by the other CTAs' increments visible (acquire; a CTA barrier
+// after it extends that to the caller's CTA).
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int r;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
+
 // ------------------------------------------------------------- PDL
 
 __device__ __forceinline__ void launch_dependents() {

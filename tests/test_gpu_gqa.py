@@ -98,9 +98,15 @@ def test_split_ranges_and_nonempty_ctas():
         if S:
             assert len(items) == 2 * min(S, n_pages)
         assert status == 0
-        # exactly one merging CTA per (b, h_kv) group when split
-        if (items[:, 3] > 1).any():
-            assert log[:, 3].sum() == len(np.unique(items[items[:, 3] > 1][:, 7]))
+        # fused merge log: bit 0 = wrote the group's output, bit 1 = merged a
+        # bundle of up to 8 consecutive splits (groups of more than 8 splits)
+        split_items = items[items[:, 3] > 1]
+        if len(split_items):
+            groups = np.unique(split_items[:, 7])
+            assert (log[:, 3] & 1).sum() == len(groups)
+            bundles = sum(-(-int(split_items[split_items[:, 7] == g][0, 3]) // 8)
+                          for g in groups if split_items[split_items[:, 7] == g][0, 3] > 8)
+            assert ((log[:, 3] >> 1) & 1).sum() == bundles
 
 
 def _sms():
