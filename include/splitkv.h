@@ -72,7 +72,8 @@ typedef enum splitkv_combine_mode {
 /* Shapes and element types of one decode-attention call (no pointers). */
 typedef struct splitkv_desc {
   int32_t batch;              /* B, >= 1                                        */
-  int32_t q_tokens;           /* T query tokens per sequence, causal among them */
+  int32_t q_tokens;           /* T query tokens per sequence, causal among them;
+                                 GQA: T * (Hq / Hkv) <= 16; MLA: T <= 16       */
   int32_t num_q_heads;        /* Hq                                             */
   int32_t num_kv_heads;       /* Hkv, divides Hq                                */
   int32_t qk_dim;             /* Dk: 128 (GQA) or 576 (MLA latent + rope)       */
@@ -146,8 +147,8 @@ int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan);
 
 /* KV heads one work item covers: 4, 2 or 1 (the largest dividing Hkv) for the
- * e4m3 GQA path, where one TMA box then brings a 16-key tile of all of them;
- * 1 otherwise.  Partial-result rows of an item are numbered
+ * e4m3 GQA path with at most 8 query rows (T * G) per KV head, where one TMA
+ * box then brings a 16-key tile of all of them; 1 otherwise.  Partial-result rows of an item are numbered
  * head_slot * T * G + t * G + g. */
 int32_t splitkv_plan_heads_per_item(const splitkv_plan_t* plan);
 

@@ -145,7 +145,7 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
   if (family_of(*d) == Family::kNone)
     return fail(SPLITKV_EUNSUPPORTED,
                 "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
-                "(GQA: qk_dim=v_dim=128, T*G<=8; MLA: 128 q heads, 1 bf16 latent head, "
+                "(GQA: qk_dim=v_dim=128, T*G<=16; MLA: 128 q heads, 1 bf16 latent head, "
                 "qk_dim=576, v_dim=512, v_shares_k, page_size 64, T<=16)",
                 d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
                 d->v_shares_k);
@@ -164,7 +164,7 @@ splitkv_status fail(splitkv_status s, const char* fmt, ...) {
 
 Family family_of(const splitkv_desc_t& d) {
   const int G = d.num_q_heads / d.num_kv_heads;
-  if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 8) return Family::kGqa;
+  if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 16) return Family::kGqa;
   if (d.qk_dim == 576 && d.v_dim == 512 && d.v_shares_k && d.num_kv_heads == 1 &&
       d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.page_size == 64 && d.q_tokens <= 16)
     return Family::kMla;
@@ -180,7 +180,8 @@ int ctas_per_sm(const splitkv_desc_t& d) {
 }
 
 int heads_per_item(const splitkv_desc_t& d) {
-  if (family_of(d) != Family::kGqa || d.kv_dtype != SPLITKV_FP8_E4M3) return 1;
+  const int rows_per_head = d.q_tokens * (d.num_q_heads / d.num_kv_heads);
+  if (family_of(d) != Family::kGqa || d.kv_dtype != SPLITKV_FP8_E4M3 || rows_per_head > 8) return 1;
   for (int h : {4, 2})
     if (d.num_kv_heads % h == 0) return h;
   return 1;

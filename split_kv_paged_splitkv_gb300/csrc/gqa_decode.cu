@@ -48,9 +48,10 @@ using namespace ptx;
 // stream more slowly than large ones, so per-SM bandwidth comes from several
 // CTAs per SM (a two-stage ring and 160 threads let three CTAs share an SM)
 // and from boxes that span several heads (HPI > 1, e4m3 only).
-template <bool FP8, int HPI>
+template <bool FP8, int HPI, int NRG = 1>
 struct Gqa {
   static_assert(HPI == 1 || (FP8 && (HPI == 2 || HPI == 4)), "heads per item");
+  static_assert(NRG == 1 || (NRG == 2 && HPI == 1), "row groups per head");
   static constexpr int D = 128;
   static constexpr int TK = 16;                            // keys per tile
   static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one head's K (or V) rows
@@ -59,10 +60,13 @@ struct Gqa {
   static constexpr int TPS = STAGE / TILE;                 // tiles per stage
   static constexpr int NST = 2;                            // stages in the ring
   static constexpr int NCW = 4;                            // consumer warps
-  static constexpr int WPH = NCW / HPI;                    // warps per head slot
+  // A slot is (head slot hs, row group rg) = (slot % HPI, slot / HPI): the
+  // warps of a slot score query rows [8 rg, 8 rg + 8) of KV head h0 + hs.
+  static constexpr int SLOTS = HPI * NRG;
+  static constexpr int WPH = NCW / SLOTS;                  // warps per slot
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int RING = NST * STAGE;
-  static constexpr int ROWS = 8 * HPI;                     // merge rows (8 per head)
+  static constexpr int ROWS = 8 * SLOTS;                   // merge rows (8 per slot)
   static constexpr int MERGE = NCW * 8 * D * 4 + NCW * 8 * 2 * 4;
   static_assert(MERGE + 64 * ROWS * 4 <= RING, "merge area and staged LSEs alias the ring");
   // Warp w takes tiles w / HPI, w / HPI + WPH, ...: its successive visits to
@@ -119,23 +123,25 @@ __device__ __forceinline__ void store_row(const float (&acc)[DPT], __nv_bfloat16
   }
 }
 
-// Merges the (m, l, O) of the warps sharing each head slot and writes the
-// item's result.  Runs on the NT = NCW * 32 consumer threads: merge row
-// n = tid / TPR (head slot n / 8, query row n % 8 of that head), DPT =
-// 128 / TPR consecutive dims from d0.  `mo` is [NCW][8][128] fp32, `mm`/`ml`
-// [NCW][8]; m is in log2 units.  Partial rows are numbered hs * T*G + row.
-template <bool FP8, int HPI>
+// Merges the (m, l, O) of the warps sharing each slot and writes the item's
+// result.  Runs on the NT = NCW * 32 consumer threads: merge row n = tid /
+// TPR (slot n / 8, i.e. head slot hs and row group rg; query row rg * 8 +
+// n % 8 of that head), DPT = 128 / TPR consecutive dims from d0.  `mo` is
+// [NCW][8][128] fp32, `mm`/`ml` [NCW][8]; m is in log2 units.  Partial rows
+// are numbered hs * T*G + row.
+template <bool FP8, int HPI, int NRG>
 __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, const float* mo,
                                                 const float* mm, const float* ml, int b, int h0,
                                                 int slot) {
-  using C = Gqa<FP8, HPI>;
+  using C = Gqa<FP8, HPI, NRG>;
   constexpr int NT = C::NCW * 32, TPR = NT / C::ROWS, DPT = 128 / TPR;
   const int n = tid / TPR;           // merge row
-  const int hs = n >> 3, r = n & 7;  // head slot, query row of that head
+  const int sl = n >> 3, r8 = n & 7;
+  const int hs = sl % HPI, r = (sl / HPI) * 8 + r8;  // head slot, query row of that head
   const int d0 = (tid % TPR) * DPT;  // first of DPT consecutive dims
   float M = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < C::WPH; ++j) M = fmaxf(M, mm[(hs + HPI * j) * 8 + r]);
+  for (int j = 0; j < C::WPH; ++j) M = fmaxf(M, mm[(sl + C::SLOTS * j) * 8 + r8]);
   float acc[DPT];
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
@@ -143,10 +149,10 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
   if (M != -INFINITY) {
 #pragma unroll
     for (int j = 0; j < C::WPH; ++j) {
-      const int w = hs + HPI * j;
-      const float sc = ex2(mm[w * 8 + r] - M);
-      lsum += sc * ml[w * 8 + r];
-      axpy<DPT>(acc, sc, mo + (w * 8 + r) * 128 + d0);
+      const int w = sl + C::SLOTS * j;
+      const float sc = ex2(mm[w * 8 + r8] - M);
+      lsum += sc * ml[w * 8 + r8];
+      axpy<DPT>(acc, sc, mo + (w * 8 + r8) * 128 + d0);
     }
   }
   float lse_n = -INFINITY;
@@ -170,7 +176,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
 
 // Log-sum-exp merge of `count` partials of one (b, head group) group -- the
 // slots first, first + stride, ... -- by one CTA.  NT threads over ROWS =
-// 8 * HPI merge rows.  The count x rows LSE values are first staged in shared
+// 8 * HPI * NRG merge rows.  The count x rows LSE values are first staged in shared
 // memory (`sl`, [count][ROWS]) by all threads at once; then thread (row n,
 // DPT dims from d0) accumulates the weighted partials with U partials' loads
 // in flight per step, so the L2 round trips overlap instead of serialising.
@@ -178,18 +184,21 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
 // written as a partial (fp32 O, natural-log LSE) into slot out_slot, which may
 // be one of the slots read (each thread reads its own elements before writing
 // them, and the LSEs were staged before any is written).
-template <int NT, int HPI>
+template <int NT, int HPI, int NRG>
 __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b, int h0, int first,
                                             int count, int stride, int out_slot, float* sl) {
-  constexpr int ROWS = 8 * HPI, TPR = NT / ROWS, DPT = 128 / TPR, U = 64 / DPT;
+  constexpr int ROWS = 8 * HPI * NRG, TPR = NT / ROWS, DPT = 128 / TPR, U = 64 / DPT;
   const int rows = a.rows, rph = a.T * a.G;
+  // merge row n: slot n / 8 = (head slot, row group), query row of that head
+  auto hs_of = [](int n) { return (n >> 3) % HPI; };
+  auto r_of = [](int n) { return ((n >> 3) / HPI) * 8 + (n & 7); };
   for (int i = tid; i < count * ROWS; i += NT) {
-    const int s = i / ROWS, n = i % ROWS, hs = n >> 3, r = n & 7;
+    const int s = i / ROWS, n = i % ROWS, hs = hs_of(n), r = r_of(n);
     sl[i] = r < rph ? __ldcg(a.lse_part + size_t(first + s * stride) * rows + hs * rph + r) : -INFINITY;
   }
   asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
   const int n = tid / TPR;
-  const int hs = n >> 3, r = n & 7;
+  const int hs = hs_of(n), r = r_of(n);
   const int d0 = (tid % TPR) * DPT;
   if (r >= rph) return;
   float M = -INFINITY;
@@ -240,11 +249,11 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
   if (d0 == 0 && a.lse) a.lse[row] = lse_n;
 }
 
-template <bool FP8, int HPI>
-__global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
+template <bool FP8, int HPI, int NRG>
+__global__ void __launch_bounds__(Gqa<FP8, HPI, NRG>::THREADS, kGqaCtasPerSm)
     gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
-  using C = Gqa<FP8, HPI>;
+  using C = Gqa<FP8, HPI, NRG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), C::TPS * HPI);  // one arrival per tile and head
+      mbar_init(smem_u32(empty + s), C::TPS * C::SLOTS);  // one arrival per tile and slot
     }
     misc[0] = 0;
     misc[1] = 0;
@@ -370,14 +379,18 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
   // ------------------------------------------------------------------ consumers
   const int tid = threadIdx.x;  // consumer threads 0 .. NCW*32-1
   const int gi = lane >> 2, ti = lane & 3;
-  const int hs = warp % HPI;    // head slot: this warp serves KV head h0 + hs
+  const int slot_w = warp % C::SLOTS;  // this warp's slot:
+  const int hs = slot_w % HPI;         //   KV head h0 + hs,
+  const int rg = slot_w / HPI;         //   query rows [8 rg, 8 rg + 8) of that head
   const int hkv = h0 + hs;
+  const int rph = a.T * a.G;           // query rows per KV head
 
-  // Q^T operand fragments: row n = gi, dims by ti (see the layout notes).
+  // Q^T operand fragments: query row n = 8 rg + gi of this head, dims by ti
+  // (see the layout notes); rows past the head's T*G rows are zero.
   uint32_t qf[8][2];
   {
-    const int n = gi;
-    if (n < a.rows) {
+    const int n = rg * 8 + gi;
+    if (n < rph) {
       const int t = n / a.G, g = n - t * a.G;
       const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) +
                                 ((size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g) * 128;
@@ -404,9 +417,9 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
   // Visible-key limits of the two query rows whose scores this lane holds.
   int lim0 = -1, lim1 = -1;
   {
-    const int n0 = 2 * ti, n1 = 2 * ti + 1;
-    if (n0 < a.rows) lim0 = L - a.T + n0 / a.G;
-    if (n1 < a.rows) lim1 = L - a.T + n1 / a.G;
+    const int n0 = rg * 8 + 2 * ti, n1 = n0 + 1;
+    if (n0 < rph) lim0 = L - a.T + n0 / a.G;
+    if (n1 < rph) lim1 = L - a.T + n1 / a.G;
   }
   const int min_lim = L - a.T;
 
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int keys_scored = 0;
 
-  for (int i = warp / HPI; i < n_tiles; i += C::WPH) {
+  for (int i = warp / C::SLOTS; i < n_tiles; i += C::WPH) {
     const int j = i / C::TPS, st = j % C::NST;
     const bool arrived = __all_sync(kFull, mbar_wait(smem_u32(full + st), (j / C::NST) & 1));
     if (!arrived) {
@@ -427,7 +440,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
     uint8_t* vt = kt + HPI * C::KT_BYTES;
     const int key0 = k_begin + i * 16;
     const int valid = min(16, k_end - key0);
-    if (hs == 0) keys_scored += valid;
+    if (slot_w == 0) keys_scored += valid;
     if (valid < 16) {
       // Slots past the last visible key may hold anything (even NaN): zero
       // those V rows so that 0 * V stays 0 in the PV product.
@@ -584,7 +597,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
     ml[warp * 8 + 2 * ti + 1] = l1;
   }
   asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-  merge_and_store<FP8, HPI>(a, tid, mo, mm, ml, b, h0, slot);
+  merge_and_store<FP8, HPI, NRG>(a, tid, mo, mm, ml, b, h0, slot);
 
   // Fused combine: last-arriver merges, no waiting.  With S <= kBundle splits
   // the CTA that finishes last merges the group's S partials into the output.
@@ -607,11 +620,11 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
                           : (atom_add_acq_rel_gpu(a.tickets + group, 1) == nsplit - 1);
     asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
     if (misc[0] && !two_level) {
-      merge_group<C::NCW * 32, HPI>(a, tid, b, h0, slot0, nsplit, 1, -1, sl);
+      merge_group<C::NCW * 32, HPI, NRG>(a, tid, b, h0, slot0, nsplit, 1, -1, sl);
       if (tid == 0) a.tickets[group] = 0;
       merged = 1;
     } else if (misc[0]) {
-      merge_group<C::NCW * 32, HPI>(a, tid, b, h0, bslot, bcount, 1, bslot, sl);
+      merge_group<C::NCW * 32, HPI, NRG>(a, tid, b, h0, bslot, bcount, 1, bslot, sl);
       if (tid == 0) a.tickets[a.n_groups + bslot] = 0;
       merged = 2;
       const int nb = (nsplit + kBundle - 1) / kBundle;
@@ -619,7 +632,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI>::THREADS, kGqaCtasPerSm)
       if (tid == 0) misc[0] = (atom_add_acq_rel_gpu(a.tickets + group, 1) == nb - 1);
       asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
       if (misc[0]) {
-        merge_group<C::NCW * 32, HPI>(a, tid, b, h0, slot0, nb, kBundle, -1, sl);
+        merge_group<C::NCW * 32, HPI, NRG>(a, tid, b, h0, slot0, nb, kBundle, -1, sl);
         if (tid == 0) a.tickets[group] = 0;
         merged = 3;
       }
@@ -694,13 +707,13 @@ namespace {
 // programmatic dependent launch: the kernel's prologue may overlap the tail
 // of the previous kernel on the stream; it waits (griddepcontrol.wait)
 // before touching anything that kernel could have written.
-template <bool FP8, int HPI>
+template <bool FP8, int HPI, int NRG = 1>
 cudaError_t launch_gqa_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                          cudaStream_t s) {
-  using C = Gqa<FP8, HPI>;
+  using C = Gqa<FP8, HPI, NRG>;
   // The shared-memory opt-in is a per-process attribute: set it on first use only.
   static cudaError_t attr = cudaFuncSetAttribute(
-      gqa_splitkv_kernel<FP8, HPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      gqa_splitkv_kernel<FP8, HPI, NRG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_items, 1, 1);
@@ -712,7 +725,7 @@ cudaError_t launch_gqa_t(const DecodeArgs& a, const CUtensorMap& mk, const CUten
   la[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = la;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<FP8, HPI>, a, mk, mv);
+  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<FP8, HPI, NRG>, a, mk, mv);
 }
 
 }  // namespace
@@ -723,6 +736,10 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
   const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(&tv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.n_items == 0) return cudaSuccess;
+  if (a.T * a.G > 8) {  // 9..16 query rows per KV head: two row groups
+    if (a.hpi != 1) return cudaErrorInvalidValue;
+    return fp8 ? launch_gqa_t<true, 1, 2>(a, mk, mv, s) : launch_gqa_t<false, 1, 2>(a, mk, mv, s);
+  }
   if (!fp8) return a.hpi == 1 ? launch_gqa_t<false, 1>(a, mk, mv, s) : cudaErrorInvalidValue;
   switch (a.hpi) {
     case 1: return launch_gqa_t<true, 1>(a, mk, mv, s);

@@ -119,7 +119,7 @@ def test_plan_slots_and_groups_are_consistent():
     (dict(P=8), skv.SPLITKV_EINVAL),
     (dict(Hq=15), skv.SPLITKV_EINVAL),
     (dict(D=96, Dv=96), skv.SPLITKV_EUNSUPPORTED),
-    (dict(T=2, Hq=16, Hkv=2), skv.SPLITKV_EUNSUPPORTED),  # 2 * 8 rows > 8
+    (dict(T=3, Hq=16, Hkv=2), skv.SPLITKV_EUNSUPPORTED),  # 3 * 8 query rows per KV head > 16
     (dict(N=0), skv.SPLITKV_EINVAL),
 ])
 def test_plan_rejects_bad_descriptors(bad, code):

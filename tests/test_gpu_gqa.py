@@ -135,16 +135,34 @@ def test_ragged_lengths(fp8, G, Hkv, P):
             assert (log[nonempty, 2] > 0).all()
 
 
-@pytest.mark.parametrize("T,G", [(2, 4), (8, 1), (4, 2), (3, 2)])
+@pytest.mark.parametrize("T,G", [(2, 4), (8, 1), (4, 2), (3, 2),
+                                 (2, 8), (4, 4), (3, 5), (16, 1), (5, 2)])
 @pytest.mark.parametrize("fp8", [False, True])
 def test_multi_token_causal(T, G, fp8):
+    """Speculative decode: T query tokens, causal among themselves; T*G > 8
+    takes the two-row-group kernel (query rows 8..15 of a KV head)."""
     lens = [T, T + 1, 37, 300, 16 * 5]
     w = _custom(lens, G=G, Hkv=2, T=T, fp8=fp8, seed=T * 7 + G)
     x = workloads.make_inputs(w, device="cuda")
     ref_o, ref_l = oracle_direct(x)
     for S in (1, 2, 5):
-        out, lse = session(x, S).run()
-        compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} S={S}")
+        for mode in ((1, 0) if S == 5 else (1,)):
+            out, lse = session(x, S, mode).run()
+            compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} S={S} mode={mode}")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_sixteen_rows_per_head_long_context(fp8):
+    """T*G = 16 over a long context with the planner's splits: many tiles per
+    warp, both row groups, merged partials."""
+    w = _custom([2048 + 9, 700, 16], G=8, Hkv=4, T=2, fp8=fp8, seed=91)
+    x = workloads.make_inputs(w, device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    s = session(x, 0)
+    out, lse = s.run()
+    compare(out, lse, ref_o, ref_l, what="T=2 G=8 Hkv=4 planner")
+    log, status = s.stats()
+    assert status == 0 and (log[:, 2] > 0).all()
 
 
 # ------------------------------------------------------------------ workloads 3 and 5
