@@ -37,7 +37,9 @@ Conventions (readings of points the pages leave open):
 * Query head ``h`` reads KV head ``h // G`` with ``G = Hq / Hkv``.
 * Pages are HND: ``pages[phys][h_kv][slot][dim]``; key ``j`` of sequence ``b``
   lives in page ``block_table[b][j // P]``, slot ``j % P``.
-* FP8 dequantisation is ``code_value * kv_scale`` for both K and V.
+* FP8 dequantisation is ``code_value * kv_scale`` for both K and V, or, with
+  per-head scales, ``code_value * k_scale[h_kv]`` for K and
+  ``code_value * v_scale[h_kv]`` for V.
 * With ``v_shares_k`` (MLA latent cache) ``V_j`` is the first ``Dv`` columns of
   ``K_j``.
 * The LSE is the natural log of ``sum_j exp(s_j)`` where ``s_j`` already
@@ -129,14 +131,16 @@ def _softmax_attend(q_row: np.ndarray, K: np.ndarray, V: np.ndarray,
 
 def attention_direct(q, k_pages, v_pages, block_table, seq_lens, *, scale,
                      kv_dtype="bf16", kv_scale=1.0, v_dim=None,
-                     v_shares_k=False, rows=None):
+                     v_shares_k=False, rows=None, k_scale=None, v_scale=None):
     """Decode attention by definition, in fp64.
 
     ``q``: bf16 bits ``[B][T][Hq][Dk]``; ``k_pages``/``v_pages``: raw pages
     ``[N][Hkv][P][D]`` (bf16 bits or e4m3 codes); ``block_table`` ``[B][max]``;
     ``seq_lens`` ``[B]``.  ``rows``: optional list of ``(b, t, h)`` to compute
-    (all rows otherwise).  Returns ``(out[B][T][Hq][Dv], lse[B][T][Hq])`` in
-    float64 (rows not computed are NaN).
+    (all rows otherwise).  ``k_scale`` / ``v_scale``: optional per-KV-head
+    dequantisation scales of an e4m3 cache, used for K / V in place of
+    ``kv_scale``.  Returns ``(out[B][T][Hq][Dv], lse[B][T][Hq])`` in float64
+    (rows not computed are NaN).
     """
     q = np.asarray(q)
     B, T, Hq, Dk = q.shape
@@ -155,12 +159,14 @@ def attention_direct(q, k_pages, v_pages, block_table, seq_lens, *, scale,
         hk = h // G
         key = (b, hk)
         if key not in cache:
+            ks = kv_scale if k_scale is None else float(k_scale[hk])
+            vs = kv_scale if v_scale is None else float(v_scale[hk])
             Kr = gather_keys(k_pages, block_table[b], L, hk)
-            K = dequant(Kr, kv_dtype, kv_scale)
+            K = dequant(Kr, kv_dtype, ks)
             if v_shares_k:
                 V = K[:, :v_dim]
             else:
-                V = dequant(gather_keys(v_pages, block_table[b], L, hk), kv_dtype, kv_scale)
+                V = dequant(gather_keys(v_pages, block_table[b], L, hk), kv_dtype, vs)
             cache = {key: (K, V)}  # one (b, h_kv) at a time keeps memory bounded
         K, V = cache[key]
         lim = L - T + t  # last visible key index for this query token

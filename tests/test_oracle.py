@@ -139,6 +139,57 @@ def test_fp8_brute_force_with_scale():
         assert abs(lse[0, 0, h] - ref_l) < 1e-12
 
 
+def _fp8_tiny(rng, L=6, D=4, P=4, Hq=4, Hkv=2, N=3):
+    q = _bf16_bits(rng.standard_normal((1, 1, Hq, D)))
+    k = rng.integers(0, 256, size=(N, Hkv, P, D)).astype(np.uint8)
+    v = rng.integers(0, 256, size=(N, Hkv, P, D)).astype(np.uint8)
+    k[(k & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    v[(v & 0x7F) == 0x7F] = 0x44
+    table = np.array([[2, 0]], np.int32)
+    return q, k, v, table, np.array([L], np.int32)
+
+
+def test_fp8_per_head_kv_scales_brute_force():
+    """Per-KV-head scales: K_j = code * k_scale[h_kv], V_j = code * v_scale[h_kv],
+    with query head h reading KV head h // G."""
+    rng = np.random.default_rng(12)
+    L, P = 6, 4
+    q, k, v, table, lens = _fp8_tiny(rng, L=L, P=P)
+    ks, vs = [0.011, 0.037], [0.21, 0.053]
+    out, lse = O.attention_direct(q, k, v, table, lens, scale=0.3, kv_dtype="fp8_e4m3",
+                                  k_scale=ks, v_scale=vs)
+    for h in range(4):
+        hk = h // 2
+        K = [O.e4m3_to_float(k[table[0, j // P], hk, j % P]) * ks[hk] for j in range(L)]
+        V = [O.e4m3_to_float(v[table[0, j // P], hk, j % P]) * vs[hk] for j in range(L)]
+        ref_o, ref_l = _mp_attention(O.bf16_to_float(q[0, 0, h]), K, V, 0.3)
+        np.testing.assert_allclose(out[0, 0, h], ref_o, atol=1e-13)
+        assert abs(lse[0, 0, h] - ref_l) < 1e-12
+
+
+def test_fp8_v_scale_is_linear_and_k_scale_is_a_temperature():
+    """Scaling V by c scales the output by c and leaves the LSE alone; scaling K
+    by a is the same as scaling the softmax scale by a."""
+    rng = np.random.default_rng(13)
+    q, k, v, table, lens = _fp8_tiny(rng)
+    base_o, base_l = O.attention_direct(q, k, v, table, lens, scale=0.3, kv_dtype="fp8_e4m3",
+                                        k_scale=[0.02, 0.02], v_scale=[0.1, 0.1])
+    o2, l2 = O.attention_direct(q, k, v, table, lens, scale=0.3, kv_dtype="fp8_e4m3",
+                                k_scale=[0.02, 0.02], v_scale=[0.35, 0.35])
+    np.testing.assert_allclose(o2, base_o * 3.5, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l2, base_l, rtol=0, atol=1e-12)
+    o3, l3 = O.attention_direct(q, k, v, table, lens, scale=0.3 * 0.02 / 0.05, kv_dtype="fp8_e4m3",
+                                k_scale=[0.05, 0.05], v_scale=[0.1, 0.1])
+    np.testing.assert_allclose(o3, base_o, rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(l3, base_l, rtol=0, atol=1e-11)
+    # a single per-tensor kv_scale is the special case k_scale = v_scale = kv_scale
+    o4, l4 = O.attention_direct(q, k, v, table, lens, scale=0.3, kv_dtype="fp8_e4m3",
+                                kv_scale=0.02)
+    o5, l5 = O.attention_direct(q, k, v, table, lens, scale=0.3, kv_dtype="fp8_e4m3",
+                                k_scale=[0.02, 0.02], v_scale=[0.02, 0.02])
+    assert np.array_equal(o4, o5) and np.array_equal(l4, l5)
+
+
 def test_head_mapping_uses_contiguous_groups():
     """With G = 2, query heads 2,3 read KV head 1.  Make KV head 1's keys all
     zero: those rows must average V (closed form) while heads 0,1 must not."""
