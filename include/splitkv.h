@@ -199,6 +199,27 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace,
                               void* out, float* lse, void* stream);
 
 /*
+ * splitkv_decode_kv_scales -- splitkv_decode over an e4m3 cache whose K and V
+ * carry their own dequantisation scale per KV head: K_j = code * k_scale[h],
+ * V_j = code * v_scale[h] for KV head h (a separate per-tensor K and V scale
+ * is the case of all-equal entries).  "Xqa decode kernels", section
+ * "Purpose", names an FP8 KV cache with a scale; the per-head, per-tensor
+ * split of that scale is this library's extension.
+ *   k_scale, v_scale  fp32 [Hkv] device arrays, positive and finite (not
+ *                     checked: they are read by the kernel after the
+ *                     dependency wait, so a preceding kernel may write them)
+ *   other arguments   as splitkv_decode (there is no kv_scale)
+ * EUNSUPPORTED for bf16 caches and the MLA shape; EINVAL for NULL or
+ * misaligned (< 4 bytes) scale arrays.
+ */
+splitkv_status splitkv_decode_kv_scales(const splitkv_plan_t* plan, void* workspace,
+                                        const void* q, const void* k_pages, const void* v_pages,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int32_t num_splits, float scale, const float* k_scale,
+                                        const float* v_scale, void* out, float* lse,
+                                        void* stream);
+
+/*
  * splitkv_decode_noalloc -- splitkv_decode for callers that cannot allocate
  * device memory (code running inside another framework's memory budget,
  * plugins whose host forbids device allocations after start-up, real-time

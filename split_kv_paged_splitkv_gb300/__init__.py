@@ -54,6 +54,8 @@ _SIGNATURES = {
     "splitkv_workspace_size": (_sz, [_vp]),
     "splitkv_plan_upload": (_i32, [_vp, _vp, _sz, _vp]),
     "splitkv_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
+    "splitkv_decode_kv_scales": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _vp, _vp, _vp,
+                                        _vp, _vp]),
     "splitkv_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
     "splitkv_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "splitkv_read_stats": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp]),
@@ -168,6 +170,17 @@ def splitkv_decode(plan: Plan, workspace, q, k_pages, v_pages, block_table, seq_
     _check(_lib.splitkv_decode(plan.handle, _ptr(workspace), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                                _ptr(block_table), _ptr(seq_lens), num_splits, scale, kv_scale,
                                _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def splitkv_decode_kv_scales(plan: Plan, workspace, q, k_pages, v_pages, block_table, seq_lens,
+                             num_splits: int, scale: float, k_scale, v_scale, out, lse,
+                             stream=None):
+    """splitkv_decode over an e4m3 cache with per-KV-head K and V scales
+    (``k_scale``, ``v_scale``: fp32 [Hkv] device tensors)."""
+    _check(_lib.splitkv_decode_kv_scales(plan.handle, _ptr(workspace), _ptr(q), _ptr(k_pages),
+                                         _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                         num_splits, scale, _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                         _ptr(lse), _stream(stream)))
 
 
 def splitkv_decode_noalloc(plan: Plan, q, k_pages, v_pages, block_table, seq_lens,

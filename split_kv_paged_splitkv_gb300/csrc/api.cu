@@ -277,11 +277,14 @@ splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace,
   return SPLITKV_OK;
 }
 
-splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const void* q,
-                              const void* k_pages, const void* v_pages,
-                              const int32_t* block_table, const int32_t* seq_lens,
-                              int32_t num_splits, float scale, float kv_scale, void* out,
-                              float* lse, void* stream) {
+namespace {
+
+// The decode call; k_scale / v_scale (device, [Hkv]) replace kv_scale when given.
+splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const void* q,
+                           const void* k_pages, const void* v_pages, const int32_t* block_table,
+                           const int32_t* seq_lens, int32_t num_splits, float scale,
+                           float kv_scale, const float* k_scale, const float* v_scale, void* out,
+                           float* lse, void* stream) {
   if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
   const splitkv_desc_t& d = plan->desc;
   if (!workspace) return fail(SPLITKV_EWORKSPACE, "workspace is NULL");
@@ -298,8 +301,16 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
                 plan->num_splits);
   if (!(scale > 0.f) || !(scale < 1e30f)) return fail(SPLITKV_EINVAL, "scale must be positive and finite");
   const bool fp8 = d.kv_dtype == SPLITKV_FP8_E4M3;
-  if (fp8 && (!(kv_scale > 0.f) || !(kv_scale < 1e30f)))
+  const bool per_head = k_scale || v_scale;
+  if (per_head) {
+    if (!k_scale || !v_scale) return fail(SPLITKV_EINVAL, "k_scale and v_scale must both be given");
+    if (!fp8 || family_of(d) != Family::kGqa)
+      return fail(SPLITKV_EUNSUPPORTED, "per-head K/V scales apply to e4m3 GQA caches only");
+    if ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+      return fail(SPLITKV_EINVAL, "k_scale and v_scale must be 4-byte aligned");
+  } else if (fp8 && (!(kv_scale > 0.f) || !(kv_scale < 1e30f))) {
     return fail(SPLITKV_EINVAL, "kv_scale must be positive and finite");
+  }
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   DecodeArgs a{};
@@ -331,8 +342,10 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
   const float kLog2e = 1.4426950408889634f;
   // FP8 tiles are converted to their e4m3 values; the per-tensor kv_scale is
   // applied once to the scores and once to the output.
-  a.qk_scale_log2 = scale * kLog2e * (fp8 ? kv_scale : 1.f);
-  a.o_scale = fp8 ? kv_scale : 1.f;
+  a.qk_scale_log2 = scale * kLog2e * (fp8 && !per_head ? kv_scale : 1.f);
+  a.o_scale = fp8 && !per_head ? kv_scale : 1.f;
+  a.k_scale = k_scale;  // per-head factors, applied by the kernel per KV head
+  a.v_scale = v_scale;
   a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
@@ -381,6 +394,28 @@ splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const
     if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
   }
   return SPLITKV_OK;
+}
+
+}  // namespace
+
+splitkv_status splitkv_decode(const splitkv_plan_t* plan, void* workspace, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              int32_t num_splits, float scale, float kv_scale, void* out,
+                              float* lse, void* stream) {
+  return decode_impl(plan, workspace, q, k_pages, v_pages, block_table, seq_lens, num_splits,
+                     scale, kv_scale, nullptr, nullptr, out, lse, stream);
+}
+
+splitkv_status splitkv_decode_kv_scales(const splitkv_plan_t* plan, void* workspace,
+                                        const void* q, const void* k_pages, const void* v_pages,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int32_t num_splits, float scale, const float* k_scale,
+                                        const float* v_scale, void* out, float* lse,
+                                        void* stream) {
+  if (!k_scale || !v_scale) return fail(SPLITKV_EINVAL, "k_scale and v_scale must not be NULL");
+  return decode_impl(plan, workspace, q, k_pages, v_pages, block_table, seq_lens, num_splits,
+                     scale, 1.f, k_scale, v_scale, out, lse, stream);
 }
 
 splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32_t n_parts,

@@ -156,7 +156,8 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
     }
   }
   float lse_n = -INFINITY;
-  const float inv = lsum > 0.f ? a.o_scale / lsum : 0.f;
+  const float osc = a.v_scale ? __ldg(a.v_scale + h0 + hs) : a.o_scale;
+  const float inv = lsum > 0.f ? osc / lsum : 0.f;
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] *= inv;
   if (lsum > 0.f) lse_n = (M + lg2(lsum)) * kLn2;
@@ -384,6 +385,8 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG>::THREADS, kGqaCtasPerSm)
   const int rg = slot_w / HPI;         //   query rows [8 rg, 8 rg + 8) of that head
   const int hkv = h0 + hs;
   const int rph = a.T * a.G;           // query rows per KV head
+  // scores -> log2 units: scale (and the e4m3 K scale, per KV head if given)
+  const float qk_l2 = a.k_scale ? a.qk_scale_log2 * __ldg(a.k_scale + hkv) : a.qk_scale_log2;
 
   // Q^T operand fragments: query row n = 8 rg + gi of this head, dims by ti
   // (see the layout notes); rows past the head's T*G rows are zero.
@@ -489,8 +492,8 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG>::THREADS, kGqaCtasPerSm)
     for (int r = 0; r < 4; ++r) sc[r] += sd[r];
 
     // ---- scores in log2 units, masked
-    float s0 = sc[0] * a.qk_scale_log2, s1 = sc[1] * a.qk_scale_log2;
-    float s2 = sc[2] * a.qk_scale_log2, s3 = sc[3] * a.qk_scale_log2;
+    float s0 = sc[0] * qk_l2, s1 = sc[1] * qk_l2;
+    float s2 = sc[2] * qk_l2, s3 = sc[3] * qk_l2;
     if (key0 + 15 > min_lim) {
       const int ka = key0 + gi, kb = ka + 8;
       s0 = ka <= lim0 ? s0 : -INFINITY;

@@ -86,6 +86,8 @@ struct DecodeArgs {
   int32_t batch, T, Hq, Hkv, G, P, max_pages, num_pages, rows, dv;
   float qk_scale_log2;  // scale * kv_scale (FP8 only) * log2(e)
   float o_scale;        // factor applied to the normalised output (FP8: kv_scale)
+  const float* k_scale;  // e4m3 per-KV-head scales [Hkv] (device) or null: the
+  const float* v_scale;  //   kernel multiplies qk_scale_log2 / o_scale by them
   int32_t fused;        // 1: last CTA of a group merges
   int32_t kv_box3d;     // bf16 K/V maps are 3-D: one [2][16][64] box per 16-key tile
   int32_t hpi;          // KV heads per item (e4m3 boxes are [hpi][16][128])

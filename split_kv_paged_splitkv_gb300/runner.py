@@ -8,7 +8,7 @@ from __future__ import annotations
 import torch
 
 from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, make_desc, splitkv_decode,
-               splitkv_plan, splitkv_plan_upload, splitkv_read_stats)
+               splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_upload, splitkv_read_stats)
 
 
 class DecodeSession:
@@ -22,7 +22,7 @@ class DecodeSession:
 
     def __init__(self, q, k_pages, v_pages, block_table, seq_lens, seq_lens_host, *, scale,
                  kv_scale=1.0, num_splits=0, num_sms=0, v_dim=None, v_shares_k=False,
-                 combine_mode=SPLITKV_COMBINE_SEPARATE, stream=None):
+                 combine_mode=SPLITKV_COMBINE_SEPARATE, stream=None, k_scale=None, v_scale=None):
         B, T, Hq, Dk = q.shape
         N, Hkv, P, _ = k_pages.shape
         if v_dim is None:
@@ -39,14 +39,21 @@ class DecodeSession:
         splitkv_plan_upload(self.plan, self.workspace, self.workspace.numel(), stream)
         self.tensors = (q, k_pages, v_pages, block_table, seq_lens)
         self.scale, self.kv_scale = float(scale), float(kv_scale)
+        self.k_scale, self.v_scale = k_scale, v_scale  # per-KV-head e4m3 scales, or None
         self.out = torch.empty((B, T, Hq, v_dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
 
     def run(self, out=None, lse=None, tensors=None):
         q, k, v, table, lens = tensors if tensors is not None else self.tensors
-        splitkv_decode(self.plan, self.workspace, q, k, v, table, lens, self.num_splits,
-                       self.scale, self.kv_scale, self.out if out is None else out,
-                       self.lse if lse is None else lse, self.stream)
+        o = self.out if out is None else out
+        l = self.lse if lse is None else lse
+        if self.k_scale is not None:
+            splitkv_decode_kv_scales(self.plan, self.workspace, q, k, v, table, lens,
+                                     self.num_splits, self.scale, self.k_scale, self.v_scale, o, l,
+                                     self.stream)
+        else:
+            splitkv_decode(self.plan, self.workspace, q, k, v, table, lens, self.num_splits,
+                           self.scale, self.kv_scale, o, l, self.stream)
         return self.out if out is None else out, self.lse if lse is None else lse
 
     def stats(self):

@@ -37,8 +37,8 @@ def _desc(B=1, T=1, Hq=16, Hkv=2, D=128, Dv=128, P=16, maxp=512, N=600, fp8=Fals
 GQA_CTAS_PER_SM = 3
 
 
-def _expected_hpi(Hkv, fp8):
-    if not fp8:
+def _expected_hpi(Hkv, fp8, rows_per_head=8):
+    if not fp8 or rows_per_head > 8:
         return 1
     return next(h for h in (4, 2, 1) if Hkv % h == 0)
 
@@ -160,6 +160,33 @@ def test_decode_validates_before_any_cuda_call():
                                      args["v"], args["table"], args["lens"], args["num_splits"],
                                      args["scale"], args["kv_scale"], args["out"], args["lse"], None)
         assert st in (skv.SPLITKV_EINVAL, skv.SPLITKV_EWORKSPACE), (c, st)
+        assert skv.splitkv_last_error()
+
+
+def test_heads_per_item_is_one_above_eight_rows_per_head():
+    for T, G, want in ((1, 8, 4), (2, 8, 1), (3, 4, 1), (2, 4, 4)):
+        d = _desc(T=T, Hq=8 * G, Hkv=8, fp8=True)
+        plan = skv.splitkv_plan(d, np.array([300], np.int32), 0, 148)
+        assert skv.splitkv_plan_heads_per_item(plan) == _expected_hpi(8, True, T * G) == want
+
+
+def test_decode_kv_scales_validates_before_any_cuda_call():
+    A = 1 << 20
+    fp8_plan = skv.splitkv_plan(_desc(fp8=True), np.array([100], np.int32), 2, 148)
+    bf16_plan = skv.splitkv_plan(_desc(), np.array([100], np.int32), 2, 148)
+    cases = [
+        (fp8_plan, dict(ks=None), skv.SPLITKV_EINVAL),
+        (fp8_plan, dict(vs=None), skv.SPLITKV_EINVAL),
+        (fp8_plan, dict(ks=A + 2), skv.SPLITKV_EINVAL),
+        (bf16_plan, dict(), skv.SPLITKV_EUNSUPPORTED),
+        (fp8_plan, dict(q=None), skv.SPLITKV_EINVAL),
+    ]
+    for plan, c, code in cases:
+        args = dict(q=A, ks=A, vs=A)
+        args.update(c)
+        st = skv._lib.splitkv_decode_kv_scales(plan.handle, A, args["q"], A, A, A, A, 2, 0.1,
+                                               args["ks"], args["vs"], A, A, None)
+        assert st == code, (c, st)
         assert skv.splitkv_last_error()
 
 

@@ -11,6 +11,7 @@ import oracle
 import workloads
 import split_kv_paged_splitkv_gb300 as skv
 from _support import LSE_TOL, OUT_TOL, compare, need_gpu, oracle_direct, session
+from split_kv_paged_splitkv_gb300.runner import DecodeSession
 
 pytestmark = pytest.mark.gpu
 W = workloads.WORKLOADS
@@ -149,6 +150,37 @@ def test_multi_token_causal(T, G, fp8):
         for mode in ((1, 0) if S == 5 else (1,)):
             out, lse = session(x, S, mode).run()
             compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} S={S} mode={mode}")
+
+
+@pytest.mark.parametrize("T,G,Hkv", [(1, 8, 4), (1, 4, 8), (2, 8, 2), (1, 2, 3)])
+def test_per_head_kv_scales(T, G, Hkv):
+    """e4m3 cache with its own K and V scale per KV head (splitkv_decode_kv_scales),
+    against the oracle dequantising K and V with those scales; also separate
+    per-tensor K and V scales (all heads equal)."""
+    w = _custom([T + 3, 233, 1000, 16 * 9], G=G, Hkv=Hkv, T=T, fp8=True, seed=40 + Hkv)
+    x = workloads.make_inputs(w, device="cuda")
+    rng = np.random.default_rng(Hkv * 10 + G)
+    # at most the cache's own quantisation scale, so values keep the N(0, 1)
+    # magnitude the absolute bf16 output bar is set for (one bf16 ulp is
+    # 2^-5 for |out| in [4, 8))
+    c = float(x.kv_scale)
+    per_head = (c * rng.uniform(0.4, 1.0, Hkv), c * rng.uniform(0.4, 1.0, Hkv))
+    per_tensor = (np.full(Hkv, 0.9 * c), np.full(Hkv, 0.6 * c))
+    for ks, vs in (per_head, per_tensor):
+        ref_o, ref_l = oracle.attention_direct(
+            workloads.bits(x.q), workloads.bits(x.k_pages), workloads.bits(x.v_pages),
+            x.block_table.cpu().numpy(), x.seq_lens_host, scale=x.scale, kv_dtype="fp8_e4m3",
+            k_scale=ks.astype(np.float32).astype(np.float64),
+            v_scale=vs.astype(np.float32).astype(np.float64))
+        kt = torch.tensor(ks, dtype=torch.float32, device="cuda")
+        vt = torch.tensor(vs, dtype=torch.float32, device="cuda")
+        for S, mode in ((1, 1), (3, 1), (0, 0)):
+            s = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens,
+                              x.seq_lens_host, scale=x.scale, num_splits=S, combine_mode=mode,
+                              k_scale=kt, v_scale=vt)
+            out, lse = s.run()
+            compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} Hkv={Hkv} S={S}")
+            assert s.stats()[1] == 0
 
 
 @pytest.mark.parametrize("fp8", [False, True])
