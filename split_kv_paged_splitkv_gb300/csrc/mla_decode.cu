@@ -13,17 +13,30 @@
 // Each CTA computes the full 576-wide scores of its token itself, so the
 // two CTAs never exchange anything (on this part, moving a 64-key block of
 // fp32 partial scores between the CTAs of a cluster took about three times
-// as long as computing the scores).  Per 64-key block (one page):
-//   1. S = Q . K^T        (tcgen05, M=128 N=64 K=576; Q dims [0, 320) from
-//                          TMEM, [320, 576) from shared memory)
+// as long as computing the scores).
+//
+// The nine 64-column chunks of a key row split by use: the CTA's four V
+// chunks (columns [256 h, 256 h + 256)) serve the scores and the PV product;
+// the other five serve the scores only.  They stream through two rings of
+// two slots, each fed by its own producer warp:
+//   N ring: the five score-only chunks of a block, released as soon as the
+//           block's score MMAs have read them;
+//   V ring: the four V chunks of a block, released after the block's PV.
+// The score product reads the V chunks last, so a V slot freed by PV(j)
+// has that much more time to be refilled for block j + 2.
+// Per 64-key block (one page):
+//   1. S = Q . K^T        (tcgen05, M=128 N=64 K=576: first the five
+//                          score-only chunks, Q from TMEM, then the four V
+//                          chunks, Q from shared memory)
 //   2. softmax warps: online softmax with a lazy reference maximum (O is
 //      rescaled only when a row maximum grows by more than 2^8); P (bf16)
 //      goes to TMEM
 //   3. O_h += P . V_h      (tcgen05, M=128 N=256 K=64, P from TMEM)
-// TMEM columns: S [0, 64), P [64, 96), Q dims [0, 320) [96, 256), O_h [256, 512).
-// Warp roles: warp 0 TMA producer and TMEM owner, warp 1 MMA issuer (whole
-// warps run the issue loops; one elected lane issues), warps 2-5 load Q,
-// then softmax and epilogue (thread = query head = TMEM lane).
+// TMEM columns: S [0, 64), P [64, 96), Q score-only chunks [96, 256), O_h
+// [256, 512).  Warp roles: warp 0 N-ring producer and TMEM owner, warp 1 MMA
+// issuer (whole warps run the issue loops; one elected lane issues), warps
+// 2-5 load Q, then softmax and epilogue (thread = query head = TMEM lane),
+// warp 6 V-ring producer.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -38,38 +51,46 @@ struct Mla {
   static constexpr int DK = 576, DV = 512;
   static constexpr int ROWS = 128;          // query heads of one token
   static constexpr int BK = 64;             // keys per block (= one page)
-  static constexpr int NCH = 9;             // 64-dim chunks of a 576-wide row
-  static constexpr int NCH_TMEM = 5;        // Q chunks held in TMEM (the rest in smem)
-  static constexpr int K_CH = BK * 128;     // one K chunk: 64 keys x 64 bf16 = 8 KB
+  static constexpr int NN = 5;              // score-only chunks of a key row
+  static constexpr int NV = 4;              // V chunks of a key row (this CTA's half)
+  static constexpr int K_CH = BK * 128;     // one key chunk: 64 keys x 64 bf16 = 8 KB
   static constexpr int Q_CH = ROWS * 128;   // one Q chunk: 128 rows x 64 bf16 = 16 KB
-  static constexpr int NST = 2;             // key-block stages
-  static constexpr int K_STAGE = NCH * K_CH;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + (NCH - NCH_TMEM) * Q_CH;
-  static constexpr int OFF_BAR = OFF_K + NST * K_STAGE;
+  static constexpr int NST = 2;             // slots per ring
+  static constexpr int N_SLOT = NN * K_CH;
+  static constexpr int V_SLOT = NV * K_CH;
+  static constexpr int OFF_Q = 0;                       // Q's V chunks (K-major, swizzled)
+  static constexpr int OFF_N = OFF_Q + NV * Q_CH;       // N ring
+  static constexpr int OFF_V = OFF_N + NST * N_SLOT;    // V ring
+  static constexpr int OFF_BAR = OFF_V + NST * V_SLOT;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 224;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL = 0, P_COL = 64, Q_COL = 96, O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.f;  // lazy maximum: rescale when it grows by > 2^8
 };
-static_assert(Mla::Q_COL + Mla::NCH_TMEM * 32 <= Mla::O_COL, "Q overlaps O in TMEM");
+static_assert(Mla::Q_COL + Mla::NN * 32 <= Mla::O_COL, "Q overlaps O in TMEM");
 static_assert(Mla::SMEM <= 227 * 1024, "shared memory budget");
 
 constexpr float kLn2m = 0.6931471805599453f;
 
 // Barrier slots (8 bytes each) after OFF_BAR.
 enum {
-  B_QFULL = 0,   // Q written to TMEM and shared memory (128 softmax threads)
-  B_KFULL = 1,   // [NST]
-  B_KEMPTY = B_KFULL + Mla::NST,  // [NST]
-  B_SFULL = B_KEMPTY + Mla::NST,
-  B_SFREE,       // softmax threads have read S (128)
-  B_PFULL,       // P written to TMEM (128)
+  B_QFULL = 0,                      // Q written to TMEM and shared memory (128 threads)
+  B_NFULL = 1,                      // [NST]
+  B_NEMPTY = B_NFULL + Mla::NST,    // [NST]
+  B_VFULL = B_NEMPTY + Mla::NST,    // [NST]
+  B_VEMPTY = B_VFULL + Mla::NST,    // [NST]
+  B_SFULL = B_VEMPTY + Mla::NST,
+  B_SFREE,                          // softmax threads have read S (128)
+  B_PFULL,                          // P written to TMEM (128)
   B_PFREE,
-  B_DONE,        // every MMA this CTA issued has completed
+  B_DONE,                           // every MMA this CTA issued has completed
   B_COUNT
 };
+
+// Column chunk (of the nine) held in N-ring slot i / V slot chunk k by half h.
+__device__ __forceinline__ int n_chunk(int h, int i) { return h == 0 ? 4 + i : (i < 4 ? i : 8); }
+__device__ __forceinline__ int v_chunk(int h, int k) { return 4 * h + k; }
 
 __global__ void __launch_bounds__(Mla::THREADS, 1)
     mla_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk) {
@@ -97,8 +118,10 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 128);
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_NFULL + s), 1);
+      mbar_init(bar(B_NEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFREE), 128);
@@ -127,8 +150,16 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
   if (threadIdx.x == 0 && h == 0 && t == 0 && a.seq_lens[b] != L)
     atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
 
-  if (warp == 0) {
-    // -------------------------------------------------------------- producer
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 loads the score-only chunks of block j into N slot j % NST (free
+    // once the score MMAs of block j - NST are done); warp 6 loads the V
+    // chunks into V slot j % NST (free once PV(j - NST) is done).
+    const bool vring = warp == 6;
+    const int nchk = vring ? C::NV : C::NN;
+    const uint32_t full0 = vring ? B_VFULL : B_NFULL, empty0 = vring ? B_VEMPTY : B_NEMPTY;
+    const int slot_bytes = vring ? C::V_SLOT : C::N_SLOT;
+    uint8_t* ring = sm + (vring ? C::OFF_V : C::OFF_N);
     const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
     bool ok = true;
     int issued = 0;
@@ -147,15 +178,14 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
           }
         }
       }
-      const int ph = __shfl_sync(kFull, phys, page - chunk0);
+      const int y = (__shfl_sync(kFull, phys, page - chunk0) * a.Hkv) * a.P;
       const int st = j % C::NST;
-      if (j >= C::NST) ok = __all_sync(kFull, mbar_wait(bar(B_KEMPTY + st), ((j / C::NST) - 1) & 1));
+      if (j >= C::NST) ok = __all_sync(kFull, mbar_wait(bar(empty0 + st), ((j / C::NST) - 1) & 1));
       if (!ok) break;
-      mbar_arrive_expect_tx_warp(bar(B_KFULL + st), C::K_STAGE);
-#pragma unroll
-      for (int i = 0; i < C::NCH; ++i)
-        tma_load_2d_warp(smem_u32(sm + C::OFF_K + st * C::K_STAGE + i * C::K_CH), &tk, bar(B_KFULL + st),
-                         i * 64, (ph * a.Hkv) * a.P);
+      mbar_arrive_expect_tx_warp(bar(full0 + st), slot_bytes);
+      for (int k = 0; k < nchk; ++k)
+        tma_load_2d_warp(smem_u32(ring + st * slot_bytes + k * C::K_CH), &tk, bar(full0 + st),
+                         (vring ? v_chunk(h, k) : n_chunk(h, k)) * 64, y);
       issued = j + 1;
     }
     if (!ok && lane == 0) {
@@ -166,30 +196,31 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     if (lane == 0) {
       for (int st = 0; st < C::NST && st < issued; ++st) {
         const int last = st + C::NST * ((issued - 1 - st) / C::NST);
-        if (!mbar_wait(bar(B_KFULL + st), (last / C::NST) & 1)) break;
+        if (!mbar_wait(bar(full0 + st), (last / C::NST) & 1)) break;
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
+    // Issue order follows readiness: PV(jp) as soon as P(jp) is in TMEM (it
+    // frees a V slot); else the next half of QK(jq): the score-only chunks
+    // once their slot landed and the softmax warps have read S(jq - 1) (S is
+    // single-buffered), then the V chunks once their slot landed.
     const uint32_t idesc_qk = umma_idesc_bf16(128, 64, 0, 0);
     const uint32_t idesc_pv = umma_idesc_bf16(128, 256, 0, 1);
     bool ok = __all_sync(kFull, mbar_wait(bar(B_QFULL), 0));
-    // Issue order follows readiness: PV(jp) as soon as P(jp) is in TMEM (it
-    // releases a K stage), else QK(jq) once its keys have landed and the
-    // softmax warps have read S(jq - 1) (S is single-buffered).
     int jq = 0, jp = 0;
+    bool qk_half = false;  // the score-only half of QK(jq) has been issued
     long long t_idle = clock64();
     while (ok && jp < nblk) {
-      const bool pv_ready = jp < jq && __shfl_sync(kFull, mbar_test(bar(B_PFULL), jp & 1), 0);
-      if (pv_ready) {  // O_h += P_jp . V_jp
-        const int st = jp % C::NST;
+      if (jp < jq && __shfl_sync(kFull, mbar_test(bar(B_PFULL), jp & 1), 0)) {  // O_h += P.V
+        const int vs = jp % C::NST;
         tc_fence_after();
-        uint8_t* vst = sm + C::OFF_K + st * C::K_STAGE + 4 * h * C::K_CH;  // this CTA's V chunks
+        uint8_t* vst = sm + C::OFF_V + vs * C::V_SLOT;
         const int valid = min(C::BK, k_end - (k_begin + jp * C::BK));
         if (valid < C::BK) {
           // key slots past the last key may hold anything (even NaN): zero their
-          // V rows so that 0 * V stays 0 in the PV product
-          for (int x = lane; x < (C::BK - valid) * 8 * 4; x += 32) {
+          // V rows so that 0 * V stays 0 in the PV product (QK(jp) is complete)
+          for (int x = lane; x < (C::BK - valid) * 8 * C::NV; x += 32) {
             const int r = valid + (x >> 5), ch = (x >> 3) & 3, c16 = x & 7;
             *reinterpret_cast<uint4*>(vst + ch * C::K_CH + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -202,42 +233,54 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
           umma_bf16_ta_warp(tmem + C::O_COL, tmem + C::P_COL + uint32_t(kin * 8), bd, idesc_pv,
                             (jp | kin) != 0);
         }
-        umma_commit_warp(bar(B_KEMPTY + st));
+        umma_commit_warp(bar(B_VEMPTY + vs));
         umma_commit_warp(bar(B_PFREE));
         __syncwarp();
         ++jp;
         t_idle = clock64();
         continue;
       }
-      const int st = jq % C::NST;
-      const bool qk_ready =
-          jq < nblk &&
-          __shfl_sync(kFull,
-                      mbar_test(bar(B_KFULL + st), (jq / C::NST) & 1) &&
-                          (jq == 0 || mbar_test(bar(B_SFREE), (jq - 1) & 1)),
-                      0);
-      if (qk_ready) {  // S = Q . K_jq^T
-        tc_fence_after();
-        const uint32_t kst = smem_u32(sm + C::OFF_K + st * C::K_STAGE);
+      const int qs = jq % C::NST;
+      if (jq < nblk && !qk_half) {  // score-only chunks of QK(jq), Q from TMEM
+        const bool rdy = __shfl_sync(
+            kFull,
+            mbar_test(bar(B_NFULL + qs), (jq / C::NST) & 1) &&
+                (jq == 0 || mbar_test(bar(B_SFREE), (jq - 1) & 1)),
+            0);
+        if (rdy) {
+          tc_fence_after();
+          const uint32_t nst = smem_u32(sm + C::OFF_N + qs * C::N_SLOT);
 #pragma unroll
-        for (int i = 0; i < C::NCH; ++i)
+          for (int i = 0; i < C::NN; ++i)
 #pragma unroll
-          for (int kin = 0; kin < 4; ++kin) {
-            const uint64_t bd = umma_desc(kst + i * C::K_CH + kin * 32, 16, 1024, 2);
-            if (i < C::NCH_TMEM) {
-              umma_bf16_ta_warp(tmem + C::S_COL, tmem + C::Q_COL + uint32_t(i * 32 + kin * 8), bd,
-                                idesc_qk, (i | kin) != 0);
-            } else {
-              const uint64_t ad =
-                  umma_desc(smem_u32(sm + C::OFF_Q + (i - C::NCH_TMEM) * C::Q_CH) + kin * 32, 16, 1024, 2);
-              umma_bf16_warp(tmem + C::S_COL, ad, bd, idesc_qk, 1u);
-            }
-          }
-        umma_commit_warp(bar(B_SFULL));
-        __syncwarp();
-        ++jq;
-        t_idle = clock64();
-        continue;
+            for (int kin = 0; kin < 4; ++kin)
+              umma_bf16_ta_warp(tmem + C::S_COL, tmem + C::Q_COL + uint32_t(i * 32 + kin * 8),
+                                umma_desc(nst + i * C::K_CH + kin * 32, 16, 1024, 2), idesc_qk,
+                                (i | kin) != 0);
+          umma_commit_warp(bar(B_NEMPTY + qs));
+          __syncwarp();
+          qk_half = true;
+          t_idle = clock64();
+          continue;
+        }
+      } else if (jq < nblk) {  // V chunks of QK(jq), Q from shared memory
+        if (__shfl_sync(kFull, mbar_test(bar(B_VFULL + qs), (jq / C::NST) & 1), 0)) {
+          tc_fence_after();
+          const uint32_t vst = smem_u32(sm + C::OFF_V + qs * C::V_SLOT);
+#pragma unroll
+          for (int k = 0; k < C::NV; ++k)
+#pragma unroll
+            for (int kin = 0; kin < 4; ++kin)
+              umma_bf16_warp(tmem + C::S_COL,
+                             umma_desc(smem_u32(sm + C::OFF_Q + k * C::Q_CH) + kin * 32, 16, 1024, 2),
+                             umma_desc(vst + k * C::K_CH + kin * 32, 16, 1024, 2), idesc_qk, 1u);
+          umma_commit_warp(bar(B_SFULL));
+          __syncwarp();
+          ++jq;
+          qk_half = false;
+          t_idle = clock64();
+          continue;
+        }
       }
       __nanosleep(32);  // leave issue slots to the softmax warp on this SM sub-partition
       ok = __shfl_sync(kFull, clock64() - t_idle < kWaitTimeoutCycles, 0);
@@ -256,18 +299,19 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     const int r = g * 32 + lane;     // query head = TMEM lane
     const uint32_t lane_base = tmem + (uint32_t(g * 32) << 16);
 
-    // Q row r: chunks [0, 5) -> TMEM (32-bit column c of a chunk holds dims
-    // 2c, 2c + 1, the even one in the low half: the A-from-TMEM layout);
-    // chunks [5, 9) -> shared memory, 128-byte swizzled K-major rows
+    // Q row r: its score-only chunks -> TMEM (32-bit column c of a chunk holds
+    // dims 2c, 2c + 1, the even one in the low half: the A-from-TMEM layout);
+    // its V chunks -> shared memory, 128-byte swizzled K-major rows
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                          ((size_t(b) * a.T + t) * a.Hq + r) * C::DK);
 #pragma unroll 1
-      for (int i = 0; i < C::NCH_TMEM; ++i) {
+      for (int i = 0; i < C::NN; ++i) {
+        const uint4* src = qrow + n_chunk(h, i) * 8;
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 x = __ldg(qrow + i * 8 + v);
+          const uint4 x = __ldg(src + v);
           w[4 * v] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
@@ -276,11 +320,12 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
         tmem_st32u(lane_base + C::Q_COL + uint32_t(i * 32), w);
       }
 #pragma unroll 1
-      for (int i = C::NCH_TMEM; i < C::NCH; ++i) {
-        uint8_t* dst = sm + C::OFF_Q + (i - C::NCH_TMEM) * C::Q_CH + r * 128;
+      for (int k = 0; k < C::NV; ++k) {
+        const uint4* src = qrow + v_chunk(h, k) * 8;
+        uint8_t* dst = sm + C::OFF_Q + k * C::Q_CH + r * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<uint4*>(dst + ((v ^ (r & 7)) << 4)) = __ldg(qrow + i * 8 + v);
+          *reinterpret_cast<uint4*>(dst + ((v ^ (r & 7)) << 4)) = __ldg(src + v);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tmem_wait_st();
