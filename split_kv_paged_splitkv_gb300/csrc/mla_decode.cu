@@ -15,28 +15,29 @@
 // fp32 partial scores between the CTAs of a cluster took about three times
 // as long as computing the scores).
 //
-// The nine 64-column chunks of a key row split by use: the CTA's four V
-// chunks (columns [256 h, 256 h + 256)) serve the scores and the PV product;
-// the other five serve the scores only.  They stream through two rings of
-// two slots, each fed by its own producer warp:
-//   N ring: the five score-only chunks of a block, released as soon as the
+// The nine 64-column chunks of a key row split by where the matching query
+// chunk lives.  Four score-only chunks pair with query chunks held in TMEM;
+// the CTA's four V chunks (columns [256 h, 256 h + 256)) and the rope chunk
+// pair with query chunks in shared memory.  They stream through two rings
+// of two slots, each fed by its own producer warp:
+//   N ring: the four TMEM-paired chunks of a block, released as soon as the
 //           block's score MMAs have read them;
-//   V ring: the four V chunks of a block, released after the block's PV.
-// The score product reads the V chunks last, so a V slot freed by PV(j)
-// has that much more time to be refilled for block j + 2.
+//   V ring: the V chunks and the rope chunk, released after the block's PV
+//           (the score product reads them last).
+// S is double-buffered; P is written over the first 32 columns of its own
+// S buffer, so the scores of block j + 1 accumulate while the softmax warps
+// work on block j, and the scores of block j + 2 wait only for PV(j).
 // Per 64-key block (one page):
-//   1. S = Q . K^T        (tcgen05, M=128 N=64 K=576: first the five
-//                          score-only chunks, Q from TMEM, then the four V
-//                          chunks, Q from shared memory)
+//   1. S_b = Q . K^T      (tcgen05, M=128 N=64 K=576, b = j % 2)
 //   2. softmax warps: online softmax with a lazy reference maximum (O is
-//      rescaled only when a row maximum grows by more than 2^8); P (bf16)
-//      goes to TMEM
+//      rescaled only when a row maximum grows by more than 2^8, after PV(j-1)
+//      has finished); P (bf16) goes into S_b
 //   3. O_h += P . V_h      (tcgen05, M=128 N=256 K=64, P from TMEM)
-// TMEM columns: S [0, 64), P [64, 96), Q score-only chunks [96, 256), O_h
-// [256, 512).  Warp roles: warp 0 N-ring producer and TMEM owner, warp 1 MMA
-// issuer (whole warps run the issue loops; one elected lane issues), warps
-// 2-5 load Q, then softmax and epilogue (thread = query head = TMEM lane),
-// warp 6 V-ring producer.
+// TMEM columns: S_0 [0, 64), S_1 [64, 128), Q's four TMEM chunks [128, 256),
+// O_h [256, 512).  Warp roles: warp 0 N-ring producer and TMEM owner, warp 1
+// MMA issuer (whole warps run the issue loops; one elected lane issues),
+// warps 2-5 load Q, then softmax and epilogue (thread = query head = TMEM
+// lane), warp 6 V-ring producer.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -51,24 +52,26 @@ struct Mla {
   static constexpr int DK = 576, DV = 512;
   static constexpr int ROWS = 128;          // query heads of one token
   static constexpr int BK = 64;             // keys per block (= one page)
-  static constexpr int NN = 5;              // score-only chunks of a key row
-  static constexpr int NV = 4;              // V chunks of a key row (this CTA's half)
+  static constexpr int NN = 4;              // N-ring chunks (query chunk in TMEM)
+  static constexpr int NV = 4;              // V chunks of this CTA's half
+  static constexpr int NX = NV + 1;         // V-ring chunks: the V chunks and the rope chunk
   static constexpr int K_CH = BK * 128;     // one key chunk: 64 keys x 64 bf16 = 8 KB
   static constexpr int Q_CH = ROWS * 128;   // one Q chunk: 128 rows x 64 bf16 = 16 KB
   static constexpr int NST = 2;             // slots per ring
   static constexpr int N_SLOT = NN * K_CH;
-  static constexpr int V_SLOT = NV * K_CH;
-  static constexpr int OFF_Q = 0;                       // Q's V chunks (K-major, swizzled)
-  static constexpr int OFF_N = OFF_Q + NV * Q_CH;       // N ring
+  static constexpr int V_SLOT = NX * K_CH;
+  static constexpr int OFF_Q = 0;                       // Q's V-ring chunks (K-major, swizzled)
+  static constexpr int OFF_N = OFF_Q + NX * Q_CH;       // N ring
   static constexpr int OFF_V = OFF_N + NST * N_SLOT;    // V ring
   static constexpr int OFF_BAR = OFF_V + NST * V_SLOT;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
   static constexpr int THREADS = 224;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL = 0, P_COL = 64, Q_COL = 96, O_COL = 256;
+  static constexpr uint32_t S_COL = 0, Q_COL = 128, O_COL = 256;  // S_b at S_COL + 64 b
   static constexpr float RESCALE_LOG2 = 8.f;  // lazy maximum: rescale when it grows by > 2^8
 };
 static_assert(Mla::Q_COL + Mla::NN * 32 <= Mla::O_COL, "Q overlaps O in TMEM");
+static_assert(Mla::S_COL + 2 * 64 <= Mla::Q_COL, "S buffers overlap Q in TMEM");
 static_assert(Mla::SMEM <= 227 * 1024, "shared memory budget");
 
 constexpr float kLn2m = 0.6931471805599453f;
@@ -80,17 +83,17 @@ enum {
   B_NEMPTY = B_NFULL + Mla::NST,    // [NST]
   B_VFULL = B_NEMPTY + Mla::NST,    // [NST]
   B_VEMPTY = B_VFULL + Mla::NST,    // [NST]
-  B_SFULL = B_VEMPTY + Mla::NST,
-  B_SFREE,                          // softmax threads have read S (128)
-  B_PFULL,                          // P written to TMEM (128)
-  B_PFREE,
+  B_SFULL = B_VEMPTY + Mla::NST,    // [2] S_b complete
+  B_PFULL = B_SFULL + 2,            // [2] P written over S_b (128); one barrier per
+                                    // buffer, so no barrier runs two phases ahead
+  B_PFREE = B_PFULL + 2,            // PV done (P read, O stable)
   B_DONE,                           // every MMA this CTA issued has completed
   B_COUNT
 };
 
-// Column chunk (of the nine) held in N-ring slot i / V slot chunk k by half h.
-__device__ __forceinline__ int n_chunk(int h, int i) { return h == 0 ? 4 + i : (i < 4 ? i : 8); }
-__device__ __forceinline__ int v_chunk(int h, int k) { return 4 * h + k; }
+// Column chunk (of the nine) in N-ring slot chunk i / V-ring slot chunk k of half h.
+__device__ __forceinline__ int n_chunk(int h, int i) { return h == 0 ? 4 + i : i; }
+__device__ __forceinline__ int v_chunk(int h, int k) { return k < 4 ? 4 * h + k : 8; }
 
 __global__ void __launch_bounds__(Mla::THREADS, 1)
     mla_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk) {
@@ -124,8 +127,9 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
       mbar_init(bar(B_VEMPTY + s), 1);
     }
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SFREE), 128);
+    mbar_init(bar(B_SFULL + 1), 1);
     mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_PFULL + 1), 128);
     mbar_init(bar(B_PFREE), 1);
     mbar_init(bar(B_DONE), 1);
     *abort_flag = 0;
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     // once the score MMAs of block j - NST are done); warp 6 loads the V
     // chunks into V slot j % NST (free once PV(j - NST) is done).
     const bool vring = warp == 6;
-    const int nchk = vring ? C::NV : C::NN;
+    const int nchk = vring ? C::NX : C::NN;
     const uint32_t full0 = vring ? B_VFULL : B_NFULL, empty0 = vring ? B_VEMPTY : B_NEMPTY;
     const int slot_bytes = vring ? C::V_SLOT : C::N_SLOT;
     uint8_t* ring = sm + (vring ? C::OFF_V : C::OFF_N);
@@ -202,20 +206,20 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     // Issue order follows readiness: PV(jp) as soon as P(jp) is in TMEM (it
-    // frees a V slot); else the next half of QK(jq): the score-only chunks
-    // once their slot landed and the softmax warps have read S(jq - 1) (S is
-    // single-buffered), then the V chunks once their slot landed.
+    // frees a V slot); else the next half of QK(jq) into S_{jq % 2}: the
+    // N-ring chunks once their slot landed and PV(jq - 2) has read the P
+    // that shares that S buffer, then the V-ring chunks once their slot landed.
     const uint32_t idesc_qk = umma_idesc_bf16(128, 64, 0, 0);
     const uint32_t idesc_pv = umma_idesc_bf16(128, 256, 0, 1);
     bool ok = __all_sync(kFull, mbar_wait(bar(B_QFULL), 0));
     int jq = 0, jp = 0;
-    bool qk_half = false;  // the score-only half of QK(jq) has been issued
+    bool qk_half = false;  // the N-ring half of QK(jq) has been issued
     long long t_idle = clock64();
     while (ok && jp < nblk) {
-      if (jp < jq && __shfl_sync(kFull, mbar_test(bar(B_PFULL), jp & 1), 0)) {  // O_h += P.V
+      if (jp < jq && __shfl_sync(kFull, mbar_test(bar(B_PFULL + (jp & 1)), (jp >> 1) & 1), 0)) {  // O_h += P.V
         const int vs = jp % C::NST;
         tc_fence_after();
-        uint8_t* vst = sm + C::OFF_V + vs * C::V_SLOT;
+        uint8_t* vst = sm + C::OFF_V + vs * C::V_SLOT;  // its first NV chunks are V_h
         const int valid = min(C::BK, k_end - (k_begin + jp * C::BK));
         if (valid < C::BK) {
           // key slots past the last key may hold anything (even NaN): zero their
@@ -227,10 +231,11 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
         }
+        const uint32_t pcol = C::S_COL + uint32_t(64 * (jp & 1));  // P over S_{jp % 2}
 #pragma unroll
         for (int kin = 0; kin < 4; ++kin) {
           const uint64_t bd = umma_desc(smem_u32(vst) + kin * 16 * 128, C::K_CH, 1024, 2);
-          umma_bf16_ta_warp(tmem + C::O_COL, tmem + C::P_COL + uint32_t(kin * 8), bd, idesc_pv,
+          umma_bf16_ta_warp(tmem + C::O_COL, tmem + pcol + uint32_t(kin * 8), bd, idesc_pv,
                             (jp | kin) != 0);
         }
         umma_commit_warp(bar(B_VEMPTY + vs));
@@ -241,11 +246,12 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
         continue;
       }
       const int qs = jq % C::NST;
-      if (jq < nblk && !qk_half) {  // score-only chunks of QK(jq), Q from TMEM
+      const uint32_t scol = C::S_COL + uint32_t(64 * (jq & 1));
+      if (jq < nblk && !qk_half) {  // N-ring chunks of QK(jq), Q from TMEM
         const bool rdy = __shfl_sync(
             kFull,
             mbar_test(bar(B_NFULL + qs), (jq / C::NST) & 1) &&
-                (jq == 0 || mbar_test(bar(B_SFREE), (jq - 1) & 1)),
+                (jq < 2 || mbar_test(bar(B_PFREE), (jq - 2) & 1)),
             0);
         if (rdy) {
           tc_fence_after();
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
           for (int i = 0; i < C::NN; ++i)
 #pragma unroll
             for (int kin = 0; kin < 4; ++kin)
-              umma_bf16_ta_warp(tmem + C::S_COL, tmem + C::Q_COL + uint32_t(i * 32 + kin * 8),
+              umma_bf16_ta_warp(tmem + scol, tmem + C::Q_COL + uint32_t(i * 32 + kin * 8),
                                 umma_desc(nst + i * C::K_CH + kin * 32, 16, 1024, 2), idesc_qk,
                                 (i | kin) != 0);
           umma_commit_warp(bar(B_NEMPTY + qs));
@@ -263,18 +269,18 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
           t_idle = clock64();
           continue;
         }
-      } else if (jq < nblk) {  // V chunks of QK(jq), Q from shared memory
+      } else if (jq < nblk) {  // V-ring chunks of QK(jq), Q from shared memory
         if (__shfl_sync(kFull, mbar_test(bar(B_VFULL + qs), (jq / C::NST) & 1), 0)) {
           tc_fence_after();
           const uint32_t vst = smem_u32(sm + C::OFF_V + qs * C::V_SLOT);
 #pragma unroll
-          for (int k = 0; k < C::NV; ++k)
+          for (int k = 0; k < C::NX; ++k)
 #pragma unroll
             for (int kin = 0; kin < 4; ++kin)
-              umma_bf16_warp(tmem + C::S_COL,
+              umma_bf16_warp(tmem + scol,
                              umma_desc(smem_u32(sm + C::OFF_Q + k * C::Q_CH) + kin * 32, 16, 1024, 2),
                              umma_desc(vst + k * C::K_CH + kin * 32, 16, 1024, 2), idesc_qk, 1u);
-          umma_commit_warp(bar(B_SFULL));
+          umma_commit_warp(bar(B_SFULL + (jq & 1)));
           __syncwarp();
           ++jq;
           qk_half = false;
@@ -299,9 +305,9 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     const int r = g * 32 + lane;     // query head = TMEM lane
     const uint32_t lane_base = tmem + (uint32_t(g * 32) << 16);
 
-    // Q row r: its score-only chunks -> TMEM (32-bit column c of a chunk holds
+    // Q row r: its N-ring chunks -> TMEM (32-bit column c of a chunk holds
     // dims 2c, 2c + 1, the even one in the low half: the A-from-TMEM layout);
-    // its V chunks -> shared memory, 128-byte swizzled K-major rows
+    // its V-ring chunks -> shared memory, 128-byte swizzled K-major rows
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                          ((size_t(b) * a.T + t) * a.Hq + r) * C::DK);
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
         tmem_st32u(lane_base + C::Q_COL + uint32_t(i * 32), w);
       }
 #pragma unroll 1
-      for (int k = 0; k < C::NV; ++k) {
+      for (int k = 0; k < C::NX; ++k) {
         const uint4* src = qrow + v_chunk(h, k) * 8;
         uint8_t* dst = sm + C::OFF_Q + k * C::Q_CH + r * 128;
 #pragma unroll
@@ -336,21 +342,20 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nblk && ok; ++j) {
-      ok = __all_sync(kFull, mbar_wait(bar(B_SFULL), j & 1));
+      const uint32_t scol = C::S_COL + uint32_t(64 * (j & 1));
+      ok = __all_sync(kFull, mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
       float s[64];
       {
         float x[32];
-        tmem_ld32(lane_base + C::S_COL, x);
+        tmem_ld32(lane_base + scol, x);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[i] = x[i];
-        tmem_ld32(lane_base + C::S_COL + 32, x);
+        tmem_ld32(lane_base + scol + 32, x);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[32 + i] = x[i];
       }
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE));
 
       // row maximum (the thread owns its row), taken on the raw scores: the
       // scale is positive (checked on the host), so it commutes with the
@@ -380,7 +385,6 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
         l *= alpha;
       }
       const float nms = m_ref == -INFINITY ? 0.f : -m_ref;
-      // P(j) in registers before waiting for PV(j-1)
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -391,12 +395,11 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) pk[4 * c + i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
       }
-
-      // P(j) may only be written after PV(j-1) has read P(j-1)
-      if (j >= 1) ok = __all_sync(kFull, mbar_wait(bar(B_PFREE), (j - 1) & 1));
-      if (!ok) break;
-      tc_fence_after();
+      // O may only be rescaled once PV(j-1) has finished accumulating into it
       if (__any_sync(kFull, rescale_o)) {
+        if (j >= 1) ok = __all_sync(kFull, mbar_wait(bar(B_PFREE), (j - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
         for (int c0 = 0; c0 < 256; c0 += 32) {
           float o[32];
           tmem_ld32(lane_base + C::O_COL + uint32_t(c0), o);
@@ -405,10 +408,11 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
           tmem_st32(lane_base + C::O_COL + uint32_t(c0), o);
         }
       }
-      tmem_st32u(lane_base + C::P_COL, pk);
+      // P over the first 32 columns of S_b (S_b has been read into registers)
+      tmem_st32u(lane_base + scol, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + (j & 1)));
     }
     if (!ok) {
       atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
