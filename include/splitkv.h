@@ -128,6 +128,47 @@ enum {
 splitkv_status splitkv_plan(const splitkv_desc_t* desc, const int32_t* seq_lens_host,
                             int32_t num_splits, int32_t num_sms, splitkv_plan_t** plan_out);
 
+/*
+ * splitkv_plan_fixed -- a capacity plan for CUDA-graph-captured serving, where
+ * the sequence lengths change from step to step while every launch's grid is
+ * fixed ("Shipped: 484.5 tok/s on one GB300 ...", table "What shipped":
+ * split attention was enabled for one captured shape only).  The plan holds
+ * num_splits work items for every (sequence, KV-head group) -- B * Hkv /
+ * heads_per_item * num_splits items, in (b, head group, s) order -- and one
+ * combine group per (sequence, head group) when num_splits > 1.  Before each
+ * decode, splitkv_plan_refresh rewrites the work list on the device from the
+ * current lengths: with S_b = min(num_splits, ceil(L_b / P)) (1 for L_b == 0),
+ * items s < S_b get the page ranges splitkv_plan gives for this num_splits,
+ * and the others are marked unused (SPLITKV_ITEM_NSPLIT = 0): their CTAs are
+ * launched and exit at once, logging 0 keys.  splitkv_plan_get_items returns
+ * the all-unused template; splitkv_read_items reads the live list.
+ *   num_splits  1..64
+ * EINVAL for bad arguments; EUNSUPPORTED for shapes no kernel serves.
+ */
+splitkv_status splitkv_plan_fixed(const splitkv_desc_t* desc, int32_t num_splits,
+                                  splitkv_plan_t** plan_out);
+
+/*
+ * splitkv_plan_refresh -- one small kernel on `stream` that writes the work
+ * list of a capacity plan into `workspace` (uploaded once with
+ * splitkv_plan_upload) from seq_lens (device, int32 [B]); capturable in a CUDA
+ * graph together with splitkv_decode.  A length outside [0, max_pages_per_seq
+ * * P] or below q_tokens (and not 0) sets SPLITKV_DEVERR_SEQLEN in the status
+ * word and the sequence is served as empty (out = 0, lse = -inf).
+ * EINVAL if the plan was not made by splitkv_plan_fixed or for NULL or
+ * misaligned pointers.
+ */
+splitkv_status splitkv_plan_refresh(const splitkv_plan_t* plan, void* workspace,
+                                    const int32_t* seq_lens, void* stream);
+
+/*
+ * splitkv_read_items -- synchronises `stream` and copies the work list held in
+ * `workspace` (splitkv_plan_num_items items, SPLITKV_ITEM_FIELDS int32 each,
+ * launch order) to items_host.  EINVAL if capacity (items) is too small.
+ */
+splitkv_status splitkv_read_items(const splitkv_plan_t* plan, const void* workspace,
+                                  int32_t* items_host, int32_t capacity, void* stream);
+
 /* Frees a plan (NULL is ignored). */
 void splitkv_plan_destroy(splitkv_plan_t* plan);
 

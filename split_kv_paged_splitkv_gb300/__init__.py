@@ -45,6 +45,9 @@ class SplitKVError(RuntimeError):
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
 _SIGNATURES = {
     "splitkv_plan": (_i32, [ctypes.POINTER(splitkv_desc_t), _vp, _i32, _i32, ctypes.POINTER(_vp)]),
+    "splitkv_plan_fixed": (_i32, [ctypes.POINTER(splitkv_desc_t), _i32, ctypes.POINTER(_vp)]),
+    "splitkv_plan_refresh": (_i32, [_vp, _vp, _vp, _vp]),
+    "splitkv_read_items": (_i32, [_vp, _vp, _vp, _i32, _vp]),
     "splitkv_plan_destroy": (None, [_vp]),
     "splitkv_plan_get_items": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32)]),
     "splitkv_plan_num_items": (_i32, [_vp]),
@@ -146,6 +149,25 @@ def splitkv_plan(desc: splitkv_desc_t, seq_lens_host, num_splits: int = 0, num_s
     h = _vp()
     _check(_lib.splitkv_plan(ctypes.byref(desc), lens.ctypes.data, num_splits, num_sms, ctypes.byref(h)))
     return Plan(h.value, desc, num_splits)
+
+
+def splitkv_plan_fixed(desc: splitkv_desc_t, num_splits: int) -> Plan:
+    """Capacity plan whose work list splitkv_plan_refresh rewrites on the device."""
+    h = _vp()
+    _check(_lib.splitkv_plan_fixed(ctypes.byref(desc), num_splits, ctypes.byref(h)))
+    return Plan(h.value, desc, num_splits)
+
+
+def splitkv_plan_refresh(plan: Plan, workspace, seq_lens, stream=None):
+    _check(_lib.splitkv_plan_refresh(plan.handle, _ptr(workspace), _ptr(seq_lens), _stream(stream)))
+
+
+def splitkv_read_items(plan: Plan, workspace, stream=None) -> np.ndarray:
+    """The work list currently in `workspace` (synchronises the stream)."""
+    n = plan.num_items
+    out = np.zeros((n, SPLITKV_ITEM_FIELDS), dtype=np.int32)
+    _check(_lib.splitkv_read_items(plan.handle, _ptr(workspace), out.ctypes.data, n, _stream(stream)))
+    return out
 
 
 def splitkv_plan_get_items(plan: Plan) -> np.ndarray:

@@ -12,7 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsplitkv.so")
-SOURCES = ["plan.cpp", "api.cu", "gqa_decode.cu", "mla_decode.cu", "combine.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "api.cu", "gqa_decode.cu", "mla_decode.cu", "combine.cu", "noalloc.cu",
+           "refresh.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -232,6 +232,54 @@ splitkv_status splitkv_plan(const splitkv_desc_t* desc, const int32_t* seq_lens_
   return SPLITKV_OK;
 }
 
+splitkv_status splitkv_plan_fixed(const splitkv_desc_t* desc, int32_t num_splits,
+                                  splitkv_plan_t** plan_out) {
+  if (!plan_out) return fail(SPLITKV_EINVAL, "plan_out is NULL");
+  *plan_out = nullptr;
+  splitkv_status st = validate_desc(desc);
+  if (st != SPLITKV_OK) return st;
+  if (num_splits < 1 || num_splits > kMaxSplits)
+    return fail(SPLITKV_EINVAL, "num_splits (%d) must be in [1, %d] for a fixed plan", num_splits,
+                kMaxSplits);
+  const int64_t items = int64_t(desc->batch) * (desc->num_kv_heads / heads_per_item(*desc)) * num_splits;
+  if (items * ctas_per_item(*desc) > (int64_t(1) << 31) - 1)
+    return fail(SPLITKV_EINVAL, "too many work items (%lld)", (long long)items);
+  splitkv_plan_s* p = new (std::nothrow) splitkv_plan_s();
+  if (!p) return fail(SPLITKV_EINVAL, "out of host memory");
+  p->desc = *desc;
+  p->num_splits = num_splits;
+  p->fixed = true;
+  build_fixed_plan(p);
+  *plan_out = p;
+  return SPLITKV_OK;
+}
+
+splitkv_status splitkv_plan_refresh(const splitkv_plan_t* plan, void* workspace,
+                                    const int32_t* seq_lens, void* stream) {
+  if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
+  if (!plan->fixed) return fail(SPLITKV_EINVAL, "plan was not made by splitkv_plan_fixed");
+  if (!workspace) return fail(SPLITKV_EWORKSPACE, "workspace is NULL");
+  if (!seq_lens) return fail(SPLITKV_EINVAL, "seq_lens is NULL");
+  if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(SPLITKV_EINVAL, "workspace must be 16-byte and seq_lens 4-byte aligned");
+  cudaError_t e = launch_refresh(*plan, workspace, seq_lens, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the plan refresh kernel");
+  return SPLITKV_OK;
+}
+
+splitkv_status splitkv_read_items(const splitkv_plan_t* plan, const void* workspace,
+                                  int32_t* items_host, int32_t capacity, void* stream) {
+  if (!plan || !workspace || !items_host) return fail(SPLITKV_EINVAL, "NULL argument");
+  if (capacity < plan->n_items)
+    return fail(SPLITKV_EINVAL, "capacity %d < %d items", capacity, plan->n_items);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(items_host, static_cast<const unsigned char*>(workspace) + plan->off_items,
+                                  plan->items.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the work list");
+  return SPLITKV_OK;
+}
+
 void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
 
 int32_t splitkv_plan_num_items(const splitkv_plan_t* plan) { return plan ? plan->n_items : 0; }
@@ -346,6 +394,7 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   a.o_scale = fp8 && !per_head ? kv_scale : 1.f;
   a.k_scale = k_scale;  // per-head factors, applied by the kernel per KV head
   a.v_scale = v_scale;
+  a.fixed = plan->fixed ? 1 : 0;
   a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;

@@ -35,12 +35,15 @@ constexpr int kPerWay = 16;
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part,
     const int32_t* __restrict__ groups, int n_parts, int rows, int dv, int T, int Hq, int G,
-    void* out_bf16, float* out_f32, float* lse_out, int pdl) {
+    void* out_bf16, float* out_f32, float* lse_out, int pdl, int fixed) {
   __shared__ float4 red[kCombineThreads];
   __shared__ float red_w[kCombineThreads], red_m[kCombineThreads];
   launch_dependents();
-  // The group table is uploaded with the plan and never written by a kernel:
-  // it is read before waiting for the split kernel, off the critical path.
+  // The group table of a host plan is uploaded with the plan and never
+  // written by a kernel: it is read before waiting for the split kernel, off
+  // the critical path.  A capacity plan's table is written by the refresh
+  // kernel, and a group with S = 0 has nothing to merge.
+  if (fixed && pdl) wait_prerequisites();
   const int n = blockIdx.y;
   int S = n_parts, slot0 = 0;
   size_t orow = n;
@@ -53,6 +56,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const int hs = n / (T * G), r = n - hs * (T * G);
     const int t = r / G, gg = r - t * G;
     orow = (size_t(b) * T + t) * Hq + size_t(hkv + hs) * G + gg;
+    if (S == 0) return;
   }
   if (pdl) wait_prerequisites();
   const int tid = threadIdx.x, dl = tid & 31, way = tid >> 5;
@@ -147,7 +151,8 @@ cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream) {
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(a.o_part),
                             static_cast<const float*>(a.lse_part), a.groups, 0, a.rows, a.dv, a.T,
-                            a.Hq, a.G, a.out, static_cast<float*>(nullptr), a.lse, pdl ? 1 : 0);
+                            a.Hq, a.G, a.out, static_cast<float*>(nullptr), a.lse, pdl ? 1 : 0,
+                            a.fixed);
 }
 
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
@@ -156,7 +161,7 @@ cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n
   if (rows == 0) return cudaSuccess;
   dim3 grid(1, rows, (dv + 127) / 128), block(kCombineThreads, 1, 1);
   combine_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
-      o_part, lse_part, nullptr, n_parts, rows, dv, 1, 1, 1, out_bf16, out_f32, lse_out, 0);
+      o_part, lse_part, nullptr, n_parts, rows, dv, 1, 1, 1, out_bf16, out_f32, lse_out, 0, 0);
   return cudaGetLastError();
 }
 

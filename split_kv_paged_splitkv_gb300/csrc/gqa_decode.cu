@@ -264,11 +264,22 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG>::THREADS, kGqaCtasPerSm)
   int* pt = misc + 16;                                 // staged block-table entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.fixed) wait_prerequisites();  // the work list was written by the refresh kernel
   const int32_t* it = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
   const int b = it[SPLITKV_ITEM_B], h0 = it[SPLITKV_ITEM_HKV];  // heads h0 .. h0+HPI-1
   const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
   const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
   const int slot = it[SPLITKV_ITEM_SLOT], group = it[SPLITKV_ITEM_GROUP];
+  if (nsplit == 0) {  // a capacity item the current sequence lengths leave unused
+    if (threadIdx.x == 0) {
+      int32_t* lg = a.cta_log + size_t(blockIdx.x) * kLogFields;
+      lg[0] = p0;
+      lg[1] = p1;
+      lg[2] = 0;
+      lg[3] = 0;
+    }
+    return;
+  }
 
   // Prologue: only shared memory, the tensor maps and the uploaded work list,
   // so it may overlap the previous kernel on the stream (programmatic

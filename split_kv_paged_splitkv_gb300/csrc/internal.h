@@ -46,6 +46,7 @@ int ctas_per_sm(const splitkv_desc_t& d);
 struct splitkv_plan_s {
   splitkv_desc_t desc;
   int32_t num_splits = 0;  // as requested (0 = planner's choice)
+  bool fixed = false;      // capacity plan whose work list a kernel rewrites (splitkv_plan_fixed)
   int32_t num_sms = 0;
   std::vector<int32_t> seq_lens;
   std::vector<int32_t> items;   // n_items * SPLITKV_ITEM_FIELDS, launch order
@@ -62,6 +63,11 @@ namespace splitkv {
 // Planner (plan.cpp, host only).  Fills items/groups/offsets of `p` from
 // p->desc, p->seq_lens, p->num_splits, p->num_sms.
 void build_plan(splitkv_plan_s* p);
+
+// Capacity plan (plan.cpp): items (b, head group, s) for every s < num_splits,
+// all marked unused (NSPLIT = 0) until splitkv_plan_refresh rewrites them on
+// the device; one combine group per (b, head group) when num_splits > 1.
+void build_fixed_plan(splitkv_plan_s* p);
 
 // Thread-local error text (api.cu).
 splitkv_status fail(splitkv_status s, const char* fmt, ...);
@@ -86,11 +92,13 @@ struct DecodeArgs {
   int32_t batch, T, Hq, Hkv, G, P, max_pages, num_pages, rows, dv;
   float qk_scale_log2;  // scale * kv_scale (FP8 only) * log2(e)
   float o_scale;        // factor applied to the normalised output (FP8: kv_scale)
-  const float* k_scale;  // e4m3 per-KV-head scales [Hkv] (device) or null: the
-  const float* v_scale;  //   kernel multiplies qk_scale_log2 / o_scale by them
   int32_t fused;        // 1: last CTA of a group merges
   int32_t kv_box3d;     // bf16 K/V maps are 3-D: one [2][16][64] box per 16-key tile
   int32_t hpi;          // KV heads per item (e4m3 boxes are [hpi][16][128])
+  const float* k_scale;  // e4m3 per-KV-head scales [Hkv] (device) or null: the
+  const float* v_scale;  //   kernel multiplies qk_scale_log2 / o_scale by them
+  int32_t fixed;         // 1: the work list was written by a kernel (read it after the
+                         //    dependency wait); items with NSPLIT = 0 are unused
 };
 
 // Raw 128-byte tensor map storage (CUtensorMap), built by the API layer.
@@ -102,6 +110,8 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
                        void* stream);
 cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, void* stream);
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
+cudaError_t launch_refresh(const splitkv_plan_s& p, void* workspace, const int32_t* seq_lens,
+                           void* stream);
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
                                int dv, void* out_bf16, float* out_f32, float* lse_out,
                                void* stream);

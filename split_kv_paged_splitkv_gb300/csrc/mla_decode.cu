@@ -112,10 +112,21 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
   const int item = pair / a.T;
   const int t = pair - item * a.T;
 
+  if (a.fixed) wait_prerequisites();  // the work list was written by the refresh kernel
   const int32_t* it = a.items + size_t(item) * SPLITKV_ITEM_FIELDS;
   const int b = it[SPLITKV_ITEM_B];
   const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
   const int slot = it[SPLITKV_ITEM_SLOT];
+  if (it[SPLITKV_ITEM_NSPLIT] == 0) {  // a capacity item the current lengths leave unused
+    if (threadIdx.x == 0) {
+      int32_t* lg = a.cta_log + size_t(blockIdx.x) * kLogFields;
+      lg[0] = p0;
+      lg[1] = p1;
+      lg[2] = 0;
+      lg[3] = 0;
+    }
+    return;
+  }
 
   // ---- prologue (shared memory, TMEM, tensor map, work list only)
   if (threadIdx.x == 0) {

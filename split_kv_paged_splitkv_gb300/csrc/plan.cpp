@@ -109,6 +109,44 @@ std::vector<int32_t> choose_splits(const std::vector<int32_t>& n_pages, int unit
   return best_S;
 }
 
+// Workspace layout of a plan, and the host image of its uploaded part.
+void layout_workspace(splitkv_plan_s* p) {
+  const splitkv_desc_t& d = p->desc;
+  const int B = d.batch;
+  p->rows = rows_per_item(d);
+  p->n_ctas = p->n_items * ctas_per_item(d);
+  // Everything before off_log is uploaded from the host.
+  size_t off = 0;
+  p->off_status = off;
+  off = align_up(off + sizeof(int32_t));
+  p->off_items = off;
+  off = align_up(off + p->items.size() * sizeof(int32_t));
+  p->off_groups = off;
+  off = align_up(off + p->groups.size() * sizeof(int32_t));
+  p->off_seqlens = off;
+  off = align_up(off + size_t(B) * sizeof(int32_t));
+  p->off_tickets = off;  // group tickets, then one bundle ticket per slot
+  off = align_up(off + size_t(p->n_groups + p->n_slots) * sizeof(int32_t));
+  p->upload_bytes = off;
+  p->off_log = off;
+  off = align_up(off + size_t(p->n_ctas) * kLogFields * sizeof(int32_t));
+  p->off_lse = off;
+  off = align_up(off + size_t(p->n_slots) * p->rows * sizeof(float));
+  p->off_o = off;
+  off = align_up(off + size_t(p->n_slots) * p->rows * d.v_dim * sizeof(float));
+  p->total = off;
+
+  p->upload.assign(p->upload_bytes, 0);
+  auto put = [&](size_t at, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::copy(reinterpret_cast<const unsigned char*>(v.data()),
+                              reinterpret_cast<const unsigned char*>(v.data() + v.size()),
+                              p->upload.begin() + at);
+  };
+  put(p->off_items, p->items);
+  put(p->off_groups, p->groups);
+  put(p->off_seqlens, p->seq_lens);
+}
+
 }  // namespace
 
 void build_plan(splitkv_plan_s* p) {
@@ -175,39 +213,29 @@ void build_plan(splitkv_plan_s* p) {
   for (size_t i = 0; i < items.size(); ++i)
     std::copy(items[i].f, items[i].f + SPLITKV_ITEM_FIELDS, p->items.begin() + i * SPLITKV_ITEM_FIELDS);
 
-  p->rows = rows_per_item(d);
-  p->n_ctas = p->n_items * ctas_per_item(d);
+  layout_workspace(p);
+}
 
-  // Workspace layout; everything before off_log is uploaded from the host.
-  size_t off = 0;
-  p->off_status = off;
-  off = align_up(off + sizeof(int32_t));
-  p->off_items = off;
-  off = align_up(off + p->items.size() * sizeof(int32_t));
-  p->off_groups = off;
-  off = align_up(off + p->groups.size() * sizeof(int32_t));
-  p->off_seqlens = off;
-  off = align_up(off + size_t(B) * sizeof(int32_t));
-  p->off_tickets = off;  // group tickets, then one bundle ticket per slot
-  off = align_up(off + size_t(p->n_groups + p->n_slots) * sizeof(int32_t));
-  p->upload_bytes = off;
-  p->off_log = off;
-  off = align_up(off + size_t(p->n_ctas) * kLogFields * sizeof(int32_t));
-  p->off_lse = off;
-  off = align_up(off + size_t(p->n_slots) * p->rows * sizeof(float));
-  p->off_o = off;
-  off = align_up(off + size_t(p->n_slots) * p->rows * d.v_dim * sizeof(float));
-  p->total = off;
-
-  p->upload.assign(p->upload_bytes, 0);
-  auto put = [&](size_t at, const std::vector<int32_t>& v) {
-    if (!v.empty()) std::copy(reinterpret_cast<const unsigned char*>(v.data()),
-                              reinterpret_cast<const unsigned char*>(v.data() + v.size()),
-                              p->upload.begin() + at);
-  };
-  put(p->off_items, p->items);
-  put(p->off_groups, p->groups);
-  put(p->off_seqlens, p->seq_lens);
+void build_fixed_plan(splitkv_plan_s* p) {
+  const splitkv_desc_t& d = p->desc;
+  const int B = d.batch, hpi = heads_per_item(d), U = d.num_kv_heads / hpi, S = p->num_splits;
+  p->seq_lens.assign(B, 0);
+  p->n_items = B * U * S;
+  p->items.assign(size_t(p->n_items) * SPLITKV_ITEM_FIELDS, 0);
+  p->groups.clear();
+  for (int b = 0; b < B; ++b)
+    for (int u = 0; u < U; ++u) {
+      const int g = b * U + u;
+      for (int s = 0; s < S; ++s) {
+        int32_t* it = p->items.data() + size_t(g * S + s) * SPLITKV_ITEM_FIELDS;
+        const int32_t f[SPLITKV_ITEM_FIELDS] = {b, u * hpi, s, 0, 0, 0, -1, -1};
+        std::copy(f, f + SPLITKV_ITEM_FIELDS, it);
+      }
+      if (S > 1) p->groups.insert(p->groups.end(), {b, u * hpi, 0, g * S});
+    }
+  p->n_groups = static_cast<int32_t>(p->groups.size() / kGroupFields);
+  p->n_slots = S > 1 ? p->n_items : 0;
+  layout_workspace(p);
 }
 
 }  // namespace splitkv

@@ -8,7 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, make_desc, splitkv_decode,
-               splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_upload, splitkv_read_stats)
+               splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_fixed, splitkv_plan_refresh,
+               splitkv_plan_upload, splitkv_read_stats)
 
 
 class DecodeSession:
@@ -22,7 +23,8 @@ class DecodeSession:
 
     def __init__(self, q, k_pages, v_pages, block_table, seq_lens, seq_lens_host, *, scale,
                  kv_scale=1.0, num_splits=0, num_sms=0, v_dim=None, v_shares_k=False,
-                 combine_mode=SPLITKV_COMBINE_SEPARATE, stream=None, k_scale=None, v_scale=None):
+                 combine_mode=SPLITKV_COMBINE_SEPARATE, stream=None, k_scale=None, v_scale=None,
+                 fixed=False):
         B, T, Hq, Dk = q.shape
         N, Hkv, P, _ = k_pages.shape
         if v_dim is None:
@@ -31,7 +33,12 @@ class DecodeSession:
         self.desc = make_desc(B, T, Hq, Hkv, Dk, v_dim, P, block_table.shape[1], N,
                               SPLITKV_FP8_E4M3 if fp8 else SPLITKV_BF16, int(v_shares_k),
                               combine_mode)
-        self.plan = splitkv_plan(self.desc, seq_lens_host, num_splits, num_sms)
+        # fixed: a capacity plan (num_splits items per sequence and head group)
+        # whose work list run() rewrites on the device from the current
+        # seq_lens, so one captured CUDA graph serves any lengths
+        self.fixed = fixed
+        self.plan = (splitkv_plan_fixed(self.desc, num_splits) if fixed else
+                     splitkv_plan(self.desc, seq_lens_host, num_splits, num_sms))
         self.num_splits = num_splits
         dev = q.device
         self.workspace = torch.empty(max(self.plan.workspace_size, 256), dtype=torch.uint8, device=dev)
@@ -47,6 +54,8 @@ class DecodeSession:
         q, k, v, table, lens = tensors if tensors is not None else self.tensors
         o = self.out if out is None else out
         l = self.lse if lse is None else lse
+        if self.fixed:
+            splitkv_plan_refresh(self.plan, self.workspace, lens, self.stream)
         if self.k_scale is not None:
             splitkv_decode_kv_scales(self.plan, self.workspace, q, k, v, table, lens,
                                      self.num_splits, self.scale, self.k_scale, self.v_scale, o, l,

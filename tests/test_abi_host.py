@@ -190,6 +190,42 @@ def test_decode_kv_scales_validates_before_any_cuda_call():
         assert skv.splitkv_last_error()
 
 
+def test_fixed_plan_template_and_layout():
+    """A capacity plan holds num_splits items per (sequence, head group), in
+    (b, head group, s) order, all unused until the device refresh."""
+    for fp8, Hkv, want_hpi in ((False, 2, 1), (True, 8, 4)):
+        d = _desc(B=3, Hq=8 * Hkv, Hkv=Hkv, fp8=fp8, mode=skv.SPLITKV_COMBINE_SEPARATE)
+        plan = skv.splitkv_plan_fixed(d, 4)
+        assert skv.splitkv_plan_heads_per_item(plan) == want_hpi
+        U = Hkv // want_hpi
+        items = skv.splitkv_plan_get_items(plan)
+        assert items.shape == (3 * U * 4, 8)
+        b, u, s_ = np.meshgrid(np.arange(3), np.arange(U), np.arange(4), indexing="ij")
+        assert np.array_equal(items[:, 0], b.ravel())
+        assert np.array_equal(items[:, 1], u.ravel() * want_hpi)
+        assert np.array_equal(items[:, 2], s_.ravel())
+        assert (items[:, 3] == 0).all() and (items[:, 6] == -1).all() and (items[:, 7] == -1).all()
+        assert skv.splitkv_plan_launches_per_call(plan) == 2
+        assert skv.splitkv_workspace_size(plan) > 0
+    one = skv.splitkv_plan_fixed(_desc(mode=skv.SPLITKV_COMBINE_SEPARATE), 1)
+    assert skv.splitkv_plan_launches_per_call(one) == 1  # nothing to merge
+    for bad in (0, 65):
+        with pytest.raises(skv.SplitKVError):
+            skv.splitkv_plan_fixed(_desc(), bad)
+
+
+def test_refresh_and_read_items_validate_before_any_cuda_call():
+    A = 1 << 20
+    host_plan = skv.splitkv_plan(_desc(), np.array([100], np.int32), 2, 148)
+    fixed = skv.splitkv_plan_fixed(_desc(), 2)
+    assert skv._lib.splitkv_plan_refresh(host_plan.handle, A, A, None) == skv.SPLITKV_EINVAL
+    assert skv._lib.splitkv_plan_refresh(fixed.handle, A, None, None) == skv.SPLITKV_EINVAL
+    assert skv._lib.splitkv_plan_refresh(fixed.handle, None, A, None) == skv.SPLITKV_EWORKSPACE
+    assert skv._lib.splitkv_plan_refresh(fixed.handle, A, A + 2, None) == skv.SPLITKV_EINVAL
+    out = np.zeros((1, 8), np.int32)
+    assert skv._lib.splitkv_read_items(fixed.handle, A, out.ctypes.data, 1, None) == skv.SPLITKV_EINVAL
+
+
 def test_upload_checks_workspace_size():
     d = _desc()
     plan = skv.splitkv_plan(d, np.array([5900], np.int32), 8, 148)
