@@ -70,6 +70,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_ctx5900", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--splits", type=int, default=0, help="num_splits (0 = planner)")
+    ap.add_argument("--fixed", action="store_true",
+                    help="capacity plan refreshed on the device every step (needs --splits; "
+                         "the refresh kernel is inside the timed region)")
     ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -276,12 +279,15 @@ def run_ours(args, rank, world, local):
     mode = skv.SPLITKV_COMBINE_FUSED if args.combine == "fused" else skv.SPLITKV_COMBINE_SEPARATE
     # Everything runs on torch's current stream: graphs are captured on a side
     # stream by torch.cuda.graph and replayed on the current stream.
+    if args.fixed and args.splits < 1:
+        raise SystemExit("--fixed needs --splits >= 1")
     sess = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
                          scale=x.scale, kv_scale=x.kv_scale, num_splits=args.splits,
-                         v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode)
+                         v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode,
+                         fixed=args.fixed)
     items = skv.splitkv_plan_get_items(sess.plan)
     n_groups = len(np.unique(items[items[:, 3] > 1][:, 7])) if len(items) else 0
-    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan)
+    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan) + (1 if args.fixed else 0)
 
     # rotating KV pools: total > 4x L2
     props = torch.cuda.get_device_properties(dev)
@@ -384,6 +390,7 @@ def run_ours(args, rank, world, local):
                    "heads_q_kv": [w.num_q_heads, w.num_kv_heads], "head_dim": w.qk_dim,
                    "context": w.lens, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
                    "num_splits": args.splits, "planned_items": int(len(items)),
+                   "plan": "capacity plan, refreshed on the device each step" if args.fixed else "host",
                    "combine": args.combine, "parallelism": f"replicas{world}",
                    "l2": f"inputs rotate over {R} KV pools ({R * pool_bytes / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
                    "timing": "CUDA-graph replay of back-to-back calls, CUDA events on the launching stream"},
