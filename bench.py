@@ -58,7 +58,6 @@ NORTH_STAR_HBM_GBS = 8000.0
 # whenever that kernel changes after its capture.
 PROFILED_TRAFFIC = {
     "gqa_ctx5900": (6111488, "profiles/gqa_splitkv_kernel_gqa_ctx5900.md"),
-    "fp8_batch8_ctx32k": (253643008, "profiles/gqa_splitkv_kernel_fp8_batch8_ctx32k.md"),
 }
 
 

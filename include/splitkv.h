@@ -187,9 +187,9 @@ int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
  * CTA pair per query token and item for MLA): the rows of the per-CTA log. */
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan);
 
-/* KV heads one work item covers: 4, 2 or 1 (the largest dividing Hkv) for the
- * e4m3 GQA path with at most 8 query rows (T * G) per KV head, where one TMA
- * box then brings a 16-key tile of all of them; 1 otherwise.  Partial-result rows of an item are numbered
+/* KV heads one work item covers: 2 when Hkv is even for the e4m3 GQA path
+ * with at most 8 query rows (T * G) per KV head, where one TMA box then
+ * brings a 16-key tile of both; 1 otherwise.  Partial-result rows of an item are numbered
  * head_slot * T * G + t * G + g. */
 int32_t splitkv_plan_heads_per_item(const splitkv_plan_t* plan);
 

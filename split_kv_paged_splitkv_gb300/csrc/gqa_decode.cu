@@ -758,7 +758,6 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
   switch (a.hpi) {
     case 1: return launch_gqa_t<true, 1>(a, mk, mv, s);
     case 2: return launch_gqa_t<true, 2>(a, mk, mv, s);
-    case 4: return launch_gqa_t<true, 4>(a, mk, mv, s);
     default: return cudaErrorInvalidValue;
   }
 }

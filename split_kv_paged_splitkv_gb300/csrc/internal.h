@@ -26,8 +26,8 @@ enum class Family { kGqa, kMla, kNone };
 Family family_of(const splitkv_desc_t& d);
 
 // KV heads one work item covers (consecutive, from the item's h_kv): for the
-// e4m3 GQA path the largest of 4, 2, 1 dividing Hkv, so that one TMA box
-// brings a 16-key tile of all of them; otherwise 1.
+// e4m3 GQA path with at most 8 query rows per head, 2 when Hkv is even (one
+// TMA box brings a 16-key tile of both), else 1; otherwise 1.
 int heads_per_item(const splitkv_desc_t& d);
 
 // Query rows one work item produces: heads_per_item * T * G.

@@ -40,7 +40,7 @@ GQA_CTAS_PER_SM = 3
 def _expected_hpi(Hkv, fp8, rows_per_head=8):
     if not fp8 or rows_per_head > 8:
         return 1
-    return next(h for h in (4, 2, 1) if Hkv % h == 0)
+    return 2 if Hkv % 2 == 0 else 1
 
 
 def _oracle_items(lens, P, Hkv, S, sms, hpi=1):
@@ -164,7 +164,7 @@ def test_decode_validates_before_any_cuda_call():
 
 
 def test_heads_per_item_is_one_above_eight_rows_per_head():
-    for T, G, want in ((1, 8, 4), (2, 8, 1), (3, 4, 1), (2, 4, 4)):
+    for T, G, want in ((1, 8, 2), (2, 8, 1), (3, 4, 1), (2, 4, 2)):
         d = _desc(T=T, Hq=8 * G, Hkv=8, fp8=True)
         plan = skv.splitkv_plan(d, np.array([300], np.int32), 0, 148)
         assert skv.splitkv_plan_heads_per_item(plan) == _expected_hpi(8, True, T * G) == want
@@ -193,7 +193,7 @@ def test_decode_kv_scales_validates_before_any_cuda_call():
 def test_fixed_plan_template_and_layout():
     """A capacity plan holds num_splits items per (sequence, head group), in
     (b, head group, s) order, all unused until the device refresh."""
-    for fp8, Hkv, want_hpi in ((False, 2, 1), (True, 8, 4)):
+    for fp8, Hkv, want_hpi in ((False, 2, 1), (True, 8, 2)):
         d = _desc(B=3, Hq=8 * Hkv, Hkv=Hkv, fp8=fp8, mode=skv.SPLITKV_COMBINE_SEPARATE)
         plan = skv.splitkv_plan_fixed(d, 4)
         assert skv.splitkv_plan_heads_per_item(plan) == want_hpi
