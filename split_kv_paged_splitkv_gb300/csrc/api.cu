@@ -396,6 +396,7 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   a.v_scale = v_scale;
   a.fixed = plan->fixed ? 1 : 0;
   a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
+  a.deep_ring = plan->n_items <= plan->num_sms ? 1 : 0;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
   if (family_of(d) == Family::kMla) {

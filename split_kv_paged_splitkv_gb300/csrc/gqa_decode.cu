@@ -47,8 +47,10 @@ using namespace ptx;
 // worth of TMA boxes in flight however deep its ring is, and small boxes
 // stream more slowly than large ones, so per-SM bandwidth comes from several
 // CTAs per SM (a two-stage ring and 160 threads let three CTAs share an SM)
-// and from boxes that span several heads (HPI > 1, e4m3 only).
-template <bool FP8, int HPI, int NRG = 1>
+// and from boxes that span several heads (HPI > 1, e4m3 only).  A grid of at
+// most one CTA per SM cannot share SMs; its CTAs take a four-stage ring
+// instead (128 KB, a whole item of a few thousand keys in flight at once).
+template <bool FP8, int HPI, int NRG = 1, int NST_ = 2>
 struct Gqa {
   static_assert(HPI == 1 || (FP8 && (HPI == 2 || HPI == 4)), "heads per item");
   static_assert(NRG == 1 || (NRG == 2 && HPI == 1), "row groups per head");
@@ -58,7 +60,7 @@ struct Gqa {
   static constexpr int TILE = 2 * HPI * KT_BYTES;          // K + V boxes of one tile
   static constexpr int STAGE = 32768;
   static constexpr int TPS = STAGE / TILE;                 // tiles per stage
-  static constexpr int NST = 2;                            // stages in the ring
+  static constexpr int NST = NST_;                         // stages in the ring
   static constexpr int NCW = 4;                            // consumer warps
   // A slot is (head slot hs, row group rg) = (slot % HPI, slot / HPI): the
   // warps of a slot score query rows [8 rg, 8 rg + 8) of KV head h0 + hs.
@@ -250,11 +252,11 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
   if (d0 == 0 && a.lse) a.lse[row] = lse_n;
 }
 
-template <bool FP8, int HPI, int NRG>
-__global__ void __launch_bounds__(Gqa<FP8, HPI, NRG>::THREADS, kGqaCtasPerSm)
+template <bool FP8, int HPI, int NRG, int NST>
+__global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerSm)
     gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
-  using C = Gqa<FP8, HPI, NRG>;
+  using C = Gqa<FP8, HPI, NRG, NST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -721,13 +723,13 @@ namespace {
 // programmatic dependent launch: the kernel's prologue may overlap the tail
 // of the previous kernel on the stream; it waits (griddepcontrol.wait)
 // before touching anything that kernel could have written.
-template <bool FP8, int HPI, int NRG = 1>
+template <bool FP8, int HPI, int NRG = 1, int NST = 2>
 cudaError_t launch_gqa_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                          cudaStream_t s) {
-  using C = Gqa<FP8, HPI, NRG>;
+  using C = Gqa<FP8, HPI, NRG, NST>;
   // The shared-memory opt-in is a per-process attribute: set it on first use only.
   static cudaError_t attr = cudaFuncSetAttribute(
-      gqa_splitkv_kernel<FP8, HPI, NRG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      gqa_splitkv_kernel<FP8, HPI, NRG, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_items, 1, 1);
@@ -739,7 +741,27 @@ cudaError_t launch_gqa_t(const DecodeArgs& a, const CUtensorMap& mk, const CUten
   la[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = la;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<FP8, HPI, NRG>, a, mk, mv);
+  return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<FP8, HPI, NRG, NST>, a, mk, mv);
+}
+
+constexpr int kDeepStages = 4;
+
+// Picks the instantiation for the query rows per KV head, the cache type and
+// the KV heads per item.
+template <int NST>
+cudaError_t launch_gqa_nst(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                           bool fp8, cudaStream_t s) {
+  if (a.T * a.G > 8) {  // 9..16 query rows per KV head: two row groups
+    if (a.hpi != 1) return cudaErrorInvalidValue;
+    return fp8 ? launch_gqa_t<true, 1, 2, NST>(a, mk, mv, s)
+               : launch_gqa_t<false, 1, 2, NST>(a, mk, mv, s);
+  }
+  if (!fp8) return a.hpi == 1 ? launch_gqa_t<false, 1, 1, NST>(a, mk, mv, s) : cudaErrorInvalidValue;
+  switch (a.hpi) {
+    case 1: return launch_gqa_t<true, 1, 1, NST>(a, mk, mv, s);
+    case 2: return launch_gqa_t<true, 2, 1, NST>(a, mk, mv, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -750,16 +772,11 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
   const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(&tv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.n_items == 0) return cudaSuccess;
-  if (a.T * a.G > 8) {  // 9..16 query rows per KV head: two row groups
-    if (a.hpi != 1) return cudaErrorInvalidValue;
-    return fp8 ? launch_gqa_t<true, 1, 2>(a, mk, mv, s) : launch_gqa_t<false, 1, 2>(a, mk, mv, s);
-  }
-  if (!fp8) return a.hpi == 1 ? launch_gqa_t<false, 1>(a, mk, mv, s) : cudaErrorInvalidValue;
-  switch (a.hpi) {
-    case 1: return launch_gqa_t<true, 1>(a, mk, mv, s);
-    case 2: return launch_gqa_t<true, 2>(a, mk, mv, s);
-    default: return cudaErrorInvalidValue;
-  }
+  // A grid of at most one CTA per SM does not share SMs, so its CTAs take the
+  // four-stage ring (more bytes in flight per SM); a larger grid keeps the
+  // two-stage ring that lets kGqaCtasPerSm CTAs share each SM.
+  if (a.deep_ring) return launch_gqa_nst<kDeepStages>(a, mk, mv, fp8, s);
+  return launch_gqa_nst<2>(a, mk, mv, fp8, s);
 }
 
 cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, bool box3d, const int32_t* table_row,

@@ -99,6 +99,8 @@ struct DecodeArgs {
   const float* v_scale;  //   kernel multiplies qk_scale_log2 / o_scale by them
   int32_t fixed;         // 1: the work list was written by a kernel (read it after the
                          //    dependency wait); items with NSPLIT = 0 are unused
+  int32_t deep_ring;     // 1: at most one CTA per SM, so the GQA kernel may take the
+                         //    deeper (four-stage) ring instead of sharing the SM
 };
 
 // Raw 128-byte tensor map storage (CUtensorMap), built by the API layer.

@@ -197,6 +197,26 @@ def test_sixteen_rows_per_head_long_context(fp8):
     assert status == 0 and (log[:, 2] > 0).all()
 
 
+@pytest.mark.parametrize("T,G,Hkv,fp8", [(1, 8, 2, False), (2, 8, 2, False), (1, 8, 3, True),
+                                          (1, 8, 2, True), (2, 8, 2, True)])
+def test_both_ring_depths(T, G, Hkv, fp8):
+    """A grid of at most one CTA per SM runs the four-stage ring, a larger one
+    the two-stage ring; a plan for a 4-SM machine forces the latter.  Covers
+    each kernel instantiation: bf16 with one and two row groups, e4m3 with one
+    and two KV heads per item, e4m3 with two row groups."""
+    w = _custom([T + 1, 333, 1500, 16 * 7 + 3, 900], G=G, Hkv=Hkv, T=T, fp8=fp8, seed=T + G + Hkv)
+    x = workloads.make_inputs(w, device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for num_sms, S in ((0, 2), (4, 6)):
+        s = session(x, S, 1, num_sms=num_sms)
+        n_items = skv.splitkv_plan_get_items(s.plan).shape[0]
+        assert (n_items <= sms) if num_sms == 0 else (n_items > num_sms)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} Hkv={Hkv} num_sms={num_sms}")
+        assert s.stats()[1] == 0
+
+
 # ------------------------------------------------------------------ workloads 3 and 5
 
 def test_fp8_batch8_ctx32k_full():
