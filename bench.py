@@ -75,6 +75,8 @@ def parse():
                     help="capacity plan refreshed on the device every step (needs --splits; "
                          "the refresh kernel is inside the timed region)")
     ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
+    ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"],
+                    help="page layout of the KV pools: [N][Hkv][P][D] or [N][P][Hkv][D]")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -276,7 +278,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
-    x = workloads.make_inputs(w, device=dev)
+    x = workloads.make_inputs(w, device=dev, layout=args.layout.upper())
     mode = skv.SPLITKV_COMBINE_FUSED if args.combine == "fused" else skv.SPLITKV_COMBINE_SEPARATE
     # Everything runs on torch's current stream: graphs are captured on a side
     # stream by torch.cuda.graph and replayed on the current stream.
@@ -285,7 +287,8 @@ def run_ours(args, rank, world, local):
     sess = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
                          scale=x.scale, kv_scale=x.kv_scale, num_splits=args.splits,
                          v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode,
-                         fixed=args.fixed)
+                         fixed=args.fixed,
+                         kv_layout=skv.SPLITKV_LAYOUT_NHD if args.layout == "nhd" else skv.SPLITKV_LAYOUT_HND)
     items = skv.splitkv_plan_get_items(sess.plan)
     n_groups = len(np.unique(items[items[:, 3] > 1][:, 7])) if len(items) else 0
     launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan) + (1 if args.fixed else 0)
@@ -374,7 +377,11 @@ def run_ours(args, rank, world, local):
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac_of_8tbs": achieved / NOMINAL_HBM_GBS, "kernel": "gqa_splitkv_kernel"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic, traffic_src = PROFILED_TRAFFIC.get(w.name, (None, None))
+    # the captures ran the default configuration (planner splits, separate
+    # combine, host plan, HND pages); other configurations report no traffic
+    default_cfg = (args.splits == 0 and not args.fixed and args.combine == "separate"
+                   and args.layout == "hnd")
+    traffic, traffic_src = PROFILED_TRAFFIC.get(w.name, (None, None)) if default_cfg else (None, None)
     roof.update({"traffic": traffic, "traffic_source": traffic_src,
                  "duration_basis": "timed-region time per call (all launches of a step)",
                  "peak_kind": peak_kind, "algorithmic_bytes": nbytes})
@@ -390,6 +397,7 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "batch": w.batch, "q_tokens": w.q_tokens,
                    "heads_q_kv": [w.num_q_heads, w.num_kv_heads], "head_dim": w.qk_dim,
                    "context": w.lens, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+                   "kv_layout": args.layout.upper(),
                    "num_splits": args.splits, "planned_items": int(len(items)),
                    "plan": "capacity plan, refreshed on the device each step" if args.fixed else "host",
                    "combine": args.combine, "parallelism": f"replicas{world}",

@@ -10,8 +10,8 @@
  *     lse  = ln sum_j exp(s_j)                                  (fp32 output)
  *     out  = sum_j exp(s_j - lse) * V_j                        (bf16 output)
  *
- * where K_j / V_j are row j % P of page block_table[b][j / P] (HND layout),
- * dequantised as code * kv_scale when the cache is FP8-e4m3.  The KV range of
+ * where K_j / V_j are row j % P of page block_table[b][j / P] (HND or NHD
+ * layout, see splitkv_kv_layout), dequantised as code * kv_scale when the cache is FP8-e4m3.  The KV range of
  * each sequence is cut into num_splits page ranges, each handled by its own
  * CTA, and the per-split results are merged by their log-sum-exp.  This is the
  * split-KV scheme of "vLLM 0.30.0 FA4 SplitKV Bug: H100 Decode Can Be 48%
@@ -69,6 +69,18 @@ typedef enum splitkv_combine_mode {
   SPLITKV_COMBINE_SEPARATE = 1  /* a second kernel merges all partials          */
 } splitkv_combine_mode;
 
+/* Order of the dimensions inside the K and V page pools.  "Xqa decode
+ * kernels" (vLLM pull request #43232), section "Test Plan", runs its decode
+ * path with the cache layout set to HND; NHD is the other value of that
+ * setting.  Both hold the same rows; only the strides differ.  The MLA
+ * family has one KV head, where the two orders coincide. */
+typedef enum splitkv_kv_layout {
+  SPLITKV_LAYOUT_HND = 0,    /* pages[num_pages][Hkv][P][dim]: one head's page rows
+                                are contiguous                                 */
+  SPLITKV_LAYOUT_NHD = 1     /* pages[num_pages][P][Hkv][dim]: the heads of one
+                                key are contiguous                             */
+} splitkv_kv_layout;
+
 /* Shapes and element types of one decode-attention call (no pointers). */
 typedef struct splitkv_desc {
   int32_t batch;              /* B, >= 1                                        */
@@ -84,6 +96,7 @@ typedef struct splitkv_desc {
   int32_t kv_dtype;           /* splitkv_dtype; q and out are always bf16       */
   int32_t v_shares_k;         /* 1: V_j = first v_dim columns of K_j (MLA)      */
   int32_t combine_mode;       /* splitkv_combine_mode                           */
+  int32_t kv_layout;          /* splitkv_kv_layout of k_pages and v_pages       */
 } splitkv_desc_t;
 
 /* Opaque host object holding the split table of one set of sequence lengths. */
@@ -216,9 +229,9 @@ splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace,
  * splitkv_decode -- one split-KV decode-attention call.
  *
  *   q            bf16 [B][T][Hq][Dk]
- *   k_pages      [num_pages_total][Hkv][P][Dk] of bf16 or e4m3 codes
- *   v_pages      [num_pages_total][Hkv][P][Dv]; ignored (may be NULL) when
- *                v_shares_k
+ *   k_pages      [num_pages_total][Hkv][P][Dk] of bf16 or e4m3 codes (HND;
+ *                [num_pages_total][P][Hkv][Dk] with SPLITKV_LAYOUT_NHD)
+ *   v_pages      the same with Dv; ignored (may be NULL) when v_shares_k
  *   block_table  int32 [B][max_pages_per_seq] physical page ids; entries past
  *                ceil(L/P) are never read
  *   seq_lens     int32 [B] device copy of the lengths the plan was built from
@@ -329,8 +342,8 @@ enum {
  * through the block table into dst_host-shaped device memory `dst`
  * ([n_keys][row_bytes / element size] raw elements), using the same TMA
  * tensor-map loads and swizzled shared-memory reads as the decode kernel.
- * `pages` is k_pages or v_pages, `row_elems` its last dimension.  For
- * checking the paged gather bit for bit.
+ * `pages` is k_pages or v_pages in desc->kv_layout, `row_elems` its last
+ * dimension.  For checking the paged gather bit for bit.
  */
 splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* pages,
                                     int32_t row_elems, const int32_t* block_table,

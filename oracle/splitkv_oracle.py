@@ -35,8 +35,11 @@ Conventions (readings of points the pages leave open):
 * ``seq_lens[b]`` counts all visible keys including the current ``T`` query
   tokens; query token ``t`` sees keys ``0 .. L - T + t`` (bottom-right causal).
 * Query head ``h`` reads KV head ``h // G`` with ``G = Hq / Hkv``.
-* Pages are HND: ``pages[phys][h_kv][slot][dim]``; key ``j`` of sequence ``b``
-  lives in page ``block_table[b][j // P]``, slot ``j % P``.
+* Pages are HND, ``pages[phys][h_kv][slot][dim]``, or NHD,
+  ``pages[phys][slot][h_kv][dim]`` (``layout="NHD"``); key ``j`` of sequence
+  ``b`` lives in page ``block_table[b][j // P]``, slot ``j % P``.  ("Xqa decode
+  kernels", section "Test Plan", runs its decode path with the cache layout
+  set to HND; NHD is the other value of that setting.)
 * FP8 dequantisation is ``code_value * kv_scale`` for both K and V, or, with
   per-head scales, ``code_value * k_scale[h_kv]`` for K and
   ``code_value * v_scale[h_kv]`` for V.
@@ -97,19 +100,35 @@ def dequant(raw: np.ndarray, kv_dtype: str, kv_scale: float) -> np.ndarray:
 # Paged gather
 # --------------------------------------------------------------------------
 
+def page_size_of(pages: np.ndarray, layout: str = "HND") -> int:
+    """P: axis 2 of HND pages ``[N][Hkv][P][D]``, axis 1 of NHD ``[N][P][Hkv][D]``."""
+    return pages.shape[2] if layout == "HND" else pages.shape[1]
+
+
+def kv_heads_of(pages: np.ndarray, layout: str = "HND") -> int:
+    """Hkv: axis 1 of HND pages, axis 2 of NHD pages."""
+    return pages.shape[1] if layout == "HND" else pages.shape[2]
+
+
 def gather_keys(pages: np.ndarray, table_row: Sequence[int], n_keys: int,
-                head: int) -> np.ndarray:
+                head: int, layout: str = "HND") -> np.ndarray:
     """Raw rows ``0 .. n_keys-1`` of one KV head, read through the block table.
 
-    ``pages[phys][h_kv][slot][dim]`` (raw storage), ``table_row[j // P]`` gives
-    the physical page of key ``j``.  Returns ``[n_keys][dim]`` raw values.
+    ``pages[phys][h_kv][slot][dim]`` (HND) or ``pages[phys][slot][h_kv][dim]``
+    (NHD), raw storage; ``table_row[j // P]`` gives the physical page of key
+    ``j``.  Returns ``[n_keys][dim]`` raw values.
     """
-    P = pages.shape[2]
+    if layout not in ("HND", "NHD"):
+        raise ValueError(layout)
+    P = page_size_of(pages, layout)
     out = np.empty((n_keys, pages.shape[3]), dtype=pages.dtype)
-    for j in range(0, n_keys, P):
+    for j in range(0, n_keys, P):  # one page (slots 0 .. take-1) at a time
         phys = int(table_row[j // P])
         take = min(P, n_keys - j)
-        out[j:j + take] = pages[phys, head, :take, :]
+        if layout == "HND":
+            out[j:j + take] = pages[phys, head, :take, :]
+        else:
+            out[j:j + take] = pages[phys, :take, head, :]
     return out
 
 
@@ -131,11 +150,13 @@ def _softmax_attend(q_row: np.ndarray, K: np.ndarray, V: np.ndarray,
 
 def attention_direct(q, k_pages, v_pages, block_table, seq_lens, *, scale,
                      kv_dtype="bf16", kv_scale=1.0, v_dim=None,
-                     v_shares_k=False, rows=None, k_scale=None, v_scale=None):
+                     v_shares_k=False, rows=None, k_scale=None, v_scale=None,
+                     layout="HND"):
     """Decode attention by definition, in fp64.
 
     ``q``: bf16 bits ``[B][T][Hq][Dk]``; ``k_pages``/``v_pages``: raw pages
-    ``[N][Hkv][P][D]`` (bf16 bits or e4m3 codes); ``block_table`` ``[B][max]``;
+    ``[N][Hkv][P][D]`` (``layout`` HND) or ``[N][P][Hkv][D]`` (NHD), bf16 bits
+    or e4m3 codes; ``block_table`` ``[B][max]``;
     ``seq_lens`` ``[B]``.  ``rows``: optional list of ``(b, t, h)`` to compute
     (all rows otherwise).  ``k_scale`` / ``v_scale``: optional per-KV-head
     dequantisation scales of an e4m3 cache, used for K / V in place of
@@ -144,7 +165,7 @@ def attention_direct(q, k_pages, v_pages, block_table, seq_lens, *, scale,
     """
     q = np.asarray(q)
     B, T, Hq, Dk = q.shape
-    Hkv = k_pages.shape[1]
+    Hkv = kv_heads_of(k_pages, layout)
     G = Hq // Hkv
     if v_dim is None:
         v_dim = k_pages.shape[3] if v_shares_k else v_pages.shape[3]
@@ -161,12 +182,12 @@ def attention_direct(q, k_pages, v_pages, block_table, seq_lens, *, scale,
         if key not in cache:
             ks = kv_scale if k_scale is None else float(k_scale[hk])
             vs = kv_scale if v_scale is None else float(v_scale[hk])
-            Kr = gather_keys(k_pages, block_table[b], L, hk)
+            Kr = gather_keys(k_pages, block_table[b], L, hk, layout)
             K = dequant(Kr, kv_dtype, ks)
             if v_shares_k:
                 V = K[:, :v_dim]
             else:
-                V = dequant(gather_keys(v_pages, block_table[b], L, hk), kv_dtype, vs)
+                V = dequant(gather_keys(v_pages, block_table[b], L, hk, layout), kv_dtype, vs)
             cache = {key: (K, V)}  # one (b, h_kv) at a time keeps memory bounded
         K, V = cache[key]
         lim = L - T + t  # last visible key index for this query token
@@ -329,12 +350,12 @@ def combine(parts: Sequence[Tuple[np.ndarray, float]]) -> Tuple[np.ndarray, floa
 
 def attention_split_mode(q, k_pages, v_pages, block_table, seq_lens, *, scale,
                          num_splits, num_sms=148, kv_dtype="bf16", kv_scale=1.0,
-                         v_dim=None, v_shares_k=False):
+                         v_dim=None, v_shares_k=False, layout="HND"):
     """Planner + per-split partials + combine, in fp64, for every row."""
     q = np.asarray(q)
     B, T, Hq, Dk = q.shape
-    Hkv = k_pages.shape[1]
-    P = k_pages.shape[2]
+    Hkv = kv_heads_of(k_pages, layout)
+    P = page_size_of(k_pages, layout)
     G = Hq // Hkv
     if v_dim is None:
         v_dim = k_pages.shape[3] if v_shares_k else v_pages.shape[3]
@@ -346,9 +367,9 @@ def attention_split_mode(q, k_pages, v_pages, block_table, seq_lens, *, scale,
     lse = np.zeros((B, T, Hq))
     for (b, hk), splits in by_bh.items():
         L = int(seq_lens[b])
-        K = dequant(gather_keys(k_pages, block_table[b], L, hk), kv_dtype, kv_scale)
+        K = dequant(gather_keys(k_pages, block_table[b], L, hk, layout), kv_dtype, kv_scale)
         V = K[:, :v_dim] if v_shares_k else dequant(
-            gather_keys(v_pages, block_table[b], L, hk), kv_dtype, kv_scale)
+            gather_keys(v_pages, block_table[b], L, hk, layout), kv_dtype, kv_scale)
         splits.sort()
         for t in range(T):
             lim = L - T + t

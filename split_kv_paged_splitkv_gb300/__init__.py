@@ -25,6 +25,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "splitkv.h")
 SPLITKV_OK, SPLITKV_EINVAL, SPLITKV_EUNSUPPORTED, SPLITKV_ECUDA, SPLITKV_EWORKSPACE, SPLITKV_EDEVICE = range(6)
 SPLITKV_BF16, SPLITKV_FP8_E4M3 = 0, 1
 SPLITKV_COMBINE_FUSED, SPLITKV_COMBINE_SEPARATE = 0, 1
+SPLITKV_LAYOUT_HND, SPLITKV_LAYOUT_NHD = 0, 1
 SPLITKV_ITEM_FIELDS = 8
 SPLITKV_DEVERR_TIMEOUT, SPLITKV_DEVERR_SEQLEN, SPLITKV_DEVERR_PAGE = 1, 2, 4
 ITEM_FIELD_NAMES = ("b", "h_kv", "split", "num_splits", "page_begin", "page_end", "slot", "group")
@@ -33,7 +34,8 @@ ITEM_FIELD_NAMES = ("b", "h_kv", "split", "num_splits", "page_begin", "page_end"
 class splitkv_desc_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "q_tokens", "num_q_heads", "num_kv_heads", "qk_dim", "v_dim", "page_size",
-        "max_pages_per_seq", "num_pages_total", "kv_dtype", "v_shares_k", "combine_mode")]
+        "max_pages_per_seq", "num_pages_total", "kv_dtype", "v_shares_k", "combine_mode",
+        "kv_layout")]
 
 
 class SplitKVError(RuntimeError):
@@ -117,9 +119,10 @@ def _check(status: int):
 
 def make_desc(batch, q_tokens, num_q_heads, num_kv_heads, qk_dim, v_dim, page_size,
               max_pages_per_seq, num_pages_total, kv_dtype=SPLITKV_BF16, v_shares_k=0,
-              combine_mode=SPLITKV_COMBINE_SEPARATE) -> splitkv_desc_t:
+              combine_mode=SPLITKV_COMBINE_SEPARATE, kv_layout=SPLITKV_LAYOUT_HND) -> splitkv_desc_t:
     return splitkv_desc_t(batch, q_tokens, num_q_heads, num_kv_heads, qk_dim, v_dim, page_size,
-                          max_pages_per_seq, num_pages_total, kv_dtype, int(v_shares_k), combine_mode)
+                          max_pages_per_seq, num_pages_total, kv_dtype, int(v_shares_k), combine_mode,
+                          kv_layout)
 
 
 class Plan:

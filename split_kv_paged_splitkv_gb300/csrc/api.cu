@@ -32,70 +32,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over [rows][dim] K or V elements with 16-row boxes and the 128-byte
-// swizzle: bf16 boxes are 64 columns wide (two per 128-wide row), e4m3 boxes
-// 128 columns.
-splitkv_status make_kv_map_2d(TmaDesc* out, const void* base, bool fp8, int dim, int64_t rows) {
+// Tensor map over a GQA K or V page pool (rows of 128 elements) in either
+// layout, with coordinates that do not depend on the layout -- (dims, key in
+// page, [column half,] KV head, page) -- and the 128-byte swizzle:
+//   e4m3: 4-D (128 dims, key, head, page), boxes [hpi heads][16 keys][128];
+//   bf16: 5-D (64 dims, key, column half, head, page), boxes
+//         [2 halves][16 keys][64] (one 16-key tile of one head; a 128-byte
+//         swizzled row holds 64 bf16, so each key row is two 64-wide halves).
+// Only the strides tell the layouts apart (HND: key rows of a head adjacent;
+// NHD: the heads of a key adjacent); the shared-memory image of a box is the
+// same in both.
+splitkv_status make_gqa_map(TmaDesc* out, const void* base, bool fp8, int P, int Hkv,
+                            int num_pages, int hpi, bool nhd) {
   auto fn = encode_fn();
   if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const int elt = fp8 ? 1 : 2;
+  const cuuint64_t row = fp8 ? 128u : 256u;  // bytes of one 128-element row
+  const cuuint64_t key_stride = nhd ? row * Hkv : row;
+  const cuuint64_t head_stride = nhd ? row : row * P;
+  const cuuint64_t page_stride = row * P * Hkv;
   CUtensorMap m;
-  cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
-  cuuint64_t gstride[1] = {cuuint64_t(dim) * elt};
-  cuuint32_t box[2] = {cuuint32_t(fp8 ? 128 : 64), 16u};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                  const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (fp8) {
+    cuuint64_t gdim[4] = {128u, cuuint64_t(P), cuuint64_t(Hkv), cuuint64_t(num_pages)};
+    cuuint64_t gstride[3] = {key_stride, head_stride, page_stride};
+    cuuint32_t box[4] = {128u, 16u, cuuint32_t(hpi), 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), gdim, gstride, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t gdim[5] = {64u, cuuint64_t(P), 2u, cuuint64_t(Hkv), cuuint64_t(num_pages)};
+    cuuint64_t gstride[4] = {key_stride, 128u, head_stride, page_stride};
+    cuuint32_t box[5] = {64u, 16u, 2u, 1u, 1u};
+    cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), gdim, gstride, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "tensor map size");
-  std::memcpy(out, &m, sizeof(m));
-  return SPLITKV_OK;
-}
-
-// As make_kv_map_2d, but for bf16 rows of 128 first tries a 3-D view (64
-// columns, rows, 2 column halves; strides 256 B and 128 B) so that one box
-// brings a whole 16-key tile as [2 halves][16 rows][64] -- the same shared
-// memory layout as two 2-D boxes, in half the TMA transactions.  *box3d
-// reports which form was built.
-splitkv_status make_kv_map(TmaDesc* out, const void* base, bool fp8, int dim, int64_t rows,
-                           bool* box3d) {
-  *box3d = false;
-  auto fn = encode_fn();
-  if (fn && !fp8 && dim == 128) {
-    CUtensorMap m;
-    cuuint64_t gdim3[3] = {64u, cuuint64_t(rows), 2u};
-    cuuint64_t gstride3[2] = {256u, 128u};
-    cuuint32_t box3[3] = {64u, 16u, 2u};
-    cuuint32_t estr3[3] = {1u, 1u, 1u};
-    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim3, gstride3, box3,
-           estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
-      std::memcpy(out, &m, sizeof(m));
-      *box3d = true;
-      return SPLITKV_OK;
-    }
-  }
-  return make_kv_map_2d(out, base, fp8, dim, rows);
-}
-
-// 3-D map over e4m3 pages viewed as (dim, key in page, page * Hkv + head),
-// 128-byte swizzle, boxes of [hpi heads][16 keys][128]: one box brings a
-// 16-key tile of hpi consecutive KV heads of one page (2 KB per head).
-splitkv_status make_fp8_map(TmaDesc* out, const void* base, int dim, int P, int64_t page_heads,
-                            int hpi) {
-  auto fn = encode_fn();
-  if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  CUtensorMap m;
-  cuuint64_t gdim[3] = {cuuint64_t(dim), cuuint64_t(P), cuuint64_t(page_heads)};
-  cuuint64_t gstride[2] = {cuuint64_t(dim), cuuint64_t(dim) * P};
-  cuuint32_t box[3] = {128u, 16u, cuuint32_t(hpi)};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   std::memcpy(out, &m, sizeof(m));
   return SPLITKV_OK;
 }
@@ -140,6 +115,8 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
     return fail(SPLITKV_EINVAL, "v_shares_k needs v_dim <= qk_dim");
   if (d->combine_mode != SPLITKV_COMBINE_FUSED && d->combine_mode != SPLITKV_COMBINE_SEPARATE)
     return fail(SPLITKV_EINVAL, "unknown combine_mode %d", d->combine_mode);
+  if (d->kv_layout != SPLITKV_LAYOUT_HND && d->kv_layout != SPLITKV_LAYOUT_NHD)
+    return fail(SPLITKV_EINVAL, "unknown kv_layout %d", d->kv_layout);
   if (int64_t(d->num_pages_total) * d->num_kv_heads * d->page_size >= (int64_t(1) << 31))
     return fail(SPLITKV_EINVAL, "num_pages_total * num_kv_heads * page_size must be < 2^31");
   if (family_of(*d) == Family::kNone)
@@ -415,27 +392,12 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   }
   TmaDesc tk, tv;
   a.hpi = heads_per_item(d);
-  a.kv_box3d = 0;
-  if (fp8) {
-    const int64_t page_heads = int64_t(d.num_pages_total) * d.num_kv_heads;
-    splitkv_status st = make_fp8_map(&tk, k_pages, d.qk_dim, d.page_size, page_heads, a.hpi);
-    if (st != SPLITKV_OK) return st;
-    st = make_fp8_map(&tv, v_pages, d.v_dim, d.page_size, page_heads, a.hpi);
-    if (st != SPLITKV_OK) return st;
-  } else {
-    bool k3 = false, v3 = false;
-    splitkv_status st = make_kv_map(&tk, k_pages, fp8, d.qk_dim, rows_total, &k3);
-    if (st != SPLITKV_OK) return st;
-    st = make_kv_map(&tv, v_pages, fp8, d.v_dim, rows_total, &v3);
-    if (st != SPLITKV_OK) return st;
-    if (k3 != v3) {  // keep both maps in the same form
-      if (k3) st = make_kv_map_2d(&tk, k_pages, fp8, d.qk_dim, rows_total);
-      else st = make_kv_map_2d(&tv, v_pages, fp8, d.v_dim, rows_total);
-      if (st != SPLITKV_OK) return st;
-      k3 = v3 = false;
-    }
-    a.kv_box3d = k3 ? 1 : 0;
-  }
+  const bool nhd = d.kv_layout == SPLITKV_LAYOUT_NHD;
+  splitkv_status st =
+      make_gqa_map(&tk, k_pages, fp8, d.page_size, d.num_kv_heads, d.num_pages_total, a.hpi, nhd);
+  if (st != SPLITKV_OK) return st;
+  st = make_gqa_map(&tv, v_pages, fp8, d.page_size, d.num_kv_heads, d.num_pages_total, a.hpi, nhd);
+  if (st != SPLITKV_OK) return st;
 
   cudaError_t e = launch_gqa(a, tk, tv, fp8, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the split-KV kernel");
@@ -516,17 +478,12 @@ splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* page
     return fail(SPLITKV_EINVAL, "n_keys out of range");
   if (!aligned16(pages) || !aligned16(dst)) return fail(SPLITKV_EINVAL, "misaligned buffers");
   const bool fp8 = desc->kv_dtype == SPLITKV_FP8_E4M3;
-  const int64_t rows_total = int64_t(desc->num_pages_total) * desc->num_kv_heads * desc->page_size;
   TmaDesc t;
-  bool box3d = false;
-  if (fp8)
-    st = make_fp8_map(&t, pages, row_elems, desc->page_size,
-                      int64_t(desc->num_pages_total) * desc->num_kv_heads, 1);
-  else
-    st = make_kv_map(&t, pages, fp8, row_elems, rows_total, &box3d);
+  st = make_gqa_map(&t, pages, fp8, desc->page_size, desc->num_kv_heads, desc->num_pages_total, 1,
+                    desc->kv_layout == SPLITKV_LAYOUT_NHD);
   if (st != SPLITKV_OK) return st;
-  cudaError_t e = launch_debug_gather(t, fp8, box3d, block_table + size_t(b) * desc->max_pages_per_seq,
-                                      desc->num_kv_heads, h_kv, desc->page_size, n_keys, dst, stream);
+  cudaError_t e = launch_debug_gather(t, fp8, block_table + size_t(b) * desc->max_pages_per_seq,
+                                      h_kv, desc->page_size, n_keys, dst, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the gather kernel");
   return SPLITKV_OK;
 }

@@ -357,20 +357,15 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
         }
         const uint32_t dk = smem_u32(ring + st * C::STAGE + u * C::TILE);
         const uint32_t dv = dk + HPI * C::KT_BYTES;
-        if (FP8) {  // [HPI heads][16 rows][128] of the map (dim, key in page, page*Hkv + head)
-          tma_load_3d_warp(dk, &tk, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
-          tma_load_3d_warp(dv, &tv, bar, 0, key0 - page * a.P, ph * a.Hkv + h0);
-          continue;
-        }
-        const int row = (ph * a.Hkv + h0) * a.P + (key0 - page * a.P);
-        if (a.kv_box3d) {  // one [2 halves][16 rows][64] box per tile
-          tma_load_3d_warp(dk, &tk, bar, 0, row, 0);
-          tma_load_3d_warp(dv, &tv, bar, 0, row, 0);
-        } else {
-          tma_load_2d_warp(dk, &tk, bar, 0, row);
-          tma_load_2d_warp(dk + 2048, &tk, bar, 64, row);
-          tma_load_2d_warp(dv, &tv, bar, 0, row);
-          tma_load_2d_warp(dv + 2048, &tv, bar, 64, row);
+        // The maps' coordinates are (dims, key in page, [column half,] KV
+        // head, page) in either page layout; one box per operand and tile.
+        const int kp = key0 - page * a.P;
+        if (FP8) {  // [HPI heads][16 keys][128]
+          tma_load_4d_warp(dk, &tk, bar, 0, kp, h0, ph);
+          tma_load_4d_warp(dv, &tv, bar, 0, kp, h0, ph);
+        } else {    // [2 halves][16 keys][64]
+          tma_load_5d_warp(dk, &tk, bar, 0, kp, 0, h0, ph);
+          tma_load_5d_warp(dv, &tv, bar, 0, kp, 0, h0, ph);
         }
       }
     }
@@ -668,9 +663,9 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
 // kernel.  One CTA of 128 threads; tiles are loaded one at a time.
 template <bool FP8>
 __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant__ CUtensorMap tm,
-                                                           const int32_t* table_row, int Hkv,
-                                                           int h_kv, int P, int n_keys,
-                                                           uint8_t* dst, int32_t* status, int box3d) {
+                                                           const int32_t* table_row, int h_kv,
+                                                           int P, int n_keys, uint8_t* dst,
+                                                           int32_t* status) {
   constexpr int KT = Gqa<FP8, 1>::KT_BYTES;
   __shared__ __align__(1024) uint8_t tile[KT];
   __shared__ __align__(8) uint64_t bar;
@@ -684,16 +679,12 @@ __global__ void __launch_bounds__(128) gather_debug_kernel(const __grid_constant
     const int key0 = i * 16;
     if (threadIdx.x == 0) {
       const int ph = table_row[key0 / P];
-      const int row = (ph * Hkv + h_kv) * P + key0 % P;
       mbar_arrive_expect_tx(smem_u32(&bar), KT);
-      if (FP8) {  // the decode kernel's e4m3 map: (dim, key in page, page * Hkv + head)
-        tma_load_3d(smem_u32(tile), &tm, smem_u32(&bar), 0, key0 % P, ph * Hkv + h_kv);
-      } else if (box3d) {
-        tma_load_3d(smem_u32(tile), &tm, smem_u32(&bar), 0, row, 0);
-      } else {
-        tma_load_2d(smem_u32(tile), &tm, smem_u32(&bar), 0, row);
-        if (!FP8) tma_load_2d(smem_u32(tile) + 2048, &tm, smem_u32(&bar), 64, row);
-      }
+      // the decode kernel's maps: (dims, key in page, [column half,] head, page)
+      if (FP8)
+        tma_load_4d(smem_u32(tile), &tm, smem_u32(&bar), 0, key0 % P, h_kv, ph);
+      else
+        tma_load_5d(smem_u32(tile), &tm, smem_u32(&bar), 0, key0 % P, 0, h_kv, ph);
     }
     if (!__syncthreads_and(mbar_wait(smem_u32(&bar), i & 1))) {
       if (threadIdx.x == 0 && status) atomicOr(status, SPLITKV_DEVERR_TIMEOUT);
@@ -779,18 +770,17 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
   return launch_gqa_nst<2>(a, mk, mv, fp8, s);
 }
 
-cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, bool box3d, const int32_t* table_row,
-                                int32_t hkv, int32_t h_kv, int32_t P, int32_t n_keys, void* dst,
-                                void* stream) {
+cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, const int32_t* table_row,
+                                int32_t h_kv, int32_t P, int32_t n_keys, void* dst, void* stream) {
   const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(&t);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* status = nullptr;
   if (fp8)
-    gather_debug_kernel<true><<<1, 128, 0, s>>>(m, table_row, hkv, h_kv, P, n_keys,
-                                                static_cast<uint8_t*>(dst), status, 0);
+    gather_debug_kernel<true><<<1, 128, 0, s>>>(m, table_row, h_kv, P, n_keys,
+                                                static_cast<uint8_t*>(dst), status);
   else
-    gather_debug_kernel<false><<<1, 128, 0, s>>>(m, table_row, hkv, h_kv, P, n_keys,
-                                                 static_cast<uint8_t*>(dst), status, box3d ? 1 : 0);
+    gather_debug_kernel<false><<<1, 128, 0, s>>>(m, table_row, h_kv, P, n_keys,
+                                                 static_cast<uint8_t*>(dst), status);
   return cudaGetLastError();
 }
 

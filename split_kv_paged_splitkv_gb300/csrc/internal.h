@@ -93,7 +93,6 @@ struct DecodeArgs {
   float qk_scale_log2;  // scale * kv_scale (FP8 only) * log2(e)
   float o_scale;        // factor applied to the normalised output (FP8: kv_scale)
   int32_t fused;        // 1: last CTA of a group merges
-  int32_t kv_box3d;     // bf16 K/V maps are 3-D: one [2][16][64] box per 16-key tile
   int32_t hpi;          // KV heads per item (e4m3 boxes are [hpi][16][128])
   const float* k_scale;  // e4m3 per-KV-head scales [Hkv] (device) or null: the
   const float* v_scale;  //   kernel multiplies qk_scale_log2 / o_scale by them
@@ -117,8 +116,7 @@ cudaError_t launch_refresh(const splitkv_plan_s& p, void* workspace, const int32
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
                                int dv, void* out_bf16, float* out_f32, float* lse_out,
                                void* stream);
-cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, bool box3d, const int32_t* table_row,
-                                int32_t hkv, int32_t h_kv, int32_t P, int32_t n_keys, void* dst,
-                                void* stream);
+cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, const int32_t* table_row,
+                                int32_t h_kv, int32_t P, int32_t n_keys, void* dst, void* stream);
 
 }  // namespace splitkv

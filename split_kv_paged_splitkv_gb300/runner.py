@@ -7,7 +7,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, make_desc, splitkv_decode,
+from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, SPLITKV_LAYOUT_HND,
+               SPLITKV_LAYOUT_NHD, make_desc, splitkv_decode,
                splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_fixed, splitkv_plan_refresh,
                splitkv_plan_upload, splitkv_read_stats)
 
@@ -16,7 +17,8 @@ class DecodeSession:
     """Holds a plan and its uploaded workspace for one set of KV-cache tensors.
 
     ``q`` bf16 [B][T][Hq][Dk]; ``k_pages`` bf16 or uint8 (e4m3 codes)
-    [N][Hkv][P][Dk]; ``v_pages`` likewise or None with ``v_shares_k``;
+    [N][Hkv][P][Dk] (``kv_layout`` HND) or [N][P][Hkv][Dk] (NHD); ``v_pages``
+    likewise or None with ``v_shares_k``;
     ``block_table`` int32 [B][max_pages]; ``seq_lens`` int32 [B] on the device
     and ``seq_lens_host`` the same values on the host.
     """
@@ -24,15 +26,18 @@ class DecodeSession:
     def __init__(self, q, k_pages, v_pages, block_table, seq_lens, seq_lens_host, *, scale,
                  kv_scale=1.0, num_splits=0, num_sms=0, v_dim=None, v_shares_k=False,
                  combine_mode=SPLITKV_COMBINE_SEPARATE, stream=None, k_scale=None, v_scale=None,
-                 fixed=False):
+                 fixed=False, kv_layout=SPLITKV_LAYOUT_HND):
         B, T, Hq, Dk = q.shape
-        N, Hkv, P, _ = k_pages.shape
+        if kv_layout == SPLITKV_LAYOUT_NHD:
+            N, P, Hkv, _ = k_pages.shape
+        else:
+            N, Hkv, P, _ = k_pages.shape
         if v_dim is None:
             v_dim = Dk if v_pages is None else v_pages.shape[3]
         fp8 = k_pages.dtype == torch.uint8
         self.desc = make_desc(B, T, Hq, Hkv, Dk, v_dim, P, block_table.shape[1], N,
                               SPLITKV_FP8_E4M3 if fp8 else SPLITKV_BF16, int(v_shares_k),
-                              combine_mode)
+                              combine_mode, kv_layout)
         # fixed: a capacity plan (num_splits items per sequence and head group)
         # whose work list run() rewrites on the device from the current
         # seq_lens, so one captured CUDA graph serves any lengths

@@ -3,6 +3,7 @@ import numpy as np
 import torch
 
 import oracle
+import split_kv_paged_splitkv_gb300 as skv
 import workloads
 from split_kv_paged_splitkv_gb300.runner import DecodeSession
 
@@ -20,14 +21,16 @@ def oracle_direct(x: workloads.Inputs, rows=None):
         workloads.bits(x.q), workloads.bits(x.k_pages),
         None if x.v_pages is None else workloads.bits(x.v_pages),
         x.block_table.cpu().numpy(), x.seq_lens_host, scale=x.scale, kv_dtype=w.kv_dtype,
-        kv_scale=x.kv_scale, v_dim=w.v_dim, v_shares_k=w.v_shares_k, rows=rows)
+        kv_scale=x.kv_scale, v_dim=w.v_dim, v_shares_k=w.v_shares_k, rows=rows,
+        layout=x.layout)
 
 
 def session(x: workloads.Inputs, num_splits=0, combine_mode=1, num_sms=0):
     return DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
                          scale=x.scale, kv_scale=x.kv_scale, num_splits=num_splits,
                          num_sms=num_sms, v_dim=x.w.v_dim, v_shares_k=x.w.v_shares_k,
-                         combine_mode=combine_mode)
+                         combine_mode=combine_mode,
+                         kv_layout=skv.SPLITKV_LAYOUT_NHD if x.layout == "NHD" else skv.SPLITKV_LAYOUT_HND)
 
 
 def compare(out, lse, ref_o, ref_l, rows=None, what=""):

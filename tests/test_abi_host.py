@@ -129,6 +129,23 @@ def test_plan_rejects_bad_descriptors(bad, code):
     assert e.value.status == code
 
 
+def test_kv_layout_field():
+    """Both page layouts plan alike (the split table does not depend on the
+    layout); any other value is rejected."""
+    lens = np.array([700, 33], np.int32)
+    items = []
+    for layout in (skv.SPLITKV_LAYOUT_HND, skv.SPLITKV_LAYOUT_NHD):
+        d = _desc(B=2)
+        d.kv_layout = layout
+        items.append(skv.splitkv_plan_get_items(skv.splitkv_plan(d, lens, 3, 148)))
+    assert np.array_equal(items[0], items[1])
+    d = _desc(B=2)
+    d.kv_layout = 2
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(d, lens, 3, 148)
+    assert e.value.status == skv.SPLITKV_EINVAL
+
+
 def test_plan_rejects_bad_lengths_and_splits():
     d = _desc(maxp=4)
     for lens, S in (([65], 1), ([-1], 1), ([10], 65), ([10], -1)):

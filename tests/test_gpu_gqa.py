@@ -32,19 +32,23 @@ def _custom(lens, G=8, Hkv=2, T=1, P=16, fp8=False, seed=7):
 
 @pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("P", [16, 64])
-def test_paged_gather_is_bit_exact(fp8, P):
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_paged_gather_is_bit_exact(fp8, P, layout):
     w = _custom([16 * 7 + 5, 3 * P + 1], P=P, fp8=fp8)
-    x = workloads.make_inputs(w, device="cuda")
+    x = workloads.make_inputs(w, device="cuda", layout=layout)
+    kv_layout = skv.SPLITKV_LAYOUT_NHD if layout == "NHD" else skv.SPLITKV_LAYOUT_HND
     for b in range(2):
         L = int(x.seq_lens_host[b])
         for h in range(w.num_kv_heads):
             for which, pages in (("k", x.k_pages), ("v", x.v_pages)):
                 dst = torch.zeros((L, 128), dtype=pages.dtype, device="cuda")
                 skv.splitkv_debug_gather(skv.make_desc(2, 1, 16, 2, 128, 128, P, x.max_pages,
-                                                       x.num_pages, int(fp8)),
+                                                       x.num_pages, int(fp8),
+                                                       kv_layout=kv_layout),
                                          pages, 128, x.block_table, b, h, L, dst)
                 torch.cuda.synchronize()
-                ref = oracle.gather_keys(workloads.bits(pages), x.block_table[b].cpu().numpy(), L, h)
+                ref = oracle.gather_keys(workloads.bits(pages), x.block_table[b].cpu().numpy(), L, h,
+                                         layout)
                 got = workloads.bits(dst)
                 assert np.array_equal(got, ref), (which, b, h)
 
@@ -215,6 +219,27 @@ def test_both_ring_depths(T, G, Hkv, fp8):
         out, lse = s.run()
         compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} Hkv={Hkv} num_sms={num_sms}")
         assert s.stats()[1] == 0
+
+
+@pytest.mark.parametrize("T,G,Hkv,fp8", [(1, 8, 2, False), (2, 8, 2, False), (1, 4, 3, False),
+                                          (1, 8, 4, True), (1, 2, 3, True), (2, 8, 2, True)])
+def test_nhd_pages(T, G, Hkv, fp8):
+    """Pages stored NHD ([N][P][Hkv][D]) against the oracle reading the same
+    layout, and bit-identical to the same values stored HND (the kernel's
+    shared-memory tiles are the same in both)."""
+    lens = [T, T + 16, 255, 1000, 0, 16 * 9 + 3]
+    w = _custom(lens, G=G, Hkv=Hkv, T=T, fp8=fp8, seed=3 * T + G + Hkv)
+    xn = workloads.make_inputs(w, device="cuda", layout="NHD")
+    xh = workloads.make_inputs(w, device="cuda")
+    assert xn.k_pages.shape[1] == w.page_size and xn.k_pages.shape[2] == Hkv
+    ref_o, ref_l = oracle_direct(xn)
+    for S, mode in ((1, 1), (3, 1), (0, 1), (5, 0)):
+        sn = session(xn, S, mode)
+        out_n, lse_n = sn.run()
+        compare(out_n, lse_n, ref_o, ref_l, what=f"NHD T={T} G={G} Hkv={Hkv} S={S} mode={mode}")
+        assert sn.stats()[1] == 0
+        out_h, lse_h = session(xh, S, mode).run()
+        assert torch.equal(out_n, out_h) and torch.equal(lse_n, lse_h)
 
 
 # ------------------------------------------------------------------ workloads 3 and 5

@@ -102,6 +102,44 @@ def test_direct_matches_brute_force(L, D, P):
         assert abs(lse[0, 0, h] - ref_l) < 1e-13
 
 
+def test_nhd_layout_brute_force():
+    """NHD pages ``[N][P][Hkv][D]``: key j of KV head h is row
+    ``pages[table[j // P]][j % P][h]``, indexed here by hand (P != Hkv, so a
+    swap of the slot and head axes cannot pass)."""
+    rng = np.random.default_rng(17)
+    L, D, P, Hkv, G = 7, 3, 3, 2, 2
+    n = -(-L // P)
+    pool = n + 2
+    q = _bf16_bits(rng.standard_normal((1, 1, Hkv * G, D)))
+    k = _bf16_bits(rng.standard_normal((pool, P, Hkv, D)))
+    v = _bf16_bits(rng.standard_normal((pool, P, Hkv, D)))
+    table = rng.permutation(pool)[:n].astype(np.int32)[None, :]
+    lens = np.array([L], dtype=np.int32)
+    out, lse = O.attention_direct(q, k, v, table, lens, scale=0.6, layout="NHD")
+    for h in range(Hkv * G):
+        hk = h // G
+        K = [O.bf16_to_float(k[table[0, j // P], j % P, hk]) for j in range(L)]
+        V = [O.bf16_to_float(v[table[0, j // P], j % P, hk]) for j in range(L)]
+        ref_o, ref_l = _mp_attention(O.bf16_to_float(q[0, 0, h]), K, V, 0.6)
+        np.testing.assert_allclose(out[0, 0, h], ref_o, atol=1e-13)
+        assert abs(lse[0, 0, h] - ref_l) < 1e-13
+
+
+def test_layout_invariance_is_bitwise():
+    """The same rows stored HND and NHD give bit-identical results, in the
+    direct and the split mode."""
+    q, k, v, table, lens = _mid_problem(L=37, T=2, Hq=8, Hkv=2, P=4)
+    k_n = np.ascontiguousarray(k.transpose(0, 2, 1, 3))
+    v_n = np.ascontiguousarray(v.transpose(0, 2, 1, 3))
+    o1, l1 = O.attention_direct(q, k, v, table, lens, scale=0.3)
+    o2, l2 = O.attention_direct(q, k_n, v_n, table, lens, scale=0.3, layout="NHD")
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    o3, l3 = O.attention_split_mode(q, k, v, table, lens, num_splits=3, scale=0.3)
+    o4, l4 = O.attention_split_mode(q, k_n, v_n, table, lens, num_splits=3, scale=0.3,
+                                    layout="NHD")
+    assert np.array_equal(o3, o4) and np.array_equal(l3, l4)
+
+
 def test_causal_multi_token_brute_force():
     """Query token t of T sees keys 0 .. L-T+t (bottom-right aligned)."""
     rng = np.random.default_rng(7)
@@ -459,10 +497,12 @@ def _pins_on_direct():
     test_identical_keys_give_mean_of_values()
     test_causal_multi_token_brute_force()
     test_head_mapping_uses_contiguous_groups()
+    test_nhd_layout_brute_force()
 
 
 @pytest.mark.parametrize("mistake", ["no_scale", "neg_scores", "k_for_v", "lse_off_by_max",
-                                     "head_mod", "causal_off_by_one", "page_slot_swap"])
+                                     "head_mod", "causal_off_by_one", "page_slot_swap",
+                                     "nhd_read_as_hnd"])
 def test_planted_mistakes_are_caught(monkeypatch, mistake):
     """Each plausible slip, planted in the oracle on the CPU, fails a pin."""
     orig_attend = O._softmax_attend
@@ -499,10 +539,15 @@ def test_planted_mistakes_are_caught(monkeypatch, mistake):
             return orig_direct(q, k, v, table, np.asarray(lens) - (1 if q.shape[1] > 1 else 0), **kw)
         monkeypatch.setattr(O, "attention_direct", bad_direct)
     elif mistake == "page_slot_swap":
-        def bad_gather(pages, row, n, head):
-            P = pages.shape[2]
-            out = orig_gather(pages, row, n, head)
+        def bad_gather(pages, row, n, head, layout="HND"):
+            P = O.page_size_of(pages, layout)
+            out = orig_gather(pages, row, n, head, layout)
             return out[::-1].copy() if n > P else out
         monkeypatch.setattr(O, "gather_keys", bad_gather)
-    with pytest.raises(AssertionError):
+    elif mistake == "nhd_read_as_hnd":
+        # the slot and head axes of NHD pages taken in HND order
+        monkeypatch.setattr(O, "gather_keys",
+                            lambda pages, row, n, head, layout="HND": orig_gather(pages, row, n, head))
+    # (the NHD axes read in HND order index past the slot axis when P != Hkv)
+    with pytest.raises(IndexError if mistake == "nhd_read_as_hnd" else AssertionError):
         _pins_on_direct()

@@ -114,7 +114,7 @@ class Inputs:
 
     w: Workload
     q: torch.Tensor  # bf16 [B][T][Hq][Dk]
-    k_pages: torch.Tensor  # bf16 or uint8 [N][Hkv][P][Dk]
+    k_pages: torch.Tensor  # bf16 or uint8 [N][Hkv][P][Dk] (HND) or [N][P][Hkv][Dk] (NHD)
     v_pages: Optional[torch.Tensor]  # None when V shares K's rows
     block_table: torch.Tensor  # int32 [B][max_pages]
     seq_lens: torch.Tensor  # int32 [B]
@@ -122,6 +122,7 @@ class Inputs:
     kv_scale: float
     scale: float
     poison_page: int  # page filled with NaN (bf16) / 0x7F codes (e4m3)
+    layout: str = "HND"  # order of the page pools' dimensions
 
     @property
     def num_pages(self) -> int:
@@ -140,7 +141,7 @@ def _quantize_e4m3(x: torch.Tensor, kv_scale: float) -> torch.Tensor:
 
 def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
                 poison: bool = True, lens: Optional[np.ndarray] = None,
-                max_pages: Optional[int] = None) -> Inputs:
+                max_pages: Optional[int] = None, layout: str = "HND") -> Inputs:
     """Builds the inputs of workload ``w`` from ``seed`` (default ``w.seed``).
 
     * Lengths, page permutation and block tables come from numpy's PCG64.
@@ -150,7 +151,11 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
       e4m3 code 0x7F, every unused block-table entry points at it, and the
       slots past ``seq_len`` in each sequence's last page are poisoned too:
       a kernel that reads outside the visible keys shows it in its output.
+    * ``layout="NHD"`` stores the same values with the slot and head axes of
+      each page swapped (``[N][P][Hkv][D]``); everything else is unchanged.
     """
+    if layout not in ("HND", "NHD"):
+        raise ValueError(layout)
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     seq_lens = draw_seq_lens(w, rng) if lens is None else np.asarray(lens, np.int32)
@@ -211,6 +216,10 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
                 if v_t is not None:
                     v_t[last, :, L % P:, :].fill_(poison_val)
 
+    if layout == "NHD":
+        k_t = k_t.transpose(1, 2).contiguous()
+        v_t = v_t.transpose(1, 2).contiguous() if v_t is not None else None
+
     return Inputs(
         w=w,
         q=q.to(torch.bfloat16),
@@ -222,6 +231,7 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
         kv_scale=kv_scale,
         scale=w.scale,
         poison_page=poison_page,
+        layout=layout,
     )
 
 
