@@ -308,6 +308,33 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   const int k_begin = p0 * a.P;
   const int k_end = min(p1 * a.P, L);
   const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
+  if (a.deep_ring && !a.fixed && warp == C::NCW) {
+    // While the previous kernel on the stream finishes, warm L2 (and the
+    // address translations) with the tiles the ring takes first (only in a
+    // one-wave grid, whose CTAs all start early; later waves of a larger
+    // grid start with nothing to overlap, measured 0.5-1 % slower): one lane
+    // per tile reads its block-table entry speculatively (a relaxed load; the
+    // previous kernel may still be writing the table) and issues L2
+    // prefetches of its K and V boxes.  A stale entry only warms the wrong
+    // page; the copies proper are issued after the dependency wait from the
+    // entries read again.
+    const int t = lane;
+    if (t < n_tiles && t < C::NST * C::TPS) {
+      const int key0 = k_begin + t * 16;
+      const int page = key0 / a.P;
+      const int ph = ld_relaxed_gpu(a.block_table + size_t(b) * a.max_pages + page);
+      if (ph >= 0 && ph < a.num_pages) {
+        const int kp = key0 - page * a.P;
+        if (FP8) {
+          tma_prefetch_4d(&tk, 0, kp, h0, ph);
+          tma_prefetch_4d(&tv, 0, kp, h0, ph);
+        } else {
+          tma_prefetch_5d(&tk, 0, kp, 0, h0, ph);
+          tma_prefetch_5d(&tv, 0, kp, 0, h0, ph);
+        }
+      }
+    }
+  }
   __syncthreads();
   launch_dependents();
   wait_prerequisites();

@@ -102,6 +102,32 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// L2 prefetches of one box (no shared memory, no barrier): the tensor map
+// bounds-checks the coordinates, and nothing is delivered to the CTA.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* m, int32_t c0, int32_t c1,
+                                                int32_t c2, int32_t c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* m, int32_t c0, int32_t c1,
+                                                int32_t c2, int32_t c3, int32_t c4) {
+  asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+
+// Relaxed GPU-scope load: may run while another grid writes the word (it
+// returns the old or the new value).
+__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // The barrier arm and tiled loads (2-D for the MLA latent rows) issued by a
 // converged warp: one lane, chosen by elect.sync inside the instruction
 // sequence, executes them (a TMA copy issued from a lane that branched away

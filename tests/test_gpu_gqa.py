@@ -122,7 +122,7 @@ def _sms():
 
 @pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("G,Hkv", [(8, 2), (4, 2), (1, 3), (2, 1)])
-@pytest.mark.parametrize("P", [16, 64])
+@pytest.mark.parametrize("P", [16, 32, 64, 128])
 def test_ragged_lengths(fp8, G, Hkv, P):
     lens = [1, 15, 16, 17, 255, 257, 1000, 0, 3 * P, 2 * P + 1]
     w = _custom(lens, G=G, Hkv=Hkv, P=P, fp8=fp8, seed=G * 10 + Hkv + P)
@@ -221,14 +221,15 @@ def test_both_ring_depths(T, G, Hkv, fp8):
         assert s.stats()[1] == 0
 
 
-@pytest.mark.parametrize("T,G,Hkv,fp8", [(1, 8, 2, False), (2, 8, 2, False), (1, 4, 3, False),
-                                          (1, 8, 4, True), (1, 2, 3, True), (2, 8, 2, True)])
-def test_nhd_pages(T, G, Hkv, fp8):
+@pytest.mark.parametrize("T,G,Hkv,fp8,P", [(1, 8, 2, False, 16), (2, 8, 2, False, 32),
+                                            (1, 4, 3, False, 64), (1, 8, 4, True, 16),
+                                            (1, 2, 3, True, 32), (2, 8, 2, True, 16)])
+def test_nhd_pages(T, G, Hkv, fp8, P):
     """Pages stored NHD ([N][P][Hkv][D]) against the oracle reading the same
     layout, and bit-identical to the same values stored HND (the kernel's
     shared-memory tiles are the same in both)."""
     lens = [T, T + 16, 255, 1000, 0, 16 * 9 + 3]
-    w = _custom(lens, G=G, Hkv=Hkv, T=T, fp8=fp8, seed=3 * T + G + Hkv)
+    w = _custom(lens, G=G, Hkv=Hkv, T=T, fp8=fp8, P=P, seed=3 * T + G + Hkv)
     xn = workloads.make_inputs(w, device="cuda", layout="NHD")
     xh = workloads.make_inputs(w, device="cuda")
     assert xn.k_pages.shape[1] == w.page_size and xn.k_pages.shape[2] == Hkv
