@@ -94,7 +94,9 @@ typedef struct splitkv_desc {
   int32_t max_pages_per_seq;  /* row length of block_table                     */
   int32_t num_pages_total;    /* pages in k_pages / v_pages                     */
   int32_t kv_dtype;           /* splitkv_dtype; q and out are always bf16       */
-  int32_t v_shares_k;         /* 1: V_j = first v_dim columns of K_j (MLA)      */
+  int32_t v_shares_k;         /* 1: V_j = first v_dim columns of K_j (the MLA
+                                 latent cache); MLA also serves 0 (V its own
+                                 [N][1][P][512] tensor)                        */
   int32_t combine_mode;       /* splitkv_combine_mode                           */
   int32_t kv_layout;          /* splitkv_kv_layout of k_pages and v_pages       */
 } splitkv_desc_t;

@@ -123,7 +123,7 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
     return fail(SPLITKV_EUNSUPPORTED,
                 "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
                 "(GQA: qk_dim=v_dim=128, T*G<=16; MLA: 128 q heads, 1 bf16 latent head, "
-                "qk_dim=576, v_dim=512, v_shares_k, page_size 64, T<=16)",
+                "qk_dim=576, v_dim=512, page_size 64, T<=16)",
                 d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
                 d->v_shares_k);
   return SPLITKV_OK;
@@ -142,7 +142,8 @@ splitkv_status fail(splitkv_status s, const char* fmt, ...) {
 Family family_of(const splitkv_desc_t& d) {
   const int G = d.num_q_heads / d.num_kv_heads;
   if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 16) return Family::kGqa;
-  if (d.qk_dim == 576 && d.v_dim == 512 && d.v_shares_k && d.num_kv_heads == 1 &&
+  // V either shares the latent rows (their first 512 columns) or is its own tensor
+  if (d.qk_dim == 576 && d.v_dim == 512 && d.num_kv_heads == 1 &&
       d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.page_size == 64 && d.q_tokens <= 16)
     return Family::kMla;
   return Family::kNone;
@@ -377,14 +378,19 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
   if (family_of(d) == Family::kMla) {
-    // Latent cache rows of 576 bf16 (64-key boxes = one page); the query rows
-    // are read by the kernel's threads.  The partials are always merged by
-    // the separate combine kernel.
-    TmaDesc tk;
+    // Latent cache rows of 576 bf16 (64-key boxes = one page), and with a
+    // separate V tensor its rows of 512; the query rows are read by the
+    // kernel's threads.  The partials are always merged by the separate
+    // combine kernel.
+    TmaDesc tk, tv;
     splitkv_status st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, 64);
     if (st != SPLITKV_OK) return st;
+    if (!d.v_shares_k) {
+      st = make_bf16_map(&tv, v_pages, d.v_dim, rows_total, 64);
+      if (st != SPLITKV_OK) return st;
+    }
     a.fused = 0;
-    cudaError_t e = launch_mla(a, tk, stream);
+    cudaError_t e = launch_mla(a, tk, d.v_shares_k ? nullptr : &tv, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the MLA split-KV kernel");
     e = launch_combine(a, true, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");

@@ -109,7 +109,9 @@ struct alignas(64) TmaDesc {
 
 cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv, bool fp8,
                        void* stream);
-cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, void* stream);
+// tv: the V map of a cache with separate V rows, or null when V is the first
+// columns of the key rows
+cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, void* stream);
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
 cudaError_t launch_refresh(const splitkv_plan_s& p, void* workspace, const int32_t* seq_lens,
                            void* stream);

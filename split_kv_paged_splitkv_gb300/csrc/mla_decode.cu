@@ -38,6 +38,13 @@
 // MMA issuer (whole warps run the issue loops; one elected lane issues),
 // warps 2-5 load Q, then softmax and epilogue (thread = query head = TMEM
 // lane), warp 6 V-ring producer.
+//
+// Separate V (SEPV: a cache whose V rows are their own 512-wide tensor, not
+// the first columns of the key rows): the V-ring slot of block j first holds
+// the five key chunks as above; once the score MMAs of block j have read
+// them, warp 7 loads block j's V half over the first four of them, and PV(j)
+// waits for that load.  Shared memory and TMEM are laid out as for the
+// shared latent row; each V-ring slot is filled twice per use.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -65,7 +72,7 @@ struct Mla {
   static constexpr int OFF_V = OFF_N + NST * N_SLOT;    // V ring
   static constexpr int OFF_BAR = OFF_V + NST * V_SLOT;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr int THREADS = 224;
+  static constexpr int THREADS = 224;       // 256 with separate V (warp 7 loads V)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL = 0, Q_COL = 128, O_COL = 256;  // S_b at S_COL + 64 b
   static constexpr float RESCALE_LOG2 = 8.f;  // lazy maximum: rescale when it grows by > 2^8
@@ -88,15 +95,21 @@ enum {
                                     // buffer, so no barrier runs two phases ahead
   B_PFREE = B_PFULL + 2,            // PV done (P read, O stable)
   B_DONE,                           // every MMA this CTA issued has completed
-  B_COUNT
+  B_XKDONE,                         // [NST] separate V: the score MMAs have read the
+                                    // key chunks of V slot s
+  B_VDATA = B_XKDONE + Mla::NST,    // [NST] separate V: V rows landed in V slot s
+  B_COUNT = B_VDATA + Mla::NST
 };
+static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 
 // Column chunk (of the nine) in N-ring slot chunk i / V-ring slot chunk k of half h.
 __device__ __forceinline__ int n_chunk(int h, int i) { return h == 0 ? 4 + i : i; }
 __device__ __forceinline__ int v_chunk(int h, int k) { return k < 4 ? 4 * h + k : 8; }
 
-__global__ void __launch_bounds__(Mla::THREADS, 1)
-    mla_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk) {
+template <bool SEPV>
+__global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
+    mla_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv) {
   using C = Mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -143,12 +156,21 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     mbar_init(bar(B_PFULL + 1), 128);
     mbar_init(bar(B_PFREE), 1);
     mbar_init(bar(B_DONE), 1);
+    if (SEPV) {
+      for (int s = 0; s < C::NST; ++s) {
+        mbar_init(bar(B_XKDONE + s), 1);
+        mbar_init(bar(B_VDATA + s), 1);
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    if (lane == 0) prefetch_tmap(&tk);
+    if (lane == 0) {
+      prefetch_tmap(&tk);
+      if (SEPV) prefetch_tmap(&tv);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -214,10 +236,51 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
         if (!mbar_wait(bar(full0 + st), (last / C::NST) & 1)) break;
       }
     }
+  } else if (SEPV && warp == 7) {
+    // ----------------------------------------------------- V producer (SEPV)
+    // Block j's V half into the first NV chunks of V slot j % NST, once the
+    // score MMAs of block j have read the key chunks there.
+    const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
+    bool ok = true;
+    int issued = 0;
+    int phys = 0, chunk0 = -32;
+    for (int j = 0; j < nblk && ok; ++j) {
+      const int page = p0 + j;
+      if (page >= chunk0 + 32) {
+        chunk0 = page;
+        const int my = chunk0 + lane;
+        phys = 0;
+        if (my < p1) {
+          phys = __ldg(trow + my);
+          if (phys < 0 || phys >= a.num_pages) phys = 0;  // reported by the key producer
+        }
+      }
+      const int y = (__shfl_sync(kFull, phys, page - chunk0) * a.Hkv) * a.P;
+      const int st = j % C::NST;
+      ok = __all_sync(kFull, mbar_wait(bar(B_XKDONE + st), (j / C::NST) & 1));
+      if (!ok) break;
+      mbar_arrive_expect_tx_warp(bar(B_VDATA + st), C::NV * C::K_CH);
+      for (int k = 0; k < C::NV; ++k)
+        tma_load_2d_warp(smem_u32(sm + C::OFF_V + st * C::V_SLOT + k * C::K_CH), &tv,
+                         bar(B_VDATA + st), (4 * h + k) * 64, y);
+      issued = j + 1;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // stay until every issued copy has landed
+    if (lane == 0) {
+      for (int st = 0; st < C::NST && st < issued; ++st) {
+        const int last = st + C::NST * ((issued - 1 - st) / C::NST);
+        if (!mbar_wait(bar(B_VDATA + st), (last / C::NST) & 1)) break;
+      }
+    }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    // Issue order follows readiness: PV(jp) as soon as P(jp) is in TMEM (it
-    // frees a V slot); else the next half of QK(jq) into S_{jq % 2}: the
+    // Issue order follows readiness: PV(jp) as soon as P(jp) is in TMEM (and,
+    // with separate V, its V rows have landed; it frees a V slot); else the
+    // next half of QK(jq) into S_{jq % 2}: the
     // N-ring chunks once their slot landed and PV(jq - 2) has read the P
     // that shares that S buffer, then the V-ring chunks once their slot landed.
     const uint32_t idesc_qk = umma_idesc_bf16(128, 64, 0, 0);
@@ -227,10 +290,14 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
     bool qk_half = false;  // the N-ring half of QK(jq) has been issued
     long long t_idle = clock64();
     while (ok && jp < nblk) {
-      if (jp < jq && __shfl_sync(kFull, mbar_test(bar(B_PFULL + (jp & 1)), (jp >> 1) & 1), 0)) {  // O_h += P.V
+      if (jp < jq &&
+          __shfl_sync(kFull,
+                      mbar_test(bar(B_PFULL + (jp & 1)), (jp >> 1) & 1) &&
+                          (!SEPV || mbar_test(bar(B_VDATA + jp % C::NST), (jp / C::NST) & 1)),
+                      0)) {  // O_h += P.V
         const int vs = jp % C::NST;
         tc_fence_after();
-        uint8_t* vst = sm + C::OFF_V + vs * C::V_SLOT;  // its first NV chunks are V_h
+        uint8_t* vst = sm + C::OFF_V + vs * C::V_SLOT;  // its first NV chunks hold V_h
         const int valid = min(C::BK, k_end - (k_begin + jp * C::BK));
         if (valid < C::BK) {
           // key slots past the last key may hold anything (even NaN): zero their
@@ -292,6 +359,7 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
                              umma_desc(smem_u32(sm + C::OFF_Q + k * C::Q_CH) + kin * 32, 16, 1024, 2),
                              umma_desc(vst + k * C::K_CH + kin * 32, 16, 1024, 2), idesc_qk, 1u);
           umma_commit_warp(bar(B_SFULL + (jq & 1)));
+          if (SEPV) umma_commit_warp(bar(B_XKDONE + qs));  // its key chunks may be overwritten
           __syncwarp();
           ++jq;
           qk_half = false;
@@ -494,23 +562,35 @@ __global__ void __launch_bounds__(Mla::THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, void* stream) {
-  if (a.n_items == 0) return cudaSuccess;
+namespace {
+
+template <bool SEPV>
+cudaError_t launch_mla_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                         cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      mla_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Mla::SMEM);
+      mla_splitkv_kernel<SEPV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Mla::SMEM);
   if (attr != cudaSuccess) return attr;
-  const CUtensorMap& mk = *reinterpret_cast<const CUtensorMap*>(&tk);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_items * a.T * 2, 1, 1);
-  cfg.blockDim = dim3(Mla::THREADS, 1, 1);
+  cfg.blockDim = dim3(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1, 1);
   cfg.dynamicSmemBytes = Mla::SMEM;
-  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.stream = s;
   cudaLaunchAttribute attrs[1];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_splitkv_kernel, a, mk);
+  return cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<SEPV>, a, mk, mv);
+}
+
+}  // namespace
+
+cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, void* stream) {
+  if (a.n_items == 0) return cudaSuccess;
+  const CUtensorMap& mk = *reinterpret_cast<const CUtensorMap*>(&tk);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (tv) return launch_mla_t<true>(a, mk, *reinterpret_cast<const CUtensorMap*>(tv), s);
+  return launch_mla_t<false>(a, mk, mk, s);
 }
 
 }  // namespace splitkv

@@ -129,6 +129,16 @@ def test_plan_rejects_bad_descriptors(bad, code):
     assert e.value.status == code
 
 
+def test_mla_with_separate_v_is_planned():
+    """The MLA shapes plan alike whether V shares the latent rows or not."""
+    lens = np.array([5000], np.int32)
+    items = []
+    for vsk in (1, 0):
+        d = skv.make_desc(1, 6, 128, 1, 576, 512, 64, 128, 200, skv.SPLITKV_BF16, vsk)
+        items.append(skv.splitkv_plan_get_items(skv.splitkv_plan(d, lens, 4, 148)))
+    assert np.array_equal(items[0], items[1])
+
+
 def test_kv_layout_field():
     """Both page layouts plan alike (the split table does not depend on the
     layout); any other value is rejected."""

@@ -21,16 +21,19 @@ def _gpu():
     need_gpu()
 
 
-def _mla(lens, T, seed=3):
+def _mla(lens, T, seed=3, v_shares_k=True):
     return workloads.Workload("mla_custom", len(lens), T, 128, 1, 576, 512, 64, "bf16",
                               "list:" + ":".join(str(int(x)) for x in lens), std=0.5,
-                              v_shares_k=True, pool_slack=0.5, seed=seed)
+                              v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
 
 @pytest.mark.parametrize("T", [1, 2, 6])
-def test_mla_small_ragged(T):
+@pytest.mark.parametrize("sepv", [False, True])
+def test_mla_small_ragged(T, sepv):
+    """V as the first 512 columns of the latent rows, or (sepv) its own tensor."""
     lens = [T, 64, 100, 130, 1000]
-    x = workloads.make_inputs(_mla(lens, T, seed=10 + T), device="cuda")
+    x = workloads.make_inputs(_mla(lens, T, seed=10 + T + 5 * sepv, v_shares_k=not sepv),
+                              device="cuda")
     ref_o, ref_l = oracle_direct(x)
     for S in (1, 2, 3, 0):
         s = session(x, S)
@@ -45,8 +48,9 @@ def test_mla_small_ragged(T):
         assert (log[:, 3] == 0).all()
 
 
-def test_mla_ctx64k_full():
-    w = workloads.WORKLOADS["mla_t6_ctx64k"]
+@pytest.mark.parametrize("name", ["mla_t6_ctx64k", "mla_sepv_t6_ctx64k"])
+def test_mla_ctx64k_full(name):
+    w = workloads.WORKLOADS[name]
     x = workloads.make_inputs(w, device="cuda")
     ref_o, ref_l = oracle_direct(x)
     for S in w.splits:

@@ -80,6 +80,10 @@ WORKLOADS = {
     "mla_t6_ctx64k": Workload(
         "mla_t6_ctx64k", 1, 6, 128, 1, 576, 512, 64, "bf16", "fixed:65536",
         std=0.5, v_shares_k=True, splits=(1, 4, 8, 0), pool_slack=0.0, seed=1004),
+    # the same MLA decode over a cache whose V rows are a separate 512-wide tensor
+    "mla_sepv_t6_ctx64k": Workload(
+        "mla_sepv_t6_ctx64k", 1, 6, 128, 1, 576, 512, 64, "bf16", "fixed:65536",
+        std=0.5, v_shares_k=False, splits=(1, 4, 0), pool_slack=0.0, seed=1006),
     "mixed_batch32_bf16": Workload(
         "mixed_batch32_bf16", 32, 1, 32, 8, 128, 128, 16, "bf16",
         "loguniform:256:131072", splits=(0,), pool_slack=0.02, seed=1005),
