@@ -276,6 +276,34 @@ splitkv_status splitkv_decode_kv_scales(const splitkv_plan_t* plan, void* worksp
                                         void* stream);
 
 /*
+ * splitkv_decode_partials / splitkv_combine_workspace -- splitkv_decode in
+ * its two steps: the per-split partial attention pass, then the log-sum-exp
+ * merge ("vLLM 0.30.0 FA4 SplitKV Bug: H100 Decode Can Be 48% Slower",
+ * sections "What SplitKV is trying to do" and "Why the result is still
+ * correct").  splitkv_decode_partials launches only the split-KV kernel, in
+ * the SEPARATE form whatever desc.combine_mode says: sequences with one
+ * split write out / lse, the others leave their fp32 (O_s, lse_s) partials
+ * in the workspace.  splitkv_combine_workspace then merges those partials
+ * into out / lse (one kernel; it reads nothing else), so the pair writes
+ * exactly what splitkv_decode writes in SPLITKV_COMBINE_SEPARATE mode.
+ * Between the two a caller may run its own work on the stream (or read,
+ * exchange and merge the partials itself), as long as it leaves the
+ * workspace's partials intact.
+ *   splitkv_decode_partials     arguments and errors as splitkv_decode
+ *   splitkv_combine_workspace   plan, workspace (as passed to the partials
+ *                               call), out bf16 [B][T][Hq][Dv] (16-byte
+ *                               aligned), lse fp32 [B][T][Hq] or NULL
+ * EINVAL for NULL or misaligned pointers; EWORKSPACE for a NULL workspace.
+ */
+splitkv_status splitkv_decode_partials(const splitkv_plan_t* plan, void* workspace,
+                                       const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int32_t num_splits, float scale, float kv_scale, void* out,
+                                       float* lse, void* stream);
+splitkv_status splitkv_combine_workspace(const splitkv_plan_t* plan, void* workspace, void* out,
+                                         float* lse, void* stream);
+
+/*
  * splitkv_decode_noalloc -- splitkv_decode for callers that cannot allocate
  * device memory (code running inside another framework's memory budget,
  * plugins whose host forbids device allocations after start-up, real-time

@@ -62,6 +62,9 @@ _SIGNATURES = {
     "splitkv_decode_kv_scales": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _vp, _vp, _vp,
                                         _vp, _vp]),
     "splitkv_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
+    "splitkv_decode_partials": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp,
+                                       _vp]),
+    "splitkv_combine_workspace": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "splitkv_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "splitkv_read_stats": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp]),
     "splitkv_debug_gather": (_i32, [ctypes.POINTER(splitkv_desc_t), _vp, _i32, _vp, _i32, _i32,
@@ -195,6 +198,21 @@ def splitkv_decode(plan: Plan, workspace, q, k_pages, v_pages, block_table, seq_
     _check(_lib.splitkv_decode(plan.handle, _ptr(workspace), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                                _ptr(block_table), _ptr(seq_lens), num_splits, scale, kv_scale,
                                _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def splitkv_decode_partials(plan: Plan, workspace, q, k_pages, v_pages, block_table, seq_lens,
+                            num_splits: int, scale: float, kv_scale: float, out, lse, stream=None):
+    """The split-KV kernel of splitkv_decode alone (partials stay in the workspace)."""
+    _check(_lib.splitkv_decode_partials(plan.handle, _ptr(workspace), _ptr(q), _ptr(k_pages),
+                                        _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                        num_splits, scale, kv_scale, _ptr(out), _ptr(lse),
+                                        _stream(stream)))
+
+
+def splitkv_combine_workspace(plan: Plan, workspace, out, lse, stream=None):
+    """The merge of the partials splitkv_decode_partials left in the workspace."""
+    _check(_lib.splitkv_combine_workspace(plan.handle, _ptr(workspace), _ptr(out), _ptr(lse),
+                                          _stream(stream)))
 
 
 def splitkv_decode_kv_scales(plan: Plan, workspace, q, k_pages, v_pages, block_table, seq_lens,

@@ -305,12 +305,14 @@ splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace,
 
 namespace {
 
-// The decode call; k_scale / v_scale (device, [Hkv]) replace kv_scale when given.
+// The decode call; k_scale / v_scale (device, [Hkv]) replace kv_scale when
+// given.  Without `merge` only the split-KV kernel runs (in SEPARATE form):
+// sequences with more than one split leave their partials in the workspace.
 splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const void* q,
                            const void* k_pages, const void* v_pages, const int32_t* block_table,
                            const int32_t* seq_lens, int32_t num_splits, float scale,
                            float kv_scale, const float* k_scale, const float* v_scale, void* out,
-                           float* lse, void* stream) {
+                           float* lse, void* stream, bool merge = true) {
   if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
   const splitkv_desc_t& d = plan->desc;
   if (!workspace) return fail(SPLITKV_EWORKSPACE, "workspace is NULL");
@@ -373,7 +375,7 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   a.k_scale = k_scale;  // per-head factors, applied by the kernel per KV head
   a.v_scale = v_scale;
   a.fixed = plan->fixed ? 1 : 0;
-  a.fused = d.combine_mode == SPLITKV_COMBINE_FUSED;
+  a.fused = merge && d.combine_mode == SPLITKV_COMBINE_FUSED;
   a.deep_ring = plan->n_items <= plan->num_sms ? 1 : 0;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
@@ -392,8 +394,10 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
     a.fused = 0;
     cudaError_t e = launch_mla(a, tk, d.v_shares_k ? nullptr : &tv, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the MLA split-KV kernel");
-    e = launch_combine(a, true, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
+    if (merge) {
+      e = launch_combine(a, true, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
+    }
     return SPLITKV_OK;
   }
   TmaDesc tk, tv;
@@ -407,7 +411,7 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
 
   cudaError_t e = launch_gqa(a, tk, tv, fp8, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the split-KV kernel");
-  if (!a.fused) {
+  if (merge && !a.fused) {
     e = launch_combine(a, true, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
   }
@@ -434,6 +438,43 @@ splitkv_status splitkv_decode_kv_scales(const splitkv_plan_t* plan, void* worksp
   if (!k_scale || !v_scale) return fail(SPLITKV_EINVAL, "k_scale and v_scale must not be NULL");
   return decode_impl(plan, workspace, q, k_pages, v_pages, block_table, seq_lens, num_splits,
                      scale, 1.f, k_scale, v_scale, out, lse, stream);
+}
+
+splitkv_status splitkv_decode_partials(const splitkv_plan_t* plan, void* workspace,
+                                       const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int32_t num_splits, float scale, float kv_scale, void* out,
+                                       float* lse, void* stream) {
+  return decode_impl(plan, workspace, q, k_pages, v_pages, block_table, seq_lens, num_splits,
+                     scale, kv_scale, nullptr, nullptr, out, lse, stream, false);
+}
+
+splitkv_status splitkv_combine_workspace(const splitkv_plan_t* plan, void* workspace, void* out,
+                                         float* lse, void* stream) {
+  if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
+  if (!workspace) return fail(SPLITKV_EWORKSPACE, "workspace is NULL");
+  if (!out) return fail(SPLITKV_EINVAL, "out must not be NULL");
+  if (!aligned16(workspace) || !aligned16(out))
+    return fail(SPLITKV_EINVAL, "device pointers must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SPLITKV_EINVAL, "lse must be 4-byte aligned");
+  const splitkv_desc_t& d = plan->desc;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  DecodeArgs a{};
+  a.groups = reinterpret_cast<const int32_t*>(ws + plan->off_groups);
+  a.lse_part = reinterpret_cast<float*>(ws + plan->off_lse);
+  a.o_part = reinterpret_cast<float*>(ws + plan->off_o);
+  a.out = out;
+  a.lse = lse;
+  a.n_groups = plan->n_groups;
+  a.T = d.q_tokens;
+  a.Hq = d.num_q_heads;
+  a.G = d.num_q_heads / d.num_kv_heads;
+  a.rows = plan->rows;
+  a.dv = d.v_dim;
+  a.fixed = plan->fixed ? 1 : 0;
+  cudaError_t e = launch_combine(a, true, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
+  return SPLITKV_OK;
 }
 
 splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32_t n_parts,

@@ -8,7 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, SPLITKV_LAYOUT_HND,
-               SPLITKV_LAYOUT_NHD, make_desc, splitkv_decode,
+               SPLITKV_LAYOUT_NHD, make_desc, splitkv_combine_workspace, splitkv_decode,
+               splitkv_decode_partials,
                splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_fixed, splitkv_plan_refresh,
                splitkv_plan_upload, splitkv_read_stats)
 
@@ -69,6 +70,25 @@ class DecodeSession:
             splitkv_decode(self.plan, self.workspace, q, k, v, table, lens, self.num_splits,
                            self.scale, self.kv_scale, o, l, self.stream)
         return self.out if out is None else out, self.lse if lse is None else lse
+
+    def run_partials(self, out=None, lse=None, tensors=None):
+        """The split-KV kernel alone (splitkv_decode_partials): rows of sequences
+        with one split are final, the others wait for merge()."""
+        q, k, v, table, lens = tensors if tensors is not None else self.tensors
+        o = self.out if out is None else out
+        l = self.lse if lse is None else lse
+        if self.fixed:
+            splitkv_plan_refresh(self.plan, self.workspace, lens, self.stream)
+        splitkv_decode_partials(self.plan, self.workspace, q, k, v, table, lens, self.num_splits,
+                                self.scale, self.kv_scale, o, l, self.stream)
+        return o, l
+
+    def merge(self, out=None, lse=None):
+        """Merges the partials run_partials left in the workspace (splitkv_combine_workspace)."""
+        o = self.out if out is None else out
+        l = self.lse if lse is None else lse
+        splitkv_combine_workspace(self.plan, self.workspace, o, l, self.stream)
+        return o, l
 
     def stats(self):
         """(per-CTA log [n][4], device status word) -- synchronises the stream."""

@@ -139,6 +139,19 @@ def test_mla_with_separate_v_is_planned():
     assert np.array_equal(items[0], items[1])
 
 
+def test_two_step_entry_points_validate_before_any_cuda_call():
+    plan = skv.splitkv_plan(_desc(B=1), np.array([300], np.int32), 2, 148)
+    A = 1 << 20  # aligned, never dereferenced: validation fails first
+    assert skv._lib.splitkv_combine_workspace(None, A, A, A, None) == skv.SPLITKV_EINVAL
+    assert skv._lib.splitkv_combine_workspace(plan.handle, None, A, A, None) == skv.SPLITKV_EWORKSPACE
+    assert skv._lib.splitkv_combine_workspace(plan.handle, A, None, A, None) == skv.SPLITKV_EINVAL
+    assert skv._lib.splitkv_combine_workspace(plan.handle, A + 8, A, A, None) == skv.SPLITKV_EINVAL
+    assert skv._lib.splitkv_combine_workspace(plan.handle, A, A, A + 2, None) == skv.SPLITKV_EINVAL
+    st = skv._lib.splitkv_decode_partials(plan.handle, A, A, A, A, A, A, 0, 0.1, 1.0, None, None,
+                                          None)
+    assert st == skv.SPLITKV_EINVAL  # out is NULL
+
+
 def test_kv_layout_field():
     """Both page layouts plan alike (the split table does not depend on the
     layout); any other value is rejected."""
