@@ -195,6 +195,21 @@ void splitkv_plan_destroy(splitkv_plan_t* plan);
 splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items_host,
                                       int32_t capacity, int32_t* n_items);
 
+/*
+ * splitkv_plan_get_ranges -- the split table per KV head: one row of
+ * SPLITKV_RANGE_FIELDS int32 (b, h_kv, s, page_begin, page_end) for every
+ * sequence b, KV head h_kv and split s < S_b, in launch order (the KV heads of
+ * one work item consecutively).  Split s of sequence b covers pages
+ * [floor(s * n_b / S_b), floor((s + 1) * n_b / S_b)) of n_b = ceil(L_b / P),
+ * never empty unless L_b == 0.  capacity is in rows; *n_ranges always
+ * receives the row count (items * heads_per_item); EINVAL if capacity is
+ * smaller (nothing copied).  For a capacity plan these are the template's
+ * rows, all empty until splitkv_plan_refresh fills the device list.
+ */
+enum { SPLITKV_RANGE_FIELDS = 5 };
+splitkv_status splitkv_plan_get_ranges(const splitkv_plan_t* plan, int32_t* ranges_host,
+                                       int32_t capacity, int32_t* n_ranges);
+
 /* Number of work items. */
 int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
 

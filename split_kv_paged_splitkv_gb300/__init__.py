@@ -27,6 +27,7 @@ SPLITKV_BF16, SPLITKV_FP8_E4M3 = 0, 1
 SPLITKV_COMBINE_FUSED, SPLITKV_COMBINE_SEPARATE = 0, 1
 SPLITKV_LAYOUT_HND, SPLITKV_LAYOUT_NHD = 0, 1
 SPLITKV_ITEM_FIELDS = 8
+SPLITKV_RANGE_FIELDS = 5
 SPLITKV_DEVERR_TIMEOUT, SPLITKV_DEVERR_SEQLEN, SPLITKV_DEVERR_PAGE = 1, 2, 4
 ITEM_FIELD_NAMES = ("b", "h_kv", "split", "num_splits", "page_begin", "page_end", "slot", "group")
 
@@ -52,6 +53,7 @@ _SIGNATURES = {
     "splitkv_read_items": (_i32, [_vp, _vp, _vp, _i32, _vp]),
     "splitkv_plan_destroy": (None, [_vp]),
     "splitkv_plan_get_items": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32)]),
+    "splitkv_plan_get_ranges": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32)]),
     "splitkv_plan_num_items": (_i32, [_vp]),
     "splitkv_plan_num_ctas": (_i32, [_vp]),
     "splitkv_plan_heads_per_item": (_i32, [_vp]),
@@ -182,6 +184,16 @@ def splitkv_plan_get_items(plan: Plan) -> np.ndarray:
     out = np.zeros((n.value, SPLITKV_ITEM_FIELDS), dtype=np.int32)
     _check(_lib.splitkv_plan_get_items(plan.handle, out.ctypes.data if n.value else None,
                                        n.value, ctypes.byref(n)))
+    return out
+
+
+def splitkv_plan_get_ranges(plan: Plan) -> np.ndarray:
+    """The split table per KV head: rows (b, h_kv, s, page_begin, page_end)."""
+    n = _i32()
+    _check(_lib.splitkv_plan_get_ranges(plan.handle, None, 0, ctypes.byref(n)))
+    out = np.zeros((n.value, SPLITKV_RANGE_FIELDS), dtype=np.int32)
+    _check(_lib.splitkv_plan_get_ranges(plan.handle, out.ctypes.data if n.value else None,
+                                        n.value, ctypes.byref(n)))
     return out
 
 

@@ -287,6 +287,28 @@ splitkv_status splitkv_plan_get_items(const splitkv_plan_t* plan, int32_t* items
   return SPLITKV_OK;
 }
 
+splitkv_status splitkv_plan_get_ranges(const splitkv_plan_t* plan, int32_t* ranges_host,
+                                       int32_t capacity, int32_t* n_ranges) {
+  if (!plan || !n_ranges) return fail(SPLITKV_EINVAL, "plan and n_ranges must not be NULL");
+  const int hpi = heads_per_item(plan->desc);
+  const int32_t n = plan->n_items * hpi;
+  *n_ranges = n;
+  if (!ranges_host) return capacity == 0 ? SPLITKV_OK : fail(SPLITKV_EINVAL, "ranges_host is NULL");
+  if (capacity < n) return fail(SPLITKV_EINVAL, "capacity %d < %d ranges", capacity, n);
+  int32_t* out = ranges_host;
+  for (int32_t i = 0; i < plan->n_items; ++i) {
+    const int32_t* it = plan->items.data() + size_t(i) * SPLITKV_ITEM_FIELDS;
+    for (int hh = 0; hh < hpi; ++hh, out += SPLITKV_RANGE_FIELDS) {
+      out[0] = it[SPLITKV_ITEM_B];
+      out[1] = it[SPLITKV_ITEM_HKV] + hh;
+      out[2] = it[SPLITKV_ITEM_SPLIT];
+      out[3] = it[SPLITKV_ITEM_PAGE0];
+      out[4] = it[SPLITKV_ITEM_PAGE1];
+    }
+  }
+  return SPLITKV_OK;
+}
+
 size_t splitkv_workspace_size(const splitkv_plan_t* plan) { return plan ? plan->total : 0; }
 
 splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace,

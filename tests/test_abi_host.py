@@ -59,6 +59,11 @@ def _check_plan(lens, P, Hkv, S, sms, Hq=None, fp8=False):
     ref = _oracle_items(lens, P, Hkv, S, sms, hpi)
     assert items.shape[0] == ref.shape[0]
     assert np.array_equal(items[:, :6], ref), (lens, S)
+    # the split table per KV head: every head of an item, (b, h_kv, s, p0, p1)
+    ranges = skv.splitkv_plan_get_ranges(plan)
+    ref_rows = np.array([(b, h0 + hh, s_, p0, p1) for (b, h0, s_, _, p0, p1) in ref
+                         for hh in range(hpi)], dtype=np.int32).reshape(-1, 5)
+    assert np.array_equal(ranges, ref_rows), (lens, S)
     return items
 
 
