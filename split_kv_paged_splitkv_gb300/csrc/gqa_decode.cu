@@ -1,28 +1,34 @@
 // Split-KV partial attention for thin query groups (GQA), sm_103a.
 //
 // One CTA per work item (b, HPI consecutive KV heads, split, page range).
-// The split's pages are streamed HBM -> shared memory by TMA (one tiled box
-// per 16-key tile of K and of V covering the item's HPI heads, 128-byte
-// swizzle so the ldmatrix reads below are bank-conflict free), through a
-// ring of NST stages guarded by mbarriers.  One producer warp issues the
-// copies.  Consumer warp w serves head slot w % HPI and takes every
-// (NCW / HPI)-th tile: with HPI = 4 each warp owns one head and every tile.
+// The split's pages are streamed HBM -> shared memory by TMA: one tiled box
+// per 16-key tile of K and one of V, covering the item's HPI heads, through
+// tensor maps whose coordinates are (dims, key in page, [column half,] KV
+// head, page) whether the pools are HND or NHD, with the 128-byte swizzle so
+// the ldmatrix reads below are bank-conflict free.  The boxes land in a ring
+// of NST stages guarded by mbarriers: two 32 KB stages, so that three CTAs
+// share an SM, or four for a grid of at most one CTA per SM, whose producer
+// also warms L2 with its first tiles before the dependency wait.  One
+// producer warp issues the copies.  The four consumer warps form slots
+// (head slot, row group): each slot serves query rows [8 rg, 8 rg + 8) of
+// KV head h0 + hs, and a slot's warps take its tiles round-robin.
 //
 // Per 16-key tile a consumer warp computes, on the warp tensor-core path:
 //   S^T[16 keys x 8 rows] = K_tile[16 x 128] . Q^T      (m16n8k16, keys on M)
 //   online softmax over the keys of each query row (shuffle reductions)
 //   O^T[128 x 8 rows]   += V_tile^T[128 x 16] . P^T     (m16n8k16, dims on M)
-// so a group of up to 8 query rows (T*G <= 8) fills the MMA's N side and the
-// 16-key tile fills M with no padding.  P^T is turned from accumulator layout
-// into operand layout in registers with movmatrix.  FP8 e4m3 tiles are
-// converted to f16 in registers (exact, ptx::e4m3x2_*) and use the f16
-// MMA; BF16 tiles go straight to the bf16 MMA.
+// so a row group of up to 8 query rows fills the MMA's N side (9 to 16 rows
+// per KV head -- speculative decode -- take two row groups over the same
+// tiles) and the 16-key tile fills M with no padding.  P^T is turned from
+// accumulator layout into operand layout in registers with movmatrix.  FP8
+// e4m3 tiles are converted to f16 in registers (exact, ptx::e4m3x2_*) and
+// use the f16 MMA; BF16 tiles go straight to the bf16 MMA.
 //
-// The (m, l, O) of the warps sharing a head are merged in shared memory; the
-// item's result is
-// written as the final bf16 output (S_b == 1) or as an fp32 partial with its
-// natural-log LSE.  With the fused combine, the last CTA of a (b, h_kv) group
-// (atomic ticket, no waiting) merges the group's partials.
+// The (m, l, O) of the warps sharing a slot are merged in shared memory; the
+// item's result is written as the final bf16 output (S_b == 1) or as an fp32
+// partial with its natural-log LSE.  With the fused combine, the last CTA of
+// a (b, head group) group -- or, past 8 splits, of each bundle of 8 splits
+// and then of the bundles (atomic tickets, no waiting) -- merges the partials.
 //
 // This is the split partial of "vLLM 0.30.0 FA4 SplitKV Bug: H100 Decode Can
 // Be 48% Slower", section "What SplitKV is trying to do"; the merge gives
