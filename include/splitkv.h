@@ -367,8 +367,13 @@ splitkv_status splitkv_combine(const float* o_part, const float* lse_part, int32
  *                 one-past-last page it iterated, keys it scored, flag} in
  *                 launch order; flag (GQA, fused mode): bit 0 set if the CTA
  *                 wrote its group's merged output, bit 1 set if it merged a
- *                 bundle of up to 8 splits; flag (MLA): 1 if the CTA gave up
- *                 on a timed-out wait
+ *                 bundle of up to 8 splits; flag (MLA): nonzero if the CTA
+ *                 gave up on a timed-out wait, (role << 24) | (x << 12) | y
+ *                 with role 1 the N-ring producer, 2 the V-ring producer, 3
+ *                 the producer of a separate V tensor (y = block), 4 the MMA
+ *                 issuer (bit 23: half of QK(x) issued; x = next QK block,
+ *                 y = next PV block), 5 the softmax warps (x = 1 waiting for
+ *                 S, 2 for PV before a rescale; y = block), 6 the epilogue
  *   capacity      rows of cta_log_host; EINVAL if below splitkv_plan_num_ctas
  *   status_host   int32 or NULL: 0, or a bit set of SPLITKV_DEVERR_* values
  */

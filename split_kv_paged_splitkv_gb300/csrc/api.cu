@@ -397,6 +397,7 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   a.k_scale = k_scale;  // per-head factors, applied by the kernel per KV head
   a.v_scale = v_scale;
   a.fixed = plan->fixed ? 1 : 0;
+  a.max_splits = plan->max_group_splits;
   a.fused = merge && d.combine_mode == SPLITKV_COMBINE_FUSED;
   a.deep_ring = plan->n_items <= plan->num_sms ? 1 : 0;
 
@@ -494,6 +495,7 @@ splitkv_status splitkv_combine_workspace(const splitkv_plan_t* plan, void* works
   a.rows = plan->rows;
   a.dv = d.v_dim;
   a.fixed = plan->fixed ? 1 : 0;
+  a.max_splits = plan->max_group_splits;
   cudaError_t e = launch_combine(a, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the combine kernel");
   return SPLITKV_OK;

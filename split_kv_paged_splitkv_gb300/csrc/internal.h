@@ -52,6 +52,7 @@ struct splitkv_plan_s {
   std::vector<int32_t> items;   // n_items * SPLITKV_ITEM_FIELDS, launch order
   std::vector<int32_t> groups;  // n_groups * kGroupFields, (b, h_kv) order
   int32_t n_items = 0, n_groups = 0, n_slots = 0, rows = 0, n_ctas = 0;
+  int32_t max_group_splits = 0;  // largest S of a combine group (0: no group)
   // workspace byte offsets
   size_t off_status = 0, off_items = 0, off_groups = 0, off_seqlens = 0, off_tickets = 0;
   size_t off_log = 0, off_lse = 0, off_o = 0, upload_bytes = 0, total = 0;
@@ -98,6 +99,7 @@ struct DecodeArgs {
   const float* v_scale;  //   kernel multiplies qk_scale_log2 / o_scale by them
   int32_t fixed;         // 1: the work list was written by a kernel (read it after the
                          //    dependency wait); items with NSPLIT = 0 are unused
+  int32_t max_splits;    // largest S of a combine group (sizes the combine kernel's loads)
   int32_t deep_ring;     // 1: at most one CTA per SM, so the GQA kernel may take the
                          //    deeper (four-stage) ring instead of sharing the SM
 };

@@ -83,6 +83,14 @@ static_assert(Mla::SMEM <= 227 * 1024, "shared memory budget");
 
 constexpr float kLn2m = 0.6931471805599453f;
 
+// Where a CTA gave up on a timed-out wait, for the per-CTA log: the first
+// site recorded wins.  (role << 24) | (x << 12) | y with role 1 the N-ring
+// producer, 2 the V-ring producer, 3 the V producer of a separate V tensor
+// (y = block), 4 the MMA issuer (bit 23: the N-ring half of QK(x) issued;
+// x = next QK block, y = next PV block), 5 the softmax warps (x = 1 waiting
+// for S, 2 for PV(y - 1) before a rescale; y = block), 6 the epilogue.
+__device__ __forceinline__ void note_abort(int* site, int code) { atomicCAS(site, 0, code); }
+
 // Barrier slots (8 bytes each) after OFF_BAR.
 enum {
   B_QFULL = 0,                      // Q written to TMEM and shared memory (128 threads)
@@ -93,8 +101,12 @@ enum {
   B_SFULL = B_VEMPTY + Mla::NST,    // [2] S_b complete
   B_PFULL = B_SFULL + 2,            // [2] P written over S_b (128); one barrier per
                                     // buffer, so no barrier runs two phases ahead
-  B_PFREE = B_PFULL + 2,            // PV done (P read, O stable)
-  B_DONE,                           // every MMA this CTA issued has completed
+  B_PFREE = B_PFULL + 2,            // [2] PV(j) done for j % 2 = b: P read out of S_b,
+                                    // O stable.  One barrier per buffer: QK(j) waits
+                                    // for PV(j - 2), and with a single barrier PV(j - 2)
+                                    // and PV(j - 1) could both complete before that test,
+                                    // leaving the barrier two phases ahead of it
+  B_DONE = B_PFREE + 2,             // every MMA this CTA issued has completed
   B_XKDONE,                         // [NST] separate V: the score MMAs have read the
                                     // key chunks of V slot s
   B_VDATA = B_XKDONE + Mla::NST,    // [NST] separate V: V rows landed in V slot s
@@ -155,6 +167,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     mbar_init(bar(B_PFULL), 128);
     mbar_init(bar(B_PFULL + 1), 128);
     mbar_init(bar(B_PFREE), 1);
+    mbar_init(bar(B_PFREE + 1), 1);
     mbar_init(bar(B_DONE), 1);
     if (SEPV) {
       for (int s = 0; s < C::NST; ++s) {
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     }
     if (!ok && lane == 0) {
       atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
+      note_abort(abort_flag, ((vring ? 2 : 1) << 24) | (issued & 0xfff));
     }
     // stay until every issued copy has landed
     if (lane == 0) {
@@ -267,7 +280,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     }
     if (!ok && lane == 0) {
       atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
+      note_abort(abort_flag, (3 << 24) | (issued & 0xfff));
     }
     // stay until every issued copy has landed
     if (lane == 0) {
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
                             (jp | kin) != 0);
         }
         umma_commit_warp(bar(B_VEMPTY + vs));
-        umma_commit_warp(bar(B_PFREE));
+        umma_commit_warp(bar(B_PFREE + (jp & 1)));
         __syncwarp();
         ++jp;
         t_idle = clock64();
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
         const bool rdy = __shfl_sync(
             kFull,
             mbar_test(bar(B_NFULL + qs), (jq / C::NST) & 1) &&
-                (jq < 2 || mbar_test(bar(B_PFREE), (jq - 2) & 1)),
+                (jq < 2 || mbar_test(bar(B_PFREE + (jq & 1)), ((jq - 2) >> 1) & 1)),
             0);
         if (rdy) {
           tc_fence_after();
@@ -372,7 +385,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     }
     if (!ok && lane == 0) {
       atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
+      note_abort(abort_flag, (4 << 24) | (qk_half ? 1 << 23 : 0) | ((jq & 0x7ff) << 12) | (jp & 0xfff));
     }
     // every MMA issued above completes before TMEM can be released
     umma_commit_warp(bar(B_DONE));
@@ -420,10 +433,14 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
 
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    int fail_at = 0;  // (wait kind << 12) | block, for the abort record
     for (int j = 0; j < nblk && ok; ++j) {
       const uint32_t scol = C::S_COL + uint32_t(64 * (j & 1));
       ok = __all_sync(kFull, mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1));
-      if (!ok) break;
+      if (!ok) {
+        fail_at = (1 << 12) | (j & 0xfff);
+        break;
+      }
       tc_fence_after();
       float s[64];
       {
@@ -476,8 +493,12 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
       }
       // O may only be rescaled once PV(j-1) has finished accumulating into it
       if (__any_sync(kFull, rescale_o)) {
-        if (j >= 1) ok = __all_sync(kFull, mbar_wait(bar(B_PFREE), (j - 1) & 1));
-        if (!ok) break;
+        if (j >= 1)
+          ok = __all_sync(kFull, mbar_wait(bar(B_PFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1));
+        if (!ok) {
+          fail_at = (2 << 12) | (j & 0xfff);
+          break;
+        }
         tc_fence_after();
         for (int c0 = 0; c0 < 256; c0 += 32) {
           float o[32];
@@ -495,7 +516,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     }
     if (!ok) {
       atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
+      note_abort(abort_flag, (5 << 24) | fail_at);
     }
 
     // ---- epilogue: O / l for this CTA's 256 V columns
@@ -503,8 +524,14 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     float lse_n = -INFINITY;
     if (l > 0.f) lse_n = (m_ref + lg2(l)) * kLn2m;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const bool have_o = ok && nblk > 0 &&
-                        __all_sync(kFull, mbar_wait(bar(B_PFREE), (nblk - 1) & 1));
+    bool have_o = ok && nblk > 0;
+    // PV(nblk - 1) complete (its commit covers every earlier MMA, PV(nblk - 2) too)
+    if (have_o && !__all_sync(kFull, mbar_wait(bar(B_PFREE + ((nblk - 1) & 1)),
+                                               ((nblk - 1) >> 1) & 1))) {
+      have_o = false;
+      atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+      note_abort(abort_flag, 6 << 24);
+    }
     if (have_o) tc_fence_after();
     const size_t out_row = (size_t(b) * a.T + t) * a.Hq + r;
     for (int c0 = 0; c0 < 256; c0 += 32) {

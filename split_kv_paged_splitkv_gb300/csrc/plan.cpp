@@ -180,6 +180,9 @@ void build_plan(splitkv_plan_s* p) {
   }
   p->n_groups = static_cast<int32_t>(p->groups.size() / kGroupFields);
   p->n_slots = slots;
+  p->max_group_splits = 0;
+  for (int32_t g = 0; g < p->n_groups; ++g)
+    p->max_group_splits = std::max(p->max_group_splits, p->groups[size_t(g) * kGroupFields + 2]);
 
   struct Item {
     int32_t f[SPLITKV_ITEM_FIELDS];
@@ -235,6 +238,7 @@ void build_fixed_plan(splitkv_plan_s* p) {
     }
   p->n_groups = static_cast<int32_t>(p->groups.size() / kGroupFields);
   p->n_slots = S > 1 ? p->n_items : 0;
+  p->max_group_splits = S > 1 ? S : 0;  // the refresh kernel writes S_b <= S
   layout_workspace(p);
 }
 

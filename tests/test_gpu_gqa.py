@@ -330,7 +330,8 @@ def test_seq_len_mismatch_is_reported():
     assert status & skv.SPLITKV_DEVERR_SEQLEN
 
 
-@pytest.mark.parametrize("S,R,D", [(200, 3, 512), (70, 2, 96), (1, 4, 128), (64, 5, 128)])
+@pytest.mark.parametrize("S,R,D", [(200, 3, 512), (70, 2, 96), (1, 4, 128), (64, 5, 128),
+                                   (16, 6, 512), (17, 3, 128), (12, 768, 512)])
 def test_combine_many_parts_and_widths(S, R, D):
     """More splits than one load round covers (running maximum across chunks),
     V widths that are not a multiple of 128, a single part, and -inf rows."""
