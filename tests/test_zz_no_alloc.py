@@ -4,10 +4,11 @@ plugins that may not allocate after start-up, real-time loops that must not
 stall on an allocation).  It keeps its workspace in a fixed 16 MiB device array
 inside the library instead of a caller buffer.
 
-The GPU test calls it through the C-ABI twice in a row (a different workload
-each time, so the second call must not see the first call's work list or
-tickets) and compares each result with splitkv_decode's on a caller workspace,
-within the bars the other parity tests use.  The file sorts last so that a run
+The GPU test calls it through the C-ABI on four workloads in a row (bf16 GQA,
+e4m3 GQA in NHD pages, MLA with a separate V tensor; each call must not see
+the previous call's work list or tickets) and compares each result with
+splitkv_decode's on a caller workspace, within the bars the other parity
+tests use.  The file sorts last so that a run
 stopping at the first failure has already run every other test.
 """
 import numpy as np
@@ -35,9 +36,17 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_decode_on_two_calls():
     need_gpu()
-    cases = [(workloads.WORKLOADS["gqa_ctx5900"], 0), (workloads.WORKLOADS["tiny_gqa_ctx260"], 4)]
-    for w, splits in cases:
-        x = workloads.make_inputs(w, device="cuda")
+    cases = [
+        (workloads.WORKLOADS["gqa_ctx5900"], 0, "HND"),
+        (workloads.WORKLOADS["tiny_gqa_ctx260"], 4, "HND"),
+        # an e4m3 cache in NHD pages, and an MLA decode with a separate V tensor
+        (workloads.Workload("noalloc_e4m3", 3, 1, 32, 4, 128, 128, 16, "fp8_e4m3",
+                            "list:500:1200:33", pool_slack=0.5, seed=61), 0, "NHD"),
+        (workloads.Workload("noalloc_mla", 1, 2, 128, 1, 576, 512, 64, "bf16", "list:700",
+                            std=0.5, v_shares_k=False, pool_slack=0.5, seed=62), 3, "HND"),
+    ]
+    for w, splits, layout in cases:
+        x = workloads.make_inputs(w, device="cuda", layout=layout)
         ref = session(x, splits)
         ref_out, ref_lse = ref.run()
         ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
