@@ -31,10 +31,10 @@ def _gqa(lens, G=8, Hkv=2, T=1, P=16, fp8=False, seed=3):
         "list:" + ":".join(str(int(x)) for x in lens), pool_slack=0.5, seed=seed)
 
 
-def _mla(lens, T=2, seed=5):
+def _mla(lens, T=2, seed=5, v_shares_k=True):
     return workloads.Workload("fixed_mla", len(lens), T, 128, 1, 576, 512, 64, "bf16",
                               "list:" + ":".join(str(int(x)) for x in lens), std=0.5,
-                              v_shares_k=True, pool_slack=0.5, seed=seed)
+                              v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
 
 def _session(x, S, mode=skv.SPLITKV_COMBINE_SEPARATE, lens_dev=None):
@@ -103,9 +103,10 @@ def test_one_graph_serves_changing_lengths(mode, T, G):
         assert s.stats()[1] == 0
 
 
-def test_mla_capacity_plan():
+@pytest.mark.parametrize("v_shares_k", [True, False])
+def test_mla_capacity_plan(v_shares_k):
     cap = [64 * 9 + 5, 64 * 3, 2]
-    x = workloads.make_inputs(_mla(cap), device="cuda")
+    x = workloads.make_inputs(_mla(cap, v_shares_k=v_shares_k), device="cuda")
     lens_dev = x.seq_lens.clone()
     s = _session(x, 4, lens_dev=lens_dev)
     for lens in (cap, [64 * 2 + 1, 64 * 3, 0]):
