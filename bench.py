@@ -72,8 +72,8 @@ def parse():
     ap.add_argument("--workload", default="gqa_ctx5900", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--splits", type=int, default=0, help="num_splits (0 = planner)")
     ap.add_argument("--fixed", action="store_true",
-                    help="capacity plan refreshed on the device every step (needs --splits; "
-                         "the refresh kernel is inside the timed region)")
+                    help="capacity plan whose kernels derive the items from the device "
+                         "lengths every step (needs --splits)")
     ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
     ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"],
                     help="page layout of the KV pools: [N][Hkv][P][D] or [N][P][Hkv][D]")
@@ -291,7 +291,7 @@ def run_ours(args, rank, world, local):
                          kv_layout=skv.SPLITKV_LAYOUT_NHD if args.layout == "nhd" else skv.SPLITKV_LAYOUT_HND)
     items = skv.splitkv_plan_get_items(sess.plan)
     n_groups = len(np.unique(items[items[:, 3] > 1][:, 7])) if len(items) else 0
-    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan) + (1 if args.fixed else 0)
+    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan)
 
     # rotating KV pools: total > 4x L2
     props = torch.cuda.get_device_properties(dev)
@@ -409,9 +409,8 @@ def run_ours(args, rank, world, local):
                    and args.layout == "hnd")
     traffic, traffic_src = PROFILED_TRAFFIC.get(w.name, (None, None)) if default_cfg else (None, None)
     roof.update({"traffic": traffic, "traffic_source": traffic_src,
-                 "duration_basis": ("split-KV kernel alone (splitkv_decode_partials"
-                                    + (", after the plan refresh kernel" if args.fixed else "")
-                                    + "), CUDA-graph replay, CUDA events on the launching stream"
+                 "duration_basis": ("split-KV kernel alone (splitkv_decode_partials), CUDA-graph "
+                                    "replay, CUDA events on the launching stream"
                                     if kernel_us is not None else
                                     "timed-region time per call (the split kernel is the only launch)"),
                  "kernel_us": launch_us, "step_us": us_per_call_local,
@@ -430,7 +429,7 @@ def run_ours(args, rank, world, local):
                    "context": w.lens, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
                    "kv_layout": args.layout.upper(),
                    "num_splits": args.splits, "planned_items": int(len(items)),
-                   "plan": "capacity plan, refreshed on the device each step" if args.fixed else "host",
+                   "plan": "capacity plan, items derived from the device lengths each step" if args.fixed else "host",
                    "combine": args.combine, "parallelism": f"replicas{world}",
                    "l2": f"inputs rotate over {R} KV pools ({R * pool_bytes / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
                    "timing": "CUDA-graph replay of back-to-back calls, CUDA events on the launching stream"},

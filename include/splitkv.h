@@ -150,13 +150,16 @@ splitkv_status splitkv_plan(const splitkv_desc_t* desc, const int32_t* seq_lens_
  * split attention was enabled for one captured shape only).  The plan holds
  * num_splits work items for every (sequence, KV-head group) -- B * Hkv /
  * heads_per_item * num_splits items, in (b, head group, s) order -- and one
- * combine group per (sequence, head group) when num_splits > 1.  Before each
- * decode, splitkv_plan_refresh rewrites the work list on the device from the
- * current lengths: with S_b = min(num_splits, ceil(L_b / P)) (1 for L_b == 0),
- * items s < S_b get the page ranges splitkv_plan gives for this num_splits,
- * and the others are marked unused (SPLITKV_ITEM_NSPLIT = 0): their CTAs are
- * launched and exit at once, logging 0 keys.  splitkv_plan_get_items returns
- * the all-unused template; splitkv_read_items reads the live list.
+ * combine group per (sequence, head group) when num_splits > 1.  Each decode
+ * derives every item from the device lengths it is given (after its
+ * dependency wait, so a preceding kernel may write them): with S_b =
+ * min(num_splits, ceil(L_b / P)) (1 for L_b == 0), items s < S_b get the page
+ * ranges splitkv_plan gives for this num_splits, and the others are unused:
+ * their CTAs are launched and exit at once, logging 0 keys.  A length outside
+ * [0, max_pages_per_seq * P] or below q_tokens (and not 0) sets
+ * SPLITKV_DEVERR_SEQLEN in the status word and the sequence is served as
+ * empty (out = 0, lse = -inf).  splitkv_plan_get_items returns the all-unused
+ * template; splitkv_plan_refresh + splitkv_read_items show the live list.
  *   num_splits  1..64
  * EINVAL for bad arguments; EUNSUPPORTED for shapes no kernel serves.
  */
@@ -164,14 +167,13 @@ splitkv_status splitkv_plan_fixed(const splitkv_desc_t* desc, int32_t num_splits
                                   splitkv_plan_t** plan_out);
 
 /*
- * splitkv_plan_refresh -- one small kernel on `stream` that writes the work
- * list of a capacity plan into `workspace` (uploaded once with
- * splitkv_plan_upload) from seq_lens (device, int32 [B]); capturable in a CUDA
- * graph together with splitkv_decode.  A length outside [0, max_pages_per_seq
- * * P] or below q_tokens (and not 0) sets SPLITKV_DEVERR_SEQLEN in the status
- * word and the sequence is served as empty (out = 0, lse = -inf).
- * EINVAL if the plan was not made by splitkv_plan_fixed or for NULL or
- * misaligned pointers.
+ * splitkv_plan_refresh -- one small kernel on `stream` that writes into
+ * `workspace` (uploaded once with splitkv_plan_upload) the work list and the
+ * combine-group table a decode of this capacity plan derives from seq_lens
+ * (device, int32 [B]), for inspection with splitkv_read_items.  A decode does
+ * not need it: the kernels derive the same items themselves.  Invalid
+ * lengths are reported as splitkv_plan_fixed describes.  EINVAL if the plan
+ * was not made by splitkv_plan_fixed or for NULL or misaligned pointers.
  */
 splitkv_status splitkv_plan_refresh(const splitkv_plan_t* plan, void* workspace,
                                     const int32_t* seq_lens, void* stream);

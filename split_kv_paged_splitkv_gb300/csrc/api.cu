@@ -398,6 +398,8 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   a.v_scale = v_scale;
   a.fixed = plan->fixed ? 1 : 0;
   a.max_splits = plan->max_group_splits;
+  a.hpi = heads_per_item(d);
+  if (plan->fixed) a.fx = fixed_shape(*plan, seq_lens);
   a.fused = merge && d.combine_mode == SPLITKV_COMBINE_FUSED;
   a.deep_ring = plan->n_items <= plan->num_sms ? 1 : 0;
 
@@ -424,7 +426,6 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
     return SPLITKV_OK;
   }
   TmaDesc tk, tv;
-  a.hpi = heads_per_item(d);
   const bool nhd = d.kv_layout == SPLITKV_LAYOUT_NHD;
   splitkv_status st =
       make_gqa_map(&tk, k_pages, fp8, d.page_size, d.num_kv_heads, d.num_pages_total, a.hpi, nhd);

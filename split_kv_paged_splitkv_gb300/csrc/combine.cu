@@ -49,8 +49,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   launch_dependents();
   // The group table of a host plan is uploaded with the plan and never
   // written by a kernel: it is read before waiting for the split kernel, off
-  // the critical path.  A capacity plan's table is written by the refresh
-  // kernel, and a group with S = 0 has nothing to merge.
+  // the critical path.  A capacity plan's table is written by the split
+  // kernel (the first item of each group), and a group with S = 0 has
+  // nothing to merge.
   if (fixed && pdl) wait_prerequisites();
   static_assert(WAYS == 1 || WAYS == kWays, "ways");
   constexpr int RPC = kCombineThreads / 32 / WAYS;  // rows per CTA

@@ -39,6 +39,7 @@
 
 #include <cfloat>
 
+#include "fixed_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -258,6 +259,34 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, int tid, int b,
   if (d0 == 0 && a.lse) a.lse[row] = lse_n;
 }
 
+// L2 prefetches of the tiles an item's ring takes first, issued by the
+// producer warp while the previous kernel on the stream finishes (only in a
+// one-wave grid, whose CTAs all start early; later waves of a larger grid
+// start with nothing to overlap, measured 0.5-1 % slower): one lane per tile
+// reads its block-table entry speculatively (a relaxed load; the previous
+// kernel may still be writing the table) and prefetches its K and V boxes.
+// A stale entry only warms the wrong page; the copies proper are issued after
+// the dependency wait from entries read again.
+template <class C, bool FP8>
+__device__ __forceinline__ void prefetch_first_tiles(const DecodeArgs& a, const CUtensorMap* tk,
+                                                     const CUtensorMap* tv, int b, int h0,
+                                                     int k_begin, int n_tiles, int lane) {
+  const int t = lane;
+  if (t >= n_tiles || t >= C::NST * C::TPS) return;
+  const int key0 = k_begin + t * 16;
+  const int page = key0 / a.P;
+  const int ph = ld_relaxed_gpu(a.block_table + size_t(b) * a.max_pages + page);
+  if (ph < 0 || ph >= a.num_pages) return;
+  const int kp = key0 - page * a.P;
+  if (FP8) {
+    tma_prefetch_4d(tk, 0, kp, h0, ph);
+    tma_prefetch_4d(tv, 0, kp, h0, ph);
+  } else {
+    tma_prefetch_5d(tk, 0, kp, 0, h0, ph);
+    tma_prefetch_5d(tv, 0, kp, 0, h0, ph);
+  }
+}
+
 template <bool FP8, int HPI, int NRG, int NST>
 __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerSm)
     gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
@@ -272,8 +301,20 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   int* pt = misc + 16;                                 // staged block-table entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (a.fixed) wait_prerequisites();  // the work list was written by the refresh kernel
-  const int32_t* it = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
+  // A capacity plan's item is derived from the device lengths (read after the
+  // dependency wait); a host plan's comes from the uploaded work list.
+  int32_t it[SPLITKV_ITEM_FIELDS];
+  int L_fixed = 0;
+  if (a.fixed) {
+    wait_prerequisites();
+    bool bad;
+    fixed_item(a.fx, blockIdx.x, it, &L_fixed, &bad);
+    if (threadIdx.x == 0) fixed_write_group(a.fx, const_cast<int32_t*>(a.groups), it);
+  } else {
+    const int32_t* src = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
+#pragma unroll
+    for (int k = 0; k < SPLITKV_ITEM_FIELDS; ++k) it[k] = src[k];
+  }
   const int b = it[SPLITKV_ITEM_B], h0 = it[SPLITKV_ITEM_HKV];  // heads h0 .. h0+HPI-1
   const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
   const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
@@ -310,37 +351,12 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   // The plan's copy of the sequence length (uploaded with the work list, never
   // written by a kernel) is read before the wait; the caller's device copy is
   // only checked against it, off the critical path.
-  const int L = a.plan_lens[b];
+  const int L = a.fixed ? L_fixed : a.plan_lens[b];
   const int k_begin = p0 * a.P;
   const int k_end = min(p1 * a.P, L);
   const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
-  if (a.deep_ring && !a.fixed && warp == C::NCW) {
-    // While the previous kernel on the stream finishes, warm L2 (and the
-    // address translations) with the tiles the ring takes first (only in a
-    // one-wave grid, whose CTAs all start early; later waves of a larger
-    // grid start with nothing to overlap, measured 0.5-1 % slower): one lane
-    // per tile reads its block-table entry speculatively (a relaxed load; the
-    // previous kernel may still be writing the table) and issues L2
-    // prefetches of its K and V boxes.  A stale entry only warms the wrong
-    // page; the copies proper are issued after the dependency wait from the
-    // entries read again.
-    const int t = lane;
-    if (t < n_tiles && t < C::NST * C::TPS) {
-      const int key0 = k_begin + t * 16;
-      const int page = key0 / a.P;
-      const int ph = ld_relaxed_gpu(a.block_table + size_t(b) * a.max_pages + page);
-      if (ph >= 0 && ph < a.num_pages) {
-        const int kp = key0 - page * a.P;
-        if (FP8) {
-          tma_prefetch_4d(&tk, 0, kp, h0, ph);
-          tma_prefetch_4d(&tv, 0, kp, h0, ph);
-        } else {
-          tma_prefetch_5d(&tk, 0, kp, 0, h0, ph);
-          tma_prefetch_5d(&tv, 0, kp, 0, h0, ph);
-        }
-      }
-    }
-  }
+  if (a.deep_ring && !a.fixed && warp == C::NCW)
+    prefetch_first_tiles<C, FP8>(a, &tk, &tv, b, h0, k_begin, n_tiles, lane);
   __syncthreads();
   launch_dependents();
   wait_prerequisites();

@@ -75,6 +75,18 @@ splitkv_status fail(splitkv_status s, const char* fmt, ...);
 
 // ----------------------------------------------------------------- kernels
 
+// Shape of a capacity plan's work list, from which the kernels derive each
+// item and combine group from the device lengths (fixed_plan.cuh).
+struct FixedShape {
+  const int32_t* seq_lens;  // device lengths [B], read after the dependency wait
+  int32_t S;                // items per (sequence, head group)
+  int32_t U;                // head groups per sequence (Hkv / heads per item)
+  int32_t hpi;              // KV heads per item
+  int32_t P;                // page size
+  int32_t T;                // query tokens
+  int64_t cap;              // max_pages_per_seq * P
+};
+
 struct DecodeArgs {
   const int32_t* items;
   const int32_t* groups;
@@ -100,6 +112,7 @@ struct DecodeArgs {
   int32_t fixed;         // 1: the work list was written by a kernel (read it after the
                          //    dependency wait); items with NSPLIT = 0 are unused
   int32_t max_splits;    // largest S of a combine group (sizes the combine kernel's loads)
+  FixedShape fx;         // capacity plans: the kernels derive items and groups from it
   int32_t deep_ring;     // 1: at most one CTA per SM, so the GQA kernel may take the
                          //    deeper (four-stage) ring instead of sharing the SM
 };
@@ -115,6 +128,8 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
 // columns of the key rows
 cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, void* stream);
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
+// The FixedShape of a capacity plan over device lengths `seq_lens`.
+FixedShape fixed_shape(const splitkv_plan_s& p, const int32_t* seq_lens);
 cudaError_t launch_refresh(const splitkv_plan_s& p, void* workspace, const int32_t* seq_lens,
                            void* stream);
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,

@@ -47,6 +47,7 @@
 // shared latent row; each V-ring slot is filled twice per use.
 #include <cuda_runtime.h>
 
+#include "fixed_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -137,8 +138,22 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
   const int item = pair / a.T;
   const int t = pair - item * a.T;
 
-  if (a.fixed) wait_prerequisites();  // the work list was written by the refresh kernel
-  const int32_t* it = a.items + size_t(item) * SPLITKV_ITEM_FIELDS;
+  // A capacity plan's item is derived from the device lengths (read after the
+  // dependency wait); a host plan's comes from the uploaded work list.
+  int32_t it[SPLITKV_ITEM_FIELDS];
+  int L_fixed = 0;
+  if (a.fixed) {
+    wait_prerequisites();
+    bool bad;
+    fixed_item(a.fx, item, it, &L_fixed, &bad);
+    // one CTA of the item (token 0, V half 0) writes its group's entry
+    if (threadIdx.x == 0 && blockIdx.x % (2 * a.T) == 0)
+      fixed_write_group(a.fx, const_cast<int32_t*>(a.groups), it);
+  } else {
+    const int32_t* src = a.items + size_t(item) * SPLITKV_ITEM_FIELDS;
+#pragma unroll
+    for (int k = 0; k < SPLITKV_ITEM_FIELDS; ++k) it[k] = src[k];
+  }
   const int b = it[SPLITKV_ITEM_B];
   const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
   const int slot = it[SPLITKV_ITEM_SLOT];
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // plan's sequence length (uploaded, never written by a kernel): read before the wait
-  const int L = a.plan_lens[b];
+  const int L = a.fixed ? L_fixed : a.plan_lens[b];
   const int k_begin = p0 * C::BK;
   const int k_end = min(p1 * C::BK, L);
   const int nblk = k_end > k_begin ? (k_end - k_begin + C::BK - 1) / C::BK : 0;

@@ -76,11 +76,7 @@ extern "C" splitkv_status splitkv_decode_noalloc(const splitkv_plan_t* plan, con
   // word: the array still holds whatever the previous call left there.
   st = splitkv_plan_upload(plan, scratch, kNoAllocScratchBytes, stream);
   if (st != SPLITKV_OK) return st;
-  // a capacity plan's work list comes from the device lengths
-  if (plan->fixed) {
-    st = splitkv_plan_refresh(plan, scratch, seq_lens, stream);
-    if (st != SPLITKV_OK) return st;
-  }
+  // (a capacity plan's items are derived from the device lengths by the kernels)
   return splitkv_decode(plan, scratch, q, k_pages, v_pages, block_table, seq_lens, num_splits,
                         scale, kv_scale, out, lse, stream);
 }

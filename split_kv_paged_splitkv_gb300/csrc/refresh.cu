@@ -12,64 +12,80 @@
 // fixed places: group g = b * U + u owns slots [g S, g S + S).
 #include <cuda_runtime.h>
 
+#include "fixed_plan.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace splitkv {
 namespace {
 
-__global__ void refresh_kernel(const int32_t* __restrict__ seq_lens, int32_t* items, int32_t* groups,
-                               int32_t* plan_lens, int32_t* status, int B, int U, int hpi, int S,
-                               int P, int T, int64_t cap) {
+using namespace ptx;
+
+__global__ void refresh_kernel(const FixedShape f, int n_items, int32_t* items, int32_t* groups,
+                               int32_t* plan_lens, int32_t* status) {
+  // Programmatic dependent launch: a following kernel may start its prologue
+  // now; this kernel rewrites the work list only once the previous kernel on
+  // the stream (which may still read it) has finished.
+  launch_dependents();
+  wait_prerequisites();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= B * U * S) return;
-  const int s = i % S, u = (i / S) % U, b = i / (S * U);
-  int L = seq_lens[b];
-  if (L < 0 || int64_t(L) > cap || (L > 0 && L < T)) {
-    // not a length the plan can serve: the sequence is treated as empty
-    if (s == 0 && u == 0) atomicOr(status, SPLITKV_DEVERR_SEQLEN);
-    L = 0;
-  }
-  const int n = (L + P - 1) / P;
-  const int Sb = n > 0 ? min(S, n) : 1;
-  const int g = b * U + u;
-  const bool split = Sb > 1;
-  int32_t f[SPLITKV_ITEM_FIELDS] = {b, u * hpi, s, 0, 0, 0, -1, -1};
-  if (s < Sb) {
-    f[SPLITKV_ITEM_NSPLIT] = Sb;
-    f[SPLITKV_ITEM_PAGE0] = n > 0 ? int32_t((int64_t(s) * n) / Sb) : 0;
-    f[SPLITKV_ITEM_PAGE1] = n > 0 ? int32_t((int64_t(s + 1) * n) / Sb) : 0;
-    f[SPLITKV_ITEM_SLOT] = split ? g * S + s : -1;
-    f[SPLITKV_ITEM_GROUP] = split ? g : -1;
-  }
-  int32_t* it = items + size_t(i) * SPLITKV_ITEM_FIELDS;
+  if (i >= n_items) return;
+  int32_t it[SPLITKV_ITEM_FIELDS];
+  int L;
+  bool bad;
+  fixed_item(f, i, it, &L, &bad);
+  const int s = it[SPLITKV_ITEM_SPLIT], u = it[SPLITKV_ITEM_HKV] / f.hpi, b = it[SPLITKV_ITEM_B];
+  if (bad && s == 0 && u == 0) atomicOr(status, SPLITKV_DEVERR_SEQLEN);
+  int32_t* dst = items + size_t(i) * SPLITKV_ITEM_FIELDS;
 #pragma unroll
-  for (int k = 0; k < SPLITKV_ITEM_FIELDS; ++k) it[k] = f[k];
+  for (int k = 0; k < SPLITKV_ITEM_FIELDS; ++k) dst[k] = it[k];
   if (s == 0 && groups) {
-    int32_t* gr = groups + size_t(g) * kGroupFields;
-    gr[0] = b;
-    gr[1] = u * hpi;
-    gr[2] = split ? Sb : 0;  // 0: nothing to merge (the split kernel wrote the output)
-    gr[3] = g * S;
+    int gb, ghkv, gS, slot0;
+    fixed_group(f, b * f.U + u, &gb, &ghkv, &gS, &slot0);
+    int32_t* gr = groups + size_t(b * f.U + u) * kGroupFields;
+    gr[0] = gb;
+    gr[1] = ghkv;
+    gr[2] = gS;  // 0: nothing to merge (the split kernel wrote the output)
+    gr[3] = slot0;
   }
   if (s == 0 && u == 0) plan_lens[b] = L;
 }
 
 }  // namespace
 
+FixedShape fixed_shape(const splitkv_plan_s& p, const int32_t* seq_lens) {
+  const splitkv_desc_t& d = p.desc;
+  const int hpi = heads_per_item(d);
+  FixedShape f;
+  f.seq_lens = seq_lens;
+  f.S = p.num_splits;
+  f.U = d.num_kv_heads / hpi;
+  f.hpi = hpi;
+  f.P = d.page_size;
+  f.T = d.q_tokens;
+  f.cap = int64_t(d.max_pages_per_seq) * d.page_size;
+  return f;
+}
+
 cudaError_t launch_refresh(const splitkv_plan_s& p, void* workspace, const int32_t* seq_lens,
                            void* stream) {
-  const splitkv_desc_t& d = p.desc;
   if (p.n_items == 0) return cudaSuccess;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  const int hpi = heads_per_item(d);
   const int threads = 128, blocks = (p.n_items + threads - 1) / threads;
-  refresh_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      seq_lens, reinterpret_cast<int32_t*>(ws + p.off_items),
-      p.n_groups ? reinterpret_cast<int32_t*>(ws + p.off_groups) : nullptr,
-      reinterpret_cast<int32_t*>(ws + p.off_seqlens), reinterpret_cast<int32_t*>(ws + p.off_status),
-      d.batch, d.num_kv_heads / hpi, hpi, p.num_splits, d.page_size, d.q_tokens,
-      int64_t(d.max_pages_per_seq) * d.page_size);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, refresh_kernel, fixed_shape(p, seq_lens), p.n_items,
+                            reinterpret_cast<int32_t*>(ws + p.off_items),
+                            p.n_groups ? reinterpret_cast<int32_t*>(ws + p.off_groups) : nullptr,
+                            reinterpret_cast<int32_t*>(ws + p.off_seqlens),
+                            reinterpret_cast<int32_t*>(ws + p.off_status));
 }
 
 }  // namespace splitkv

@@ -40,8 +40,8 @@ class DecodeSession:
                               SPLITKV_FP8_E4M3 if fp8 else SPLITKV_BF16, int(v_shares_k),
                               combine_mode, kv_layout)
         # fixed: a capacity plan (num_splits items per sequence and head group)
-        # whose work list run() rewrites on the device from the current
-        # seq_lens, so one captured CUDA graph serves any lengths
+        # whose kernels derive every item from the current device seq_lens,
+        # so one captured CUDA graph serves any lengths
         self.fixed = fixed
         self.plan = (splitkv_plan_fixed(self.desc, num_splits) if fixed else
                      splitkv_plan(self.desc, seq_lens_host, num_splits, num_sms))
@@ -60,8 +60,6 @@ class DecodeSession:
         q, k, v, table, lens = tensors if tensors is not None else self.tensors
         o = self.out if out is None else out
         l = self.lse if lse is None else lse
-        if self.fixed:
-            splitkv_plan_refresh(self.plan, self.workspace, lens, self.stream)
         if self.k_scale is not None:
             splitkv_decode_kv_scales(self.plan, self.workspace, q, k, v, table, lens,
                                      self.num_splits, self.scale, self.k_scale, self.v_scale, o, l,
@@ -77,8 +75,6 @@ class DecodeSession:
         q, k, v, table, lens = tensors if tensors is not None else self.tensors
         o = self.out if out is None else out
         l = self.lse if lse is None else lse
-        if self.fixed:
-            splitkv_plan_refresh(self.plan, self.workspace, lens, self.stream)
         splitkv_decode_partials(self.plan, self.workspace, q, k, v, table, lens, self.num_splits,
                                 self.scale, self.kv_scale, o, l, self.stream)
         return o, l

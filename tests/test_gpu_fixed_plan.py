@@ -1,11 +1,13 @@
-"""GPU checks of capacity plans (splitkv_plan_fixed + splitkv_plan_refresh).
+"""GPU checks of capacity plans (splitkv_plan_fixed).
 
-* the work list the refresh kernel writes from device lengths equals the
-  oracle planner's for the same num_splits (every used item), and the unused
-  capacity items are marked and scored nothing;
+* the work items the decode kernels derive from the device lengths -- read
+  back through splitkv_plan_refresh / splitkv_read_items, which write the
+  same list, and through the per-CTA log of page ranges -- equal the oracle
+  planner's for the same num_splits (every used item), and the unused
+  capacity items are marked and score nothing;
 * decodes through a capacity plan match the fp64 oracle;
-* one captured CUDA graph (refresh + decode) replayed over changing device
-  lengths matches the oracle for each set of lengths.
+* one captured CUDA graph of decodes replayed over changing device lengths
+  matches the oracle for each set of lengths.
 """
 import numpy as np
 import pytest
@@ -60,7 +62,11 @@ def test_refreshed_work_list_equals_the_planner(fp8, Hkv, G):
     for S in (1, 4, 9):
         s = _session(x, S)
         s.run()
+        log, status = s.stats()
+        skv.splitkv_plan_refresh(s.plan, s.workspace, x.seq_lens)
         items = skv.splitkv_read_items(s.plan, s.workspace)
+        # the kernels iterated exactly the page ranges of the refreshed list
+        assert np.array_equal(log[:, 0], items[:, 4]) and np.array_equal(log[:, 1], items[:, 5])
         hpi = skv.splitkv_plan_heads_per_item(s.plan)
         U = Hkv // hpi
         assert items.shape[0] == len(lens) * U * S
@@ -73,7 +79,6 @@ def test_refreshed_work_list_equals_the_planner(fp8, Hkv, G):
             b, h, sp, Sb = it[:4]
             g = b * U + h // hpi
             assert it[6] == (g * S + sp if Sb > 1 else -1) and it[7] == (g if Sb > 1 else -1)
-        log, status = s.stats()
         assert status == 0
         assert (log[items[:, 3] == 0, 2] == 0).all()  # unused capacity items score nothing
         out, lse = s.out, s.lse
@@ -84,7 +89,7 @@ def test_refreshed_work_list_equals_the_planner(fp8, Hkv, G):
 @pytest.mark.parametrize("mode", [skv.SPLITKV_COMBINE_SEPARATE, skv.SPLITKV_COMBINE_FUSED])
 @pytest.mark.parametrize("T,G", [(1, 8), (2, 8)])
 def test_one_graph_serves_changing_lengths(mode, T, G):
-    """Capture refresh + decode once; change the device lengths; replay."""
+    """Capture the decode once; change the device lengths; replay."""
     cap = [16 * 30 + 3, 16 * 61, 16 * 9 + 7]
     x = workloads.make_inputs(_gqa(cap, G=G, T=T, seed=11), device="cuda")
     lens_dev = x.seq_lens.clone()

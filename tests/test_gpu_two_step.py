@@ -45,7 +45,11 @@ def _two_step_equals_decode(x, S, mode=skv.SPLITKV_COMBINE_SEPARATE, fixed=False
     two.lse.fill_(float("nan"))
     two.run_partials()
     # rows of single-split sequences are final after the partial pass alone
-    items = skv.splitkv_read_items(two.plan, two.workspace) if fixed else skv.splitkv_plan_get_items(two.plan)
+    if fixed:
+        skv.splitkv_plan_refresh(two.plan, two.workspace, x.seq_lens)
+        items = skv.splitkv_read_items(two.plan, two.workspace)
+    else:
+        items = skv.splitkv_plan_get_items(two.plan)
     single = sorted({int(b) for b, ns in zip(items[:, 0], items[:, 3]) if ns == 1})
     torch.cuda.synchronize()
     for b in single:
