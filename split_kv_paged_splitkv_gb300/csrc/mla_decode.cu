@@ -251,6 +251,16 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
       for (int k = 0; k < nchk; ++k)
         tma_load_2d_warp(smem_u32(ring + st * slot_bytes + k * C::K_CH), &tk, bar(full0 + st),
                          (vring ? v_chunk(h, k) : n_chunk(h, k)) * 64, y);
+      if (!vring) {
+        // The V-ring slot of block j is refilled only once PV(j - 2) is done,
+        // a few hundred cycles before the score MMAs need it, while this ring
+        // is refilled some 3,000 cycles earlier: warm L2 with block j's
+        // V-ring rows (and, with a separate V tensor, its V rows) now, so that
+        // copy hits L2 instead of waiting out a DRAM round trip.
+        for (int k = 0; k < C::NX; ++k) tma_prefetch_2d_warp(&tk, v_chunk(h, k) * 64, y);
+        if (SEPV)
+          for (int k = 0; k < C::NV; ++k) tma_prefetch_2d_warp(&tv, (4 * h + k) * 64, y);
+      }
       issued = j + 1;
     }
     if (!ok && lane == 0) {

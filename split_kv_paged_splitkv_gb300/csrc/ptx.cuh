@@ -120,6 +120,16 @@ __device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* m, int32_t c0
                : "memory");
 }
 
+// L2 prefetch of one 2-D box, issued by a converged warp (one elected lane).
+__device__ __forceinline__ void tma_prefetch_2d_warp(const CUtensorMap* m, int32_t x, int32_t y) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(x), "r"(y)
+      : "memory");
+}
+
 // Relaxed GPU-scope load: may run while another grid writes the word (it
 // returns the old or the new value).
 __device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* p) {
