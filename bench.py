@@ -416,6 +416,10 @@ def run_ours(args, rank, world, local):
                  "kernel_us": launch_us, "step_us": us_per_call_local,
                  "peak_kind": peak_kind, "algorithmic_bytes": nbytes})
 
+    # cold calls: L2 flushed (a buffer of twice its size written) before each
+    # call, events around the call only; the median of a few, for context
+    cold_us = run_cold(x, sess, l2, stream)
+
     # end to end: host buffers, copies inside the timed region
     e2e = run_e2e(args, x, sess, dev)
 
@@ -435,6 +439,7 @@ def run_ours(args, rank, world, local):
                    "timing": "CUDA-graph replay of back-to-back calls, CUDA events on the launching stream"},
         "roofline": roof,
         "nonempty_cta_fraction": nonempty,
+        "cold_us_per_call": cold_us,
         "gpu_launches": K * launches_per_step,
         "e2e": e2e,
         "clocks": clocks,
@@ -445,6 +450,29 @@ def run_ours(args, rank, world, local):
                                 "sample": oracle_sample_desc(w, n)}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_cold(x, sess, l2, stream, n=30):
+    """Median device µs of single calls that each start with a cold L2 (a
+    buffer of twice its size is written between calls).  The call is a
+    one-call CUDA graph, so the events time the GPU work, not the host's
+    enqueueing of an eager call."""
+    flush = torch.empty(2 * l2 // 4, dtype=torch.int32, device=x.q.device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sess.run()
+    times = []
+    for _ in range(n):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    del flush, g
+    return float(np.median(times))
 
 
 def run_e2e(args, x, sess, dev):

@@ -44,3 +44,4 @@ def test_bench_line_has_every_key():
     assert d["clocks"]["sm_max_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)
     assert d["gpu_launches"] == 400 * 2  # split kernel + combine kernel per call
     assert d["nonempty_cta_fraction"] == 1.0
+    assert d["cold_us_per_call"] > 0
