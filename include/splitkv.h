@@ -90,7 +90,8 @@ typedef struct splitkv_desc {
   int32_t num_kv_heads;       /* Hkv, divides Hq                                */
   int32_t qk_dim;             /* Dk: 128 (GQA) or 576 (MLA latent + rope)       */
   int32_t v_dim;              /* Dv: 128 (GQA) or 512 (MLA)                     */
-  int32_t page_size;          /* P tokens per page, multiple of 16              */
+  int32_t page_size;          /* P tokens per page, multiple of 16; MLA: 16, 32
+                                 or a multiple of 64                           */
   int32_t max_pages_per_seq;  /* row length of block_table                     */
   int32_t num_pages_total;    /* pages in k_pages / v_pages                     */
   int32_t kv_dtype;           /* splitkv_dtype; q and out are always bf16       */

@@ -123,7 +123,7 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
     return fail(SPLITKV_EUNSUPPORTED,
                 "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
                 "(GQA: qk_dim=v_dim=128, T*G<=16; MLA: 128 q heads, 1 bf16 latent head, "
-                "qk_dim=576, v_dim=512, page_size 64, T<=16)",
+                "qk_dim=576, v_dim=512, page_size 16, 32 or a multiple of 64, T<=16)",
                 d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
                 d->v_shares_k);
   return SPLITKV_OK;
@@ -144,7 +144,10 @@ Family family_of(const splitkv_desc_t& d) {
   if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 16) return Family::kGqa;
   // V either shares the latent rows (their first 512 columns) or is its own tensor
   if (d.qk_dim == 576 && d.v_dim == 512 && d.num_kv_heads == 1 &&
-      d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.page_size == 64 && d.q_tokens <= 16)
+      d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.q_tokens <= 16 &&
+      (64 % d.page_size == 0 || d.page_size % 64 == 0))
+    // 64-key blocks: 16- and 32-key pages fill one with 4 or 2 boxes, larger
+    // pages (multiples of 64) hold whole blocks
     return Family::kMla;
   return Family::kNone;
 }
@@ -410,10 +413,11 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
     // kernel's threads.  The partials are always merged by the separate
     // combine kernel.
     TmaDesc tk, tv;
-    splitkv_status st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, 64);
+    const int box_rows = d.page_size < 64 ? d.page_size : 64;
+    splitkv_status st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, box_rows);
     if (st != SPLITKV_OK) return st;
     if (!d.v_shares_k) {
-      st = make_bf16_map(&tv, v_pages, d.v_dim, rows_total, 64);
+      st = make_bf16_map(&tv, v_pages, d.v_dim, rows_total, box_rows);
       if (st != SPLITKV_OK) return st;
     }
     a.fused = 0;

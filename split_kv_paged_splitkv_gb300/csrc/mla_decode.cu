@@ -27,7 +27,10 @@
 // S is double-buffered; P is written over the first 32 columns of its own
 // S buffer, so the scores of block j + 1 accumulate while the softmax warps
 // work on block j, and the scores of block j + 2 wait only for PV(j).
-// Per 64-key block (one page):
+// Keys stream in blocks of 64.  A page of 16 or 32 keys fills a block chunk
+// with 4 or 2 TMA boxes of one page each; a page of 64 keys or a multiple of
+// 64 holds whole blocks (the split's first key is then a multiple of 64).
+// Per 64-key block:
 //   1. S_b = Q . K^T      (tcgen05, M=128 N=64 K=576, b = j % 2)
 //   2. softmax warps: online softmax with a lazy reference maximum (O is
 //      rescaled only when a row maximum grows by more than 2^8, after PV(j-1)
@@ -59,7 +62,7 @@ using namespace ptx;
 struct Mla {
   static constexpr int DK = 576, DV = 512;
   static constexpr int ROWS = 128;          // query heads of one token
-  static constexpr int BK = 64;             // keys per block (= one page)
+  static constexpr int BK = 64;             // keys per block
   static constexpr int NN = 4;              // N-ring chunks (query chunk in TMEM)
   static constexpr int NV = 4;              // V chunks of this CTA's half
   static constexpr int NX = NV + 1;         // V-ring chunks: the V chunks and the rope chunk
@@ -119,7 +122,57 @@ static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 __device__ __forceinline__ int n_chunk(int h, int i) { return h == 0 ? 4 + i : i; }
 __device__ __forceinline__ int v_chunk(int h, int k) { return k < 4 ? 4 * h + k : 8; }
 
-template <bool SEPV>
+// Page walk of a producer warp over its split's 64-key blocks.  Pages of
+// 64 keys or a multiple of 64 hold whole blocks: a block is one box at row
+// offset `off` of page `pg`.  Pages of 16 or 32 keys (SMALLP) take 4 or 2
+// boxes per block chunk, one page each.  The warp holds the physical ids of
+// pages chunk0 + lane (0 past the split's last page p1, whose keys are
+// masked anyway) and refreshes them when a block reaches past that window.
+// No division: the walk advances by whole pages or by 64 rows.
+template <bool SMALLP>
+struct PageWalk {
+  static constexpr int NB = SMALLP ? 4 : 1;  // boxes per block chunk, at most
+  int pg, off = 0, chunk0 = -32, phys = 0;
+
+  __device__ __forceinline__ explicit PageWalk(int p0) : pg(p0) {}
+
+  // First rows (the MLA cache has one KV head) of the current block's boxes;
+  // with pages of 32 keys y[2], y[3] repeat y[1].  `report` flags
+  // out-of-range page ids.
+  __device__ __forceinline__ void rows(const DecodeArgs& a, const int32_t* trow, int p1, int lane,
+                                       bool report, int (&y)[NB]) {
+    const int nb = SMALLP ? Mla::BK / a.P : 1;
+    if (pg + nb > chunk0 + 32) {
+      chunk0 = pg;
+      const int my = chunk0 + lane;
+      phys = 0;
+      if (my < p1) {
+        phys = __ldg(trow + my);
+        if (phys < 0 || phys >= a.num_pages) {
+          if (report) atomicOr(a.status, SPLITKV_DEVERR_PAGE);
+          phys = 0;
+        }
+      }
+    }
+    if (SMALLP) {
+#pragma unroll
+      for (int r = 0; r < NB; ++r) y[r] = __shfl_sync(kFull, phys, pg + min(r, nb - 1) - chunk0) * a.P;
+    } else {
+      y[0] = __shfl_sync(kFull, phys, pg - chunk0) * a.P + off;
+    }
+  }
+
+  __device__ __forceinline__ void next(int P) {
+    if (SMALLP) {
+      pg += Mla::BK / P;
+    } else if ((off += Mla::BK) == P) {
+      ++pg;
+      off = 0;
+    }
+  }
+};
+
+template <bool SEPV, bool SMALLP>
 __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     mla_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
@@ -206,10 +259,13 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   // plan's sequence length (uploaded, never written by a kernel): read before the wait
   const int L = a.fixed ? L_fixed : a.plan_lens[b];
-  const int k_begin = p0 * C::BK;
-  const int k_end = min(p1 * C::BK, L);
+  const int k_begin = p0 * a.P;
+  const int k_end = min(p1 * a.P, L);
   const int nblk = k_end > k_begin ? (k_end - k_begin + C::BK - 1) / C::BK : 0;
-  const int lim = L - a.T + t;  // last key visible to this token
+  // last key this CTA scores: visible to its token and inside the split (a
+  // split of 16- or 32-key pages may end inside a 64-key block; with larger
+  // pages a split ends at a block end or at L)
+  const int lim = SMALLP ? min(L - a.T + t, k_end - 1) : L - a.T + t;
   launch_dependents();
   wait_prerequisites();
   if (threadIdx.x == 0 && h == 0 && t == 0 && a.seq_lens[b] != L)
@@ -228,38 +284,35 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
     bool ok = true;
     int issued = 0;
-    int phys = 0, chunk0 = -32;
-    for (int j = 0; j < nblk && ok; ++j) {
-      const int page = p0 + j;
-      if (page >= chunk0 + 32) {
-        chunk0 = page;
-        const int my = chunk0 + lane;
-        phys = 0;
-        if (my < p1) {
-          phys = __ldg(trow + my);
-          if (phys < 0 || phys >= a.num_pages) {
-            atomicOr(a.status, SPLITKV_DEVERR_PAGE);
-            phys = 0;
-          }
-        }
-      }
-      const int y = (__shfl_sync(kFull, phys, page - chunk0) * a.Hkv) * a.P;
+    PageWalk<SMALLP> walk(p0);
+    const int br = SMALLP ? a.P : C::BK;  // rows per box
+    for (int j = 0; j < nblk && ok; ++j, walk.next(a.P)) {
+      int yr[PageWalk<SMALLP>::NB];
+      walk.rows(a, trow, p1, lane, true, yr);
       const int st = j % C::NST;
       if (j >= C::NST) ok = __all_sync(kFull, mbar_wait(bar(empty0 + st), ((j / C::NST) - 1) & 1));
       if (!ok) break;
       mbar_arrive_expect_tx_warp(bar(full0 + st), slot_bytes);
-      for (int k = 0; k < nchk; ++k)
-        tma_load_2d_warp(smem_u32(ring + st * slot_bytes + k * C::K_CH), &tk, bar(full0 + st),
-                         (vring ? v_chunk(h, k) : n_chunk(h, k)) * 64, y);
+#pragma unroll
+      for (int r = 0; r < PageWalk<SMALLP>::NB; ++r) {
+        if (r * br >= C::BK) break;
+        for (int k = 0; k < nchk; ++k)
+          tma_load_2d_warp(smem_u32(ring + st * slot_bytes + k * C::K_CH + r * br * 128), &tk,
+                           bar(full0 + st), (vring ? v_chunk(h, k) : n_chunk(h, k)) * 64, yr[r]);
+      }
       if (!vring) {
         // The V-ring slot of block j is refilled only once PV(j - 2) is done,
         // a few hundred cycles before the score MMAs need it, while this ring
         // is refilled some 3,000 cycles earlier: warm L2 with block j's
         // V-ring rows (and, with a separate V tensor, its V rows) now, so that
         // copy hits L2 instead of waiting out a DRAM round trip.
-        for (int k = 0; k < C::NX; ++k) tma_prefetch_2d_warp(&tk, v_chunk(h, k) * 64, y);
-        if (SEPV)
-          for (int k = 0; k < C::NV; ++k) tma_prefetch_2d_warp(&tv, (4 * h + k) * 64, y);
+#pragma unroll
+        for (int r = 0; r < PageWalk<SMALLP>::NB; ++r) {
+          if (r * br >= C::BK) break;
+          for (int k = 0; k < C::NX; ++k) tma_prefetch_2d_warp(&tk, v_chunk(h, k) * 64, yr[r]);
+          if (SEPV)
+            for (int k = 0; k < C::NV; ++k) tma_prefetch_2d_warp(&tv, (4 * h + k) * 64, yr[r]);
+        }
       }
       issued = j + 1;
     }
@@ -281,26 +334,22 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
     bool ok = true;
     int issued = 0;
-    int phys = 0, chunk0 = -32;
-    for (int j = 0; j < nblk && ok; ++j) {
-      const int page = p0 + j;
-      if (page >= chunk0 + 32) {
-        chunk0 = page;
-        const int my = chunk0 + lane;
-        phys = 0;
-        if (my < p1) {
-          phys = __ldg(trow + my);
-          if (phys < 0 || phys >= a.num_pages) phys = 0;  // reported by the key producer
-        }
-      }
-      const int y = (__shfl_sync(kFull, phys, page - chunk0) * a.Hkv) * a.P;
+    PageWalk<SMALLP> walk(p0);
+    const int br = SMALLP ? a.P : C::BK;
+    for (int j = 0; j < nblk && ok; ++j, walk.next(a.P)) {
+      int yr[PageWalk<SMALLP>::NB];  // (out-of-range page ids are reported by the key producer)
+      walk.rows(a, trow, p1, lane, false, yr);
       const int st = j % C::NST;
       ok = __all_sync(kFull, mbar_wait(bar(B_XKDONE + st), (j / C::NST) & 1));
       if (!ok) break;
       mbar_arrive_expect_tx_warp(bar(B_VDATA + st), C::NV * C::K_CH);
-      for (int k = 0; k < C::NV; ++k)
-        tma_load_2d_warp(smem_u32(sm + C::OFF_V + st * C::V_SLOT + k * C::K_CH), &tv,
-                         bar(B_VDATA + st), (4 * h + k) * 64, y);
+#pragma unroll
+      for (int r = 0; r < PageWalk<SMALLP>::NB; ++r) {
+        if (r * br >= C::BK) break;
+        for (int k = 0; k < C::NV; ++k)
+          tma_load_2d_warp(smem_u32(sm + C::OFF_V + st * C::V_SLOT + k * C::K_CH + r * br * 128),
+                           &tv, bar(B_VDATA + st), (4 * h + k) * 64, yr[r]);
+      }
       issued = j + 1;
     }
     if (!ok && lane == 0) {
@@ -616,11 +665,11 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
 
 namespace {
 
-template <bool SEPV>
+template <bool SEPV, bool SMALLP>
 cudaError_t launch_mla_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                          cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      mla_splitkv_kernel<SEPV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Mla::SMEM);
+      mla_splitkv_kernel<SEPV, SMALLP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Mla::SMEM);
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_items * a.T * 2, 1, 1);
@@ -632,7 +681,7 @@ cudaError_t launch_mla_t(const DecodeArgs& a, const CUtensorMap& mk, const CUten
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<SEPV>, a, mk, mv);
+  return cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<SEPV, SMALLP>, a, mk, mv);
 }
 
 }  // namespace
@@ -641,8 +690,13 @@ cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv
   if (a.n_items == 0) return cudaSuccess;
   const CUtensorMap& mk = *reinterpret_cast<const CUtensorMap*>(&tk);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (tv) return launch_mla_t<true>(a, mk, *reinterpret_cast<const CUtensorMap*>(tv), s);
-  return launch_mla_t<false>(a, mk, mk, s);
+  // pages of 16 or 32 keys: several boxes per 64-key block
+  const bool small = a.P < Mla::BK;
+  if (tv) {
+    const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(tv);
+    return small ? launch_mla_t<true, true>(a, mk, mv, s) : launch_mla_t<true, false>(a, mk, mv, s);
+  }
+  return small ? launch_mla_t<false, true>(a, mk, mk, s) : launch_mla_t<false, false>(a, mk, mk, s);
 }
 
 }  // namespace splitkv

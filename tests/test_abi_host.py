@@ -144,6 +144,23 @@ def test_mla_with_separate_v_is_planned():
     assert np.array_equal(items[0], items[1])
 
 
+@pytest.mark.parametrize("P,ok", [(16, True), (32, True), (64, True), (128, True), (192, True),
+                                  (48, False), (80, False)])
+def test_mla_page_sizes(P, ok):
+    """The MLA kernel streams 64-key blocks: pages of 16 or 32 keys (several
+    per block) or of a multiple of 64 keys (whole blocks per page)."""
+    d = skv.make_desc(1, 2, 128, 1, 576, 512, P, 64 * 64 // P + 1, 8 * 64 * 64 // P,
+                      skv.SPLITKV_BF16, 1)
+    lens = np.array([64 * 64], np.int32)
+    if ok:
+        it = skv.splitkv_plan_get_items(skv.splitkv_plan(d, lens, 4, 148))
+        assert it[:, 5].max() * P >= 64 * 64
+    else:
+        with pytest.raises(skv.SplitKVError) as e:
+            skv.splitkv_plan(d, lens, 4, 148)
+        assert e.value.status == skv.SPLITKV_EUNSUPPORTED
+
+
 def test_two_step_entry_points_validate_before_any_cuda_call():
     plan = skv.splitkv_plan(_desc(B=1), np.array([300], np.int32), 2, 148)
     A = 1 << 20  # aligned, never dereferenced: validation fails first

@@ -21,8 +21,8 @@ def _gpu():
     need_gpu()
 
 
-def _mla(lens, T, seed=3, v_shares_k=True):
-    return workloads.Workload("mla_custom", len(lens), T, 128, 1, 576, 512, 64, "bf16",
+def _mla(lens, T, seed=3, v_shares_k=True, P=64):
+    return workloads.Workload("mla_custom", len(lens), T, 128, 1, 576, 512, P, "bf16",
                               "list:" + ":".join(str(int(x)) for x in lens), std=0.5,
                               v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
@@ -59,3 +59,23 @@ def test_mla_ctx64k_full(name):
         compare(out, lse, ref_o, ref_l, what=f"S={S}")
         log, status = s.stats()
         assert status == 0 and (log[:, 2] > 0).all()
+
+
+@pytest.mark.parametrize("P", [16, 32, 128, 192])
+@pytest.mark.parametrize("sepv", [False, True])
+def test_mla_page_sizes(P, sepv):
+    """Pages smaller than the 64-key block (several boxes per block chunk,
+    split boundaries inside a block) and larger ones (several blocks per
+    page, split boundaries at page starts)."""
+    T = 3
+    lens = [T, 40, P + 7, 3 * P, 777, 2100]
+    x = workloads.make_inputs(_mla(lens, T, seed=30 + P + sepv, v_shares_k=not sepv, P=P),
+                              device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in (1, 3, 7, 0):
+        s = session(x, S)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"P={P} sepv={sepv} S={S}")
+        log, status = s.stats()
+        assert status == 0, status
+        assert (log[:, 3] == 0).all()
