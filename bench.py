@@ -59,7 +59,7 @@ NOMINAL_HBM_GBS = 8000.0  # the "about 8 TB/s" HBM figure the metric also report
 PROFILED_TRAFFIC = {
     "gqa_ctx5900": (6115328, "profiles/gqa_splitkv_kernel_gqa_ctx5900.md"),
     "fp8_batch8_ctx32k": (253606400, "profiles/gqa_splitkv_kernel_fp8_batch8_ctx32k.md"),
-    "mla_t6_ctx64k": (79252736, "profiles/mla_splitkv_kernel_mla_t6_ctx64k.md"),
+    "mla_t6_ctx64k": (79173632, "profiles/mla_splitkv_kernel_mla_t6_ctx64k.md"),
 }
 
 
