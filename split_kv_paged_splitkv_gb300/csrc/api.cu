@@ -142,12 +142,12 @@ splitkv_status fail(splitkv_status s, const char* fmt, ...) {
 Family family_of(const splitkv_desc_t& d) {
   const int G = d.num_q_heads / d.num_kv_heads;
   if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 16) return Family::kGqa;
-  // V either shares the latent rows (their first 512 columns) or is its own tensor
+  // V either shares the latent rows (their first 512 columns) or is its own
+  // tensor.  Keys stream in 64-key blocks: pages of 16 or 32 keys fill a block
+  // with 4 or 2 boxes, larger pages (multiples of 64) hold whole blocks.
   if (d.qk_dim == 576 && d.v_dim == 512 && d.num_kv_heads == 1 &&
       d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.q_tokens <= 16 &&
       (64 % d.page_size == 0 || d.page_size % 64 == 0))
-    // 64-key blocks: 16- and 32-key pages fill one with 4 or 2 boxes, larger
-    // pages (multiples of 64) hold whole blocks
     return Family::kMla;
   return Family::kNone;
 }
@@ -408,8 +408,8 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
   if (family_of(d) == Family::kMla) {
-    // Latent cache rows of 576 bf16 (64-key boxes = one page), and with a
-    // separate V tensor its rows of 512; the query rows are read by the
+    // Latent cache rows of 576 bf16 (boxes of min(P, 64) rows, one page at
+    // most), and with a separate V tensor its rows of 512; the query rows are read by the
     // kernel's threads.  The partials are always merged by the separate
     // combine kernel.
     TmaDesc tk, tv;

@@ -33,8 +33,8 @@ def _gqa(lens, G=8, Hkv=2, T=1, P=16, fp8=False, seed=3):
         "list:" + ":".join(str(int(x)) for x in lens), pool_slack=0.5, seed=seed)
 
 
-def _mla(lens, T=2, seed=5, v_shares_k=True):
-    return workloads.Workload("fixed_mla", len(lens), T, 128, 1, 576, 512, 64, "bf16",
+def _mla(lens, T=2, seed=5, v_shares_k=True, P=64):
+    return workloads.Workload("fixed_mla", len(lens), T, 128, 1, 576, 512, P, "bf16",
                               "list:" + ":".join(str(int(x)) for x in lens), std=0.5,
                               v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
@@ -108,10 +108,10 @@ def test_one_graph_serves_changing_lengths(mode, T, G):
         assert s.stats()[1] == 0
 
 
-@pytest.mark.parametrize("v_shares_k", [True, False])
-def test_mla_capacity_plan(v_shares_k):
+@pytest.mark.parametrize("v_shares_k,P", [(True, 64), (False, 64), (True, 16), (False, 32)])
+def test_mla_capacity_plan(v_shares_k, P):
     cap = [64 * 9 + 5, 64 * 3, 2]
-    x = workloads.make_inputs(_mla(cap, v_shares_k=v_shares_k), device="cuda")
+    x = workloads.make_inputs(_mla(cap, v_shares_k=v_shares_k, P=P), device="cuda")
     lens_dev = x.seq_lens.clone()
     s = _session(x, 4, lens_dev=lens_dev)
     for lens in (cap, [64 * 2 + 1, 64 * 3, 0]):
@@ -119,7 +119,7 @@ def test_mla_capacity_plan(v_shares_k):
         s.run()
         torch.cuda.synchronize()
         ref_o, ref_l = _oracle_at(x, lens)
-        compare(s.out, s.lse, ref_o, ref_l, what=f"mla lens={lens}")
+        compare(s.out, s.lse, ref_o, ref_l, what=f"mla P={P} lens={lens}")
         log, status = s.stats()
         assert status == 0
 
