@@ -3,7 +3,7 @@
 * brute force in 60-digit arithmetic (mpmath) on tiny hand-built inputs, with
   the softmax written without max-subtraction;
 * closed forms (identical keys, one key, one dominant key);
-* invariants (number of splits, physical page permutation, combine
+* invariants (number of splits, physical page permutation, page size, combine
   associativity and permutation, -inf as the combine's identity);
 * library special cases (torch.softmax in float64, torch's e4m3 and bf16
   decoders);
@@ -355,6 +355,50 @@ def test_page_permutation_invariance_is_bitwise():
     table2 = perm[table].astype(np.int32)
     out2, lse2 = O.attention_direct(q, k2, v2, table2, lens, scale=0.25)
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def _repage(pages, P_new, perm):
+    """The key rows of a contiguous pool (pages 0..n-1 in table order) cut
+    into pages of P_new rows; logical page i is stored at physical perm[i]."""
+    N, Hkv, P, D = pages.shape
+    rows = pages.transpose(1, 0, 2, 3).reshape(Hkv, N * P, D)  # [Hkv][keys][D]
+    n_new = len(perm)
+    pad = n_new * P_new - N * P
+    rows = np.concatenate([rows, np.zeros((Hkv, pad, D), rows.dtype)], axis=1)
+    logical = rows.reshape(Hkv, n_new, P_new, D).transpose(1, 0, 2, 3)
+    out = np.empty_like(logical)
+    out[perm] = logical
+    return out
+
+
+@pytest.mark.parametrize("P_old,P_new", [(4, 16), (16, 4), (8, 24)])
+@pytest.mark.parametrize("latent", [False, True])
+def test_page_size_is_transparent(P_old, P_new, latent):
+    """Cutting the same key rows into pages of another size (the 576-wide
+    latent rows with V as their first columns, or separate K and V) and
+    scattering them over the pool changes nothing: bitwise for the direct
+    definition, to rounding in split mode (whose page-granular split
+    boundaries move)."""
+    rng = np.random.default_rng(40 + P_old + P_new)
+    L, T, Hq = 45, 3, 4
+    D, dv = (12, 8) if latent else (6, 6)
+    n = -(-L // P_old)
+    q = _bf16_bits(rng.standard_normal((1, T, Hq, D)))
+    k = _bf16_bits(rng.standard_normal((n, 1, P_old, D)))
+    v = None if latent else _bf16_bits(rng.standard_normal((n, 1, P_old, dv)))
+    table = np.arange(n, dtype=np.int32)[None, :]
+    lens = np.array([L], np.int32)
+    kw = dict(scale=0.3, v_dim=dv, v_shares_k=latent)
+    ref = O.attention_direct(q, k, v, table, lens, **kw)
+    perm = rng.permutation(-(-(n * P_old) // P_new)).astype(np.int32)
+    k2 = _repage(k, P_new, perm)
+    v2 = None if latent else _repage(v, P_new, perm)
+    got = O.attention_direct(q, k2, v2, perm[None, :], lens, **kw)
+    assert np.array_equal(ref[0], got[0]) and np.array_equal(ref[1], got[1])
+    for S in (1, 2, 3):
+        o, l = O.attention_split_mode(q, k2, v2, perm[None, :], lens, num_splits=S, **kw)
+        np.testing.assert_allclose(o, ref[0], atol=1e-12)
+        np.testing.assert_allclose(l, ref[1], atol=1e-12)
 
 
 def _rand_part(rng, dim=6):
