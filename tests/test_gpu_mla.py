@@ -27,7 +27,7 @@ def _mla(lens, T, seed=3, v_shares_k=True, P=64):
                               v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
 
-@pytest.mark.parametrize("T", [1, 2, 6])
+@pytest.mark.parametrize("T", [1, 2, 6, 16])
 @pytest.mark.parametrize("sepv", [False, True])
 def test_mla_small_ragged(T, sepv):
     """V as the first 512 columns of the latent rows, or (sepv) its own tensor."""
