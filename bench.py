@@ -33,6 +33,7 @@ reference arm: the pages ship no code of their own).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -75,6 +76,8 @@ def parse():
                     help="capacity plan whose kernels derive the items from the device "
                          "lengths every step (needs --splits)")
     ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="page size in keys (0 = the workload's own)")
     ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"],
                     help="page layout of the KV pools: [N][Hkv][P][D] or [N][P][Hkv][D]")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -204,15 +207,17 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
-def time_oracle(w, x, seconds, threads=1):
-    """Runs the oracle on the full call repeatedly in a clean single-threaded
-    subprocess; returns (µs per call, calls)."""
+def time_oracle(w, x, seconds, threads=1, calls=0, warmup=0):
+    """Runs the oracle on the full call in a clean single-threaded subprocess:
+    `warmup` untimed calls, then exactly `calls` timed ones, or (calls = 0)
+    timed ones until `seconds` have passed (at least one); returns (µs per
+    call, timed calls)."""
     import pickle
     payload = dict(q=workloads.bits(x.q), k=workloads.bits(x.k_pages),
                    v=None if x.v_pages is None else workloads.bits(x.v_pages),
                    table=x.block_table.cpu().numpy(), lens=x.seq_lens_host, scale=x.scale,
                    kv_dtype=w.kv_dtype, kv_scale=x.kv_scale, v_dim=w.v_dim,
-                   v_shares_k=w.v_shares_k, seconds=seconds)
+                   v_shares_k=w.v_shares_k, seconds=seconds, calls=calls, warmup=warmup)
     with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
         pickle.dump(payload, f)
         path = f.name
@@ -221,12 +226,15 @@ def time_oracle(w, x, seconds, threads=1):
         f"sys.path.insert(0, {ROOT!r})\n"
         "import oracle\n"
         f"d = pickle.load(open({path!r}, 'rb'))\n"
-        "n = 0; t0 = time.perf_counter()\n"
-        "while True:\n"
+        "def call():\n"
         "    oracle.attention_direct(d['q'], d['k'], d['v'], d['table'], d['lens'], scale=d['scale'],\n"
         "        kv_dtype=d['kv_dtype'], kv_scale=d['kv_scale'], v_dim=d['v_dim'], v_shares_k=d['v_shares_k'])\n"
+        "for _ in range(d['warmup']): call()\n"
+        "n = 0; t0 = time.perf_counter()\n"
+        "while True:\n"
+        "    call()\n"
         "    n += 1\n"
-        "    if time.perf_counter() - t0 >= d['seconds']: break\n"
+        "    if n == d['calls'] or (not d['calls'] and time.perf_counter() - t0 >= d['seconds']): break\n"
         "print(json.dumps({'us': (time.perf_counter() - t0) / n * 1e6, 'n': n}))\n")
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -250,18 +258,20 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w = workloads.WORKLOADS[args.workload]
+    if args.page_size:
+        w = dataclasses.replace(w, page_size=args.page_size)
     x = workloads.make_inputs(w, device="cpu")
     # Each step is one full oracle call; the run is bounded by --cpu-seconds
     # (so at most --steps calls, at least one).
     per_call, _ = time_oracle(w, x, 0.0)
     steps = max(1, min(args.steps, int(args.cpu_seconds * 1e6 / max(per_call, 1.0))))
-    warm = 1
-    us, n = time_oracle(w, x, steps * per_call / 1e6)
+    warm = max(1, min(args.warmup, steps))
+    us, n = time_oracle(w, x, 0.0, calls=steps, warmup=warm)
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
         "steps": n, "warmup": warm, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
+        "config": {"workload": w.name, "page_size": w.page_size},
         "cpu_baseline": {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": oracle_sample_desc(w, n)},
         "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -278,6 +288,8 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
+    if args.page_size:
+        w = dataclasses.replace(w, page_size=args.page_size)
     x = workloads.make_inputs(w, device=dev, layout=args.layout.upper())
     mode = skv.SPLITKV_COMBINE_FUSED if args.combine == "fused" else skv.SPLITKV_COMBINE_SEPARATE
     # Everything runs on torch's current stream: graphs are captured on a side
@@ -406,7 +418,8 @@ def run_ours(args, rank, world, local):
     # the captures ran the default configuration (planner splits, separate
     # combine, host plan, HND pages); other configurations report no traffic
     default_cfg = (args.splits == 0 and not args.fixed and args.combine == "separate"
-                   and args.layout == "hnd")
+                   and args.layout == "hnd"
+                   and args.page_size in (0, workloads.WORKLOADS[args.workload].page_size))
     traffic, traffic_src = PROFILED_TRAFFIC.get(w.name, (None, None)) if default_cfg else (None, None)
     roof.update({"traffic": traffic, "traffic_source": traffic_src,
                  "duration_basis": ("split-KV kernel alone (splitkv_decode_partials), CUDA-graph "
