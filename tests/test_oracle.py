@@ -156,6 +156,25 @@ def test_causal_multi_token_brute_force():
             assert abs(lse[0, t, h] - ref_l) < 1e-13
 
 
+def test_latent_v_brute_force():
+    """The latent cache (V shares the key rows): V_j is the first v_dim
+    columns of K_j, for every query head of the one KV head, causal over T."""
+    rng = np.random.default_rng(29)
+    L, T, D, dv, P, Hq = 6, 2, 5, 3, 4, 3
+    q, k, _, table, lens = _tiny_problem(rng, L, D, Hq=Hq, Hkv=1, T=T, P=P)
+    out, lse = O.attention_direct(q, k, None, table, lens, scale=0.45, v_dim=dv,
+                                  v_shares_k=True)
+    assert out.shape == (1, T, Hq, dv)
+    for t in range(T):
+        for h in range(Hq):
+            n_vis = L - T + t + 1
+            K = [O.bf16_to_float(k[table[0, j // P], 0, j % P]) for j in range(n_vis)]
+            V = [row[:dv] for row in K]
+            ref_o, ref_l = _mp_attention(O.bf16_to_float(q[0, t, h]), K, V, 0.45)
+            np.testing.assert_allclose(out[0, t, h], ref_o, atol=1e-13)
+            assert abs(lse[0, t, h] - ref_l) < 1e-13
+
+
 def test_fp8_brute_force_with_scale():
     """e4m3 keys/values are code * kv_scale in both the scores and the output."""
     rng = np.random.default_rng(11)
@@ -542,11 +561,12 @@ def _pins_on_direct():
     test_causal_multi_token_brute_force()
     test_head_mapping_uses_contiguous_groups()
     test_nhd_layout_brute_force()
+    test_latent_v_brute_force()
 
 
 @pytest.mark.parametrize("mistake", ["no_scale", "neg_scores", "k_for_v", "lse_off_by_max",
                                      "head_mod", "causal_off_by_one", "page_slot_swap",
-                                     "nhd_read_as_hnd"])
+                                     "nhd_read_as_hnd", "latent_v_last_columns"])
 def test_planted_mistakes_are_caught(monkeypatch, mistake):
     """Each plausible slip, planted in the oracle on the CPU, fails a pin."""
     orig_attend = O._softmax_attend
@@ -588,6 +608,14 @@ def test_planted_mistakes_are_caught(monkeypatch, mistake):
             out = orig_gather(pages, row, n, head, layout)
             return out[::-1].copy() if n > P else out
         monkeypatch.setattr(O, "gather_keys", bad_gather)
+    elif mistake == "latent_v_last_columns":
+        # V of the latent cache taken from the last v_dim columns of the key rows
+        def bad_attend(q, K, V, s):
+            dv = V.shape[1]
+            if dv < K.shape[1] and np.array_equal(V, K[:, :dv]):
+                V = K[:, K.shape[1] - dv:]
+            return orig_attend(q, K, V, s)
+        monkeypatch.setattr(O, "_softmax_attend", bad_attend)
     elif mistake == "nhd_read_as_hnd":
         # the slot and head axes of NHD pages taken in HND order
         monkeypatch.setattr(O, "gather_keys",
