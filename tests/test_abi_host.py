@@ -306,13 +306,15 @@ def test_combine_validates():
 def test_plan_matches_oracle_mla_cta_pairs():
     """MLA items launch a CTA pair per query token; the automatic split count
     plans over num_sms / (2 T) machines in both the library and the oracle."""
-    for T, L in ((6, 65536), (1, 4096), (2, 300)):
-        d = skv.make_desc(1, T, 128, 1, 576, 512, 64, 1024, 1100, skv.SPLITKV_BF16, 1)
+    for T, L, P in ((6, 65536, 64), (1, 4096, 64), (2, 300, 64), (16, 9000, 64),
+                    (6, 65536, 16), (3, 777, 32), (6, 65536, 128)):
+        maxp = -(-65536 // P)
+        d = skv.make_desc(1, T, 128, 1, 576, 512, P, maxp, maxp + 8, skv.SPLITKV_BF16, 1)
         for S in (0, 1, 4, 8):
             plan = skv.splitkv_plan(d, np.array([L], np.int32), S, 148)
             items = skv.splitkv_plan_get_items(plan)
-            ref = np.array(oracle.plan_items([L], 64, 1, S, 148, ctas_per_item=2 * T), np.int32)
-            assert np.array_equal(items[:, :6], ref), (T, L, S)
+            ref = np.array(oracle.plan_items([L], P, 1, S, 148, ctas_per_item=2 * T), np.int32)
+            assert np.array_equal(items[:, :6], ref), (T, L, P, S)
 
 
 def test_launches_per_call():
