@@ -11,8 +11,15 @@ Protocol
     batch.  Steps are captured in CUDA graphs and replayed; the timed region
     is bracketed by a barrier and ``torch.cuda.synchronize()`` and timed with
     CUDA events on the launching stream.
-  * The KV inputs rotate over R copies of the page pool whose total exceeds 4x
-    the L2 size, so no step starts with its pages in L2.
+  * Every step reads pages no recent step touched: either (``--pool single``,
+    the default) one pool of R x the workload's pages in a random physical
+    order with R block tables, each naming its own disjoint random set of
+    pages, or (``--pool rotate``) R separate copies of the workload's pool;
+    either way R x the pool bytes exceed 4x the L2 size.
+  * Every captured graph is replayed before the timed region; exactly
+    ``--steps`` calls are timed, from the device's start of the first call
+    (a short device-side spin before the start event hides the host's graph
+    launch latency) to the end of the last.
   * ``value`` = timed-region time / steps (whole-job: / (steps x ranks)).
   * ``roofline``: algorithmic bytes of one launch of the split-KV kernel (KV
     bytes of the visible keys + Q bytes) / its average launch duration,
@@ -23,7 +30,12 @@ Protocol
   * ``e2e``: the same call with host buffers -- pinned-host -> device copies
     of every input, the decode, and device -> host copies of out and lse,
     all inside the timed region.
-  * ``cpu_baseline``: the fp64 oracle, single-threaded, on a bounded sample.
+  * ``cpu_baseline``: the fp64 oracle on a bounded sample, as independent
+    calls on every host core at once (``value``, ``cores``) and on one thread
+    (``single_thread``).
+  * ``per_config``: every workload of the suite, measured the same way with
+    fewer steps (µs per call, the split kernel alone, roofline fraction, the
+    fraction of split CTAs that scored keys).
   * Clocks: ``nvidia-smi`` samples every 200 ms while the same work runs
     (a >= 1 s soak immediately followed by the timed region).
 
@@ -80,6 +92,11 @@ def parse():
                     help="page size in keys (0 = the workload's own)")
     ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"],
                     help="page layout of the KV pools: [N][Hkv][P][D] or [N][P][Hkv][D]")
+    ap.add_argument("--pool", default="single", choices=["single", "rotate"],
+                    help="single: one large pool in random page order, a block table per "
+                         "step; rotate: separate pool copies")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config measurements of the other workloads")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -207,11 +224,41 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
-def time_oracle(w, x, seconds, threads=1, calls=0, warmup=0):
-    """Runs the oracle on the full call in a clean single-threaded subprocess:
-    `warmup` untimed calls, then exactly `calls` timed ones, or (calls = 0)
-    timed ones until `seconds` have passed (at least one); returns (µs per
-    call, timed calls)."""
+_ORACLE_CHILD = """
+import json, os, pickle, sys, time
+sys.path.insert(0, {root!r})
+import oracle
+d = pickle.load(open({path!r}, 'rb'))
+def call():
+    oracle.attention_direct(d['q'], d['k'], d['v'], d['table'], d['lens'], scale=d['scale'],
+        kv_dtype=d['kv_dtype'], kv_scale=d['kv_scale'], v_dim=d['v_dim'], v_shares_k=d['v_shares_k'])
+for _ in range(d['warmup']):
+    call()
+# start together with the other processes of the same sample
+ready = {ready!r}
+if ready:
+    open(os.path.join(ready, str(os.getpid())), 'w').close()
+    t_wait = time.perf_counter()
+    while len(os.listdir(ready)) < {nproc} and time.perf_counter() - t_wait < 60:
+        time.sleep(0.001)
+n = 0
+t0 = time.perf_counter()
+while True:
+    call()
+    n += 1
+    if n == d['calls'] or (not d['calls'] and time.perf_counter() - t0 >= d['seconds']):
+        break
+print(json.dumps({{'s': time.perf_counter() - t0, 'n': n}}))
+"""
+
+
+def time_oracle(w, x, seconds, calls=0, warmup=0, procs=1):
+    """Runs the oracle on the full call in `procs` single-threaded
+    subprocesses at once (independent calls, one per host core when procs =
+    the core count): each does `warmup` untimed calls, then, once all are
+    ready, exactly `calls` timed ones or (calls = 0) timed ones until
+    `seconds` have passed.  Returns (µs per call of the whole sample = longest
+    process time / total calls, total timed calls)."""
     import pickle
     payload = dict(q=workloads.bits(x.q), k=workloads.bits(x.k_pages),
                    v=None if x.v_pages is None else workloads.bits(x.v_pages),
@@ -221,35 +268,51 @@ def time_oracle(w, x, seconds, threads=1, calls=0, warmup=0):
     with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
         pickle.dump(payload, f)
         path = f.name
-    code = (
-        "import pickle, sys, time, json\n"
-        f"sys.path.insert(0, {ROOT!r})\n"
-        "import oracle\n"
-        f"d = pickle.load(open({path!r}, 'rb'))\n"
-        "def call():\n"
-        "    oracle.attention_direct(d['q'], d['k'], d['v'], d['table'], d['lens'], scale=d['scale'],\n"
-        "        kv_dtype=d['kv_dtype'], kv_scale=d['kv_scale'], v_dim=d['v_dim'], v_shares_k=d['v_shares_k'])\n"
-        "for _ in range(d['warmup']): call()\n"
-        "n = 0; t0 = time.perf_counter()\n"
-        "while True:\n"
-        "    call()\n"
-        "    n += 1\n"
-        "    if n == d['calls'] or (not d['calls'] and time.perf_counter() - t0 >= d['seconds']): break\n"
-        "print(json.dumps({'us': (time.perf_counter() - t0) / n * 1e6, 'n': n}))\n")
+    ready = tempfile.mkdtemp(prefix="oracle_ready_") if procs > 1 else ""
+    code = _ORACLE_CHILD.format(root=ROOT, path=path, ready=ready, nproc=procs)
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = str(threads)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+        env[k] = "1"
+    ps = [subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE,
+                           stderr=subprocess.PIPE, text=True, env=env) for _ in range(procs)]
+    res = []
+    for pr in ps:
+        out, err = pr.communicate()
+        if pr.returncode != 0:
+            raise RuntimeError(err)
+        res.append(json.loads(out.strip().splitlines()[-1]))
     os.unlink(path)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr)
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return d["us"], d["n"]
+    if ready:
+        for f in os.listdir(ready):
+            os.unlink(os.path.join(ready, f))
+        os.rmdir(ready)
+    n = sum(r["n"] for r in res)
+    return max(r["s"] for r in res) / n * 1e6, n
 
 
-def oracle_sample_desc(w, n):
-    return (f"fp64 oracle (numpy, 1 thread) on the full {w.name} call "
-            f"({w.batch} seq x {w.num_q_heads} q heads x {w.lens} keys), repeated {n} times")
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_desc(w, n, procs):
+    how = ("one thread" if procs == 1 else
+           f"{procs} single-threaded processes at once, one per host core, independent calls")
+    return (f"fp64 oracle (numpy) on the full {w.name} call "
+            f"({w.batch} seq x {w.num_q_heads} q heads x {w.lens} keys), {n} calls in all, {how}")
+
+
+def cpu_baseline(w, x, seconds):
+    """The oracle on every host core at once (value, cores) and on one thread."""
+    cores = host_cores()
+    us1, n1 = time_oracle(w, x, seconds)
+    usn, nn = time_oracle(w, x, seconds, procs=cores)
+    return {"value": usn, "unit": "us", "cores": cores, "kind": "oracle",
+            "sample": oracle_sample_desc(w, nn, cores),
+            "single_thread": {"value": us1, "unit": "us", "cores": 1,
+                              "sample": oracle_sample_desc(w, n1, 1)}}
 
 
 # ----------------------------------------------------------------- reference arm
@@ -273,13 +336,240 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "page_size": w.page_size},
         "cpu_baseline": {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
-                         "sample": oracle_sample_desc(w, n)},
+                         "sample": oracle_sample_desc(w, n, 1)},
         "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------- our arm
+
+def l2_bytes(dev):
+    props = torch.cuda.get_device_properties(dev)
+    return int(getattr(props, "L2_cache_size", 126 * 2**20))
+
+
+def pool_bytes(x):
+    return x.k_pages.numel() * x.k_pages.element_size() + (
+        0 if x.v_pages is None else x.v_pages.numel() * x.v_pages.element_size())
+
+
+def step_inputs(x, R, kind, seed=7):
+    """The inputs of R consecutive steps, reading pages no recent step read.
+
+    kind "rotate": R copies of the pool, the workload's block table each.
+    kind "single": one pool of R x N pages in a random physical order; copy r
+    of page i sits at perm[r N + i] and step r's block table maps the
+    workload's page i there, so every step reads its own random set of pages
+    scattered over the whole pool (the way a serving KV cache is laid out).
+    Returns (k_pool, v_pool, list of R (k, v, table))."""
+    if kind == "rotate":
+        pools = [(x.k_pages, x.v_pages)] + [
+            (x.k_pages.clone(), None if x.v_pages is None else x.v_pages.clone())
+            for _ in range(R - 1)]
+        return None, None, [(k, v, x.block_table) for k, v in pools]
+    N = x.k_pages.shape[0]
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    perm = torch.randperm(R * N, generator=g).to(x.k_pages.device)
+    big_k = torch.empty((R * N,) + tuple(x.k_pages.shape[1:]), dtype=x.k_pages.dtype,
+                        device=x.k_pages.device)
+    big_v = None if x.v_pages is None else torch.empty(
+        (R * N,) + tuple(x.v_pages.shape[1:]), dtype=x.v_pages.dtype, device=x.v_pages.device)
+    steps = []
+    tab = x.block_table.long()
+    for r in range(R):
+        dst = perm[r * N:(r + 1) * N]
+        big_k[dst] = x.k_pages
+        if big_v is not None:
+            big_v[dst] = x.v_pages
+        steps.append((big_k, big_v, dst[tab].to(torch.int32).contiguous()))
+    return big_k, big_v, steps
+
+
+def capture(run_step, n, first=0):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(first, first + n):
+            run_step(i)
+    return g
+
+
+class Replayer:
+    """Back-to-back calls of `run_step(i)` (i cycling over R steps of
+    distinct pages) as CUDA graphs: the R-step cycle, and on demand a graph
+    of the K mod R steps left over (all K when K < R).  Every graph is
+    replayed before it is timed, and the steps just before a timed region
+    are always the cycle's, so the first timed step's pages were last read
+    R - 1 steps earlier."""
+
+    def __init__(self, run_step, R):
+        self.run_step, self.R = run_step, R
+        self.cycle = capture(run_step, R)
+        self.tails = {}
+
+    def warm(self, reps=1):
+        for _ in range(max(1, reps)):
+            self.cycle.replay()
+
+    def time(self, K, stream, warm_reps=1):
+        """µs per step over exactly K timed steps (CUDA events on `stream`)."""
+        reps, rem = divmod(K, self.R)
+        tail = None
+        if rem:
+            if rem not in self.tails:
+                self.tails[rem] = capture(self.run_step, rem)
+            tail = self.tails[rem]
+            tail.replay()  # its first replay (graph upload) stays untimed
+        self.warm(warm_reps)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        # A short device-side spin (outside the timed region) keeps the GPU
+        # busy while the host enqueues the start event and the first graph
+        # launch, so the host's launch latency does not land between the
+        # start event and the first call.
+        torch.cuda._sleep(100000)
+        e0.record(stream)
+        for _ in range(reps):
+            self.cycle.replay()
+        if tail is not None:
+            tail.replay()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / K
+
+    def steps_for(self, seconds, stream):
+        """A whole number of cycles lasting about `seconds` (at least one)."""
+        us = self.time(self.R, stream)
+        return self.R * max(1, round(seconds * 1e6 / (us * self.R)))
+
+
+def roofline(w, x, kernel_us, step_us, basis):
+    nbytes = algorithmic_bytes(w, x.seq_lens_host)
+    nflops = algorithmic_flops(w, x.seq_lens_host)
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
+    if is_tensor_bound(w):
+        roof = {"bound": "tensor", "achieved": nflops / (kernel_us * 1e-6) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "algorithmic_flops": nflops,
+                "hbm_gbs": nbytes / (kernel_us * 1e-6) / 1e9, "kernel": "mla_splitkv_kernel"}
+    else:
+        achieved = nbytes / (kernel_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac_of_8tbs": achieved / NOMINAL_HBM_GBS, "kernel": "gqa_splitkv_kernel"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"duration_basis": basis, "kernel_us": kernel_us, "step_us": step_us,
+                 "peak_kind": peak_kind, "algorithmic_bytes": nbytes})
+    return roof
+
+
+def measure(w, dev, *, splits=0, fixed=False, mode=None, layout="hnd", pool="single", steps=None,
+            warmup=5, soak_seconds=0.0, sampler=None):
+    """Times one workload: the whole call (graph replay, exactly `steps`
+    calls, or about 50 ms of calls when None) and its split-KV kernel alone.
+    Returns a dict of the results and the objects the headline run reuses."""
+    import split_kv_paged_splitkv_gb300 as skv
+    from split_kv_paged_splitkv_gb300.runner import DecodeSession
+
+    if mode is None:
+        mode = skv.SPLITKV_COMBINE_SEPARATE
+    x = workloads.make_inputs(w, device=dev, layout=layout.upper())
+    l2 = l2_bytes(dev)
+    R = max(2, min(256, math.ceil(4 * l2 / pool_bytes(x))))
+    big_k, big_v, per_step = step_inputs(x, R, pool)
+    k0, v0, t0 = per_step[0]
+    sess = DecodeSession(x.q, k0, v0, t0, x.seq_lens, x.seq_lens_host,
+                         scale=x.scale, kv_scale=x.kv_scale, num_splits=splits,
+                         v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode,
+                         fixed=fixed,
+                         kv_layout=skv.SPLITKV_LAYOUT_NHD if layout == "nhd" else skv.SPLITKV_LAYOUT_HND)
+    items = skv.splitkv_plan_get_items(sess.plan)
+    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan)
+
+    def step(i):
+        k, v, t = per_step[i % R]
+        sess.run(tensors=(x.q, k, v, t, x.seq_lens))
+
+    def step_partials(i):
+        k, v, t = per_step[i % R]
+        sess.run_partials(tensors=(x.q, k, v, t, x.seq_lens))
+
+    # eager warm-up (also sets up per-process kernel attributes before capture)
+    for i in range(max(3, min(warmup, R))):
+        step(i)
+    torch.cuda.synchronize()
+    log, status = sess.stats()
+    assert status == 0, f"device status {status}"
+    nonempty = float((log[:, 2] > 0).mean()) if len(log) else 1.0
+
+    stream = torch.cuda.current_stream()
+    # The split-KV kernel alone (splitkv_decode_partials, the first launch of
+    # each call), timed the same way on the same stream over about 20 ms of
+    # launches: its average launch duration is the roofline's denominator.
+    # With the fused combine the split kernel is the step's only launch and
+    # the step time is used.
+    kernel_us = None
+    if mode == skv.SPLITKV_COMBINE_SEPARATE:
+        rp = Replayer(step_partials, R)
+        rp.warm(3)
+        kernel_us = rp.time(rp.steps_for(0.02, stream), stream)
+        del rp
+
+    rs = Replayer(step, R)
+    if steps is None:  # about 50 ms of calls
+        steps = rs.steps_for(0.05, stream)
+    # graph warm-up + clock soak (same work), then the timed region
+    if sampler is not None:
+        sampler.start()
+    rs.warm(max(1, math.ceil(warmup / R)))
+    t_end = time.perf_counter() + soak_seconds
+    while time.perf_counter() < t_end:
+        rs.warm(20)
+        torch.cuda.synchronize()
+    us = rs.time(steps, stream)
+    clocks = sampler.stop() if sampler is not None else None
+    del rs
+    log, status = sess.stats()
+    assert status == 0, f"device status {status} after the timed region"
+    basis = ("split-KV kernel alone (splitkv_decode_partials), CUDA-graph replay, CUDA events "
+             "on the launching stream" if kernel_us is not None else
+             "timed-region time per call (the split kernel is the only launch)")
+    roof = roofline(w, x, kernel_us if kernel_us is not None else us, us, basis)
+    return {"x": x, "sess": sess, "items": items, "R": R, "pool_bytes": pool_bytes(x),
+            "launches_per_step": launches_per_step, "us": us, "kernel_us": kernel_us,
+            "nonempty": nonempty, "roof": roof, "clocks": clocks, "steps": steps}
+
+
+PER_CONFIG = ("tiny_gqa_ctx260", "gqa_ctx5900", "fp8_batch8_ctx32k", "mla_t6_ctx64k",
+              "mla_sepv_t6_ctx64k", "mixed_batch32_bf16", "mixed_batch32_fp8")
+
+
+def per_config(dev, args, headline):
+    """Every workload of the suite at its defaults (planner splits, separate
+    combine, HND pages, one large pool), about 50 ms of timed calls each."""
+    out = {}
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for name in PER_CONFIG:
+        if name == headline["name"]:
+            r = headline
+        else:
+            r = measure(workloads.WORKLOADS[name], dev, pool=args.pool, warmup=5)
+            r["name"] = name
+        roof = r["roof"]
+        out[name] = {"us_per_call": r["us"], "kernel_us": roof["kernel_us"],
+                     "roofline_bound": roof["bound"], "achieved": roof["achieved"],
+                     "unit": roof["unit"], "frac": roof["frac"],
+                     "nonempty_cta_fraction": r["nonempty"], "planned_items": int(len(r["items"])),
+                     "steps": r["steps"]}
+        if roof["bound"] == "tensor":
+            out[name]["hbm_gbs"] = roof["hbm_gbs"]
+        if name != headline["name"]:
+            del r
+            torch.cuda.empty_cache()
+    out["clocks"] = sampler.stop()
+    return out
+
 
 def run_ours(args, rank, world, local):
     import split_kv_paged_splitkv_gb300 as skv
@@ -290,152 +580,51 @@ def run_ours(args, rank, world, local):
     w = workloads.WORKLOADS[args.workload]
     if args.page_size:
         w = dataclasses.replace(w, page_size=args.page_size)
-    x = workloads.make_inputs(w, device=dev, layout=args.layout.upper())
     mode = skv.SPLITKV_COMBINE_FUSED if args.combine == "fused" else skv.SPLITKV_COMBINE_SEPARATE
     # Everything runs on torch's current stream: graphs are captured on a side
     # stream by torch.cuda.graph and replayed on the current stream.
     if args.fixed and args.splits < 1:
         raise SystemExit("--fixed needs --splits >= 1")
-    sess = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
-                         scale=x.scale, kv_scale=x.kv_scale, num_splits=args.splits,
-                         v_dim=w.v_dim, v_shares_k=w.v_shares_k, combine_mode=mode,
-                         fixed=args.fixed,
-                         kv_layout=skv.SPLITKV_LAYOUT_NHD if args.layout == "nhd" else skv.SPLITKV_LAYOUT_HND)
-    items = skv.splitkv_plan_get_items(sess.plan)
-    n_groups = len(np.unique(items[items[:, 3] > 1][:, 7])) if len(items) else 0
-    launches_per_step = skv.splitkv_plan_launches_per_call(sess.plan)
-
-    # rotating KV pools: total > 4x L2
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
-    pool_bytes = x.k_pages.numel() * x.k_pages.element_size() + (
-        0 if x.v_pages is None else x.v_pages.numel() * x.v_pages.element_size())
-    R = max(2, min(256, math.ceil(4 * l2 / pool_bytes)))
-    pools = [(x.k_pages.clone(), None if x.v_pages is None else x.v_pages.clone()) for _ in range(R - 1)]
-    pools.insert(0, (x.k_pages, x.v_pages))
-
-    def step(i):
-        k, v = pools[i % R]
-        sess.run(tensors=(x.q, k, v, x.block_table, x.seq_lens))
-
-    # eager warm-up (also sets up per-process kernel attributes before capture)
-    for i in range(max(3, min(args.warmup, R))):
-        step(i)
-    torch.cuda.synchronize()
-    log, status = sess.stats()
-    assert status == 0, f"device status {status}"
-    nonempty = float((log[:, 2] > 0).mean()) if len(log) else 1.0
-
-    def capture(n, start):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(n):
-                step(start + i)
-        return g
-
-    cycle = capture(R, 0)
+    barrier(world)
     K = args.steps
-    reps, rem = divmod(K, R)
-    tail = capture(rem, 0) if rem else None
-
-    # graph warm-up + clock soak (same work), then the timed region
-    sampler = ClockSampler(local)
-    sampler.start()
-    for _ in range(max(1, math.ceil(args.warmup / R))):
-        cycle.replay()
-    torch.cuda.synchronize()
-    t_end = time.perf_counter() + args.soak_seconds
-    while time.perf_counter() < t_end:
-        for _ in range(20):
-            cycle.replay()
-        torch.cuda.synchronize()
-
-    stream = torch.cuda.current_stream()
-    # The split-KV kernel alone (splitkv_decode_partials, the first launch of
-    # each call), timed the same way on the same stream: its average launch
-    # duration is the roofline's denominator.  With the fused combine the
-    # split kernel is the step's only launch and the step time is used.
-    kernel_us = None
-    if args.combine == "separate":
-        def step_partials(i):
-            k, v = pools[i % R]
-            sess.run_partials(tensors=(x.q, k, v, x.block_table, x.seq_lens))
-
-        pg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(pg):
-            for i in range(R):
-                step_partials(i)
-        for _ in range(3):
-            pg.replay()
-        torch.cuda.synchronize()
-        p_reps = max(1, min(max(1, K // R), math.ceil(2000 / R)))
-        p0 = torch.cuda.Event(enable_timing=True)
-        p1 = torch.cuda.Event(enable_timing=True)
-        p0.record(stream)
-        for _ in range(p_reps):
-            pg.replay()
-        p1.record(stream)
-        p1.synchronize()
-        kernel_us = p0.elapsed_time(p1) * 1e3 / (p_reps * R)
-        del pg
-
+    r = measure(w, dev, splits=args.splits, fixed=args.fixed, mode=mode, layout=args.layout,
+                pool=args.pool, steps=K, warmup=args.warmup, soak_seconds=args.soak_seconds,
+                sampler=ClockSampler(local))
+    r["name"] = w.name
     barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        cycle.replay()
-    if tail is not None:
-        tail.replay()
-    e1.record(stream)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
-    clocks = sampler.stop()
-    ms_local = e0.elapsed_time(e1)
-    ms = max_over_ranks(ms_local, world)
-    us_per_call_local = ms_local * 1e3 / K
+    x, sess, items, R = r["x"], r["sess"], r["items"], r["R"]
+    us_local = r["us"]
+    ms = max_over_ranks(us_local * K / 1e3, world)
     value = ms * 1e3 / (K * world)
-
-    log, status = sess.stats()
-    assert status == 0, f"device status {status} after the timed region"
-
-    # roofline of the split-KV kernel
-    nbytes = algorithmic_bytes(w, x.seq_lens_host)
-    nflops = algorithmic_flops(w, x.seq_lens_host)
-    hbm_peak, tc_peak, peak_kind = measured_peaks()
-    launch_us = kernel_us if kernel_us is not None else us_per_call_local
-    if is_tensor_bound(w):
-        roof = {"bound": "tensor", "achieved": nflops / (launch_us * 1e-6) / 1e12, "peak": tc_peak,
-                "unit": "TFLOP/s", "algorithmic_flops": nflops,
-                "hbm_gbs": nbytes / (launch_us * 1e-6) / 1e9, "kernel": "mla_splitkv_kernel"}
-    else:
-        achieved = nbytes / (launch_us * 1e-6) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac_of_8tbs": achieved / NOMINAL_HBM_GBS, "kernel": "gqa_splitkv_kernel"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = r["roof"]
     # the captures ran the default configuration (planner splits, separate
     # combine, host plan, HND pages); other configurations report no traffic
     default_cfg = (args.splits == 0 and not args.fixed and args.combine == "separate"
                    and args.layout == "hnd"
                    and args.page_size in (0, workloads.WORKLOADS[args.workload].page_size))
     traffic, traffic_src = PROFILED_TRAFFIC.get(w.name, (None, None)) if default_cfg else (None, None)
-    roof.update({"traffic": traffic, "traffic_source": traffic_src,
-                 "duration_basis": ("split-KV kernel alone (splitkv_decode_partials), CUDA-graph "
-                                    "replay, CUDA events on the launching stream"
-                                    if kernel_us is not None else
-                                    "timed-region time per call (the split kernel is the only launch)"),
-                 "kernel_us": launch_us, "step_us": us_per_call_local,
-                 "peak_kind": peak_kind, "algorithmic_bytes": nbytes})
+    roof.update({"traffic": traffic, "traffic_source": traffic_src})
 
+    stream = torch.cuda.current_stream()
     # cold calls: L2 flushed (a buffer of twice its size written) before each
     # call, events around the call only; the median of a few, for context
-    cold_us = run_cold(x, sess, l2, stream)
+    cold_us = run_cold(x, sess, l2_bytes(dev), stream)
 
-    # end to end: host buffers, copies inside the timed region
-    e2e = run_e2e(args, x, sess, dev)
+    # end to end: host buffers, copies inside the timed region, through a
+    # session over the workload's own pool and block table
+    e2e_sess = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens,
+                             x.seq_lens_host, scale=x.scale, kv_scale=x.kv_scale,
+                             num_splits=args.splits, v_dim=w.v_dim, v_shares_k=w.v_shares_k,
+                             combine_mode=mode, fixed=args.fixed,
+                             kv_layout=skv.SPLITKV_LAYOUT_NHD if args.layout == "nhd"
+                             else skv.SPLITKV_LAYOUT_HND)
+    e2e = run_e2e(args, x, e2e_sess, dev)
 
+    pool_desc = (f"one pool of {R} x {x.k_pages.shape[0]} pages in random order, a block table per "
+                 f"step ({R * r['pool_bytes'] / 2**20:.0f} MiB > 4x L2 {l2_bytes(dev) / 2**20:.0f} MiB)"
+                 if args.pool == "single" else
+                 f"inputs rotate over {R} KV pools ({R * r['pool_bytes'] / 2**20:.0f} MiB > 4x L2 "
+                 f"{l2_bytes(dev) / 2**20:.0f} MiB)")
     line = {
         "metric": METRIC, "value": value, "unit": "us", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": False,
@@ -448,19 +637,20 @@ def run_ours(args, rank, world, local):
                    "num_splits": args.splits, "planned_items": int(len(items)),
                    "plan": "capacity plan, items derived from the device lengths each step" if args.fixed else "host",
                    "combine": args.combine, "parallelism": f"replicas{world}",
-                   "l2": f"inputs rotate over {R} KV pools ({R * pool_bytes / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
-                   "timing": "CUDA-graph replay of back-to-back calls, CUDA events on the launching stream"},
+                   "l2": pool_desc,
+                   "timing": "CUDA-graph replay of back-to-back calls (every graph replayed "
+                             "before timing), CUDA events on the launching stream"},
         "roofline": roof,
-        "nonempty_cta_fraction": nonempty,
+        "nonempty_cta_fraction": r["nonempty"],
         "cold_us_per_call": cold_us,
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * r["launches_per_step"],
         "e2e": e2e,
-        "clocks": clocks,
+        "clocks": r["clocks"],
     }
+    if rank == 0 and world == 1 and not args.no_per_config:
+        line["per_config"] = per_config(dev, args, r)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        us, n = time_oracle(w, x, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
-                                "sample": oracle_sample_desc(w, n)}
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

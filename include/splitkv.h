@@ -341,12 +341,28 @@ splitkv_status splitkv_combine_workspace(const splitkv_plan_t* plan, void* works
  *     status word) and then decodes.  All calls share the one array and it
  *     keeps the last call's contents, so calls that overlap on the GPU (other
  *     streams, other threads) race; serialise them on one stream.
+ *   - The call's status word and per-CTA log are read with
+ *     splitkv_noalloc_read_stats.
  */
 splitkv_status splitkv_decode_noalloc(const splitkv_plan_t* plan, const void* q,
                                       const void* k_pages, const void* v_pages,
                                       const int32_t* block_table, const int32_t* seq_lens,
                                       int32_t num_splits, float scale, float kv_scale,
                                       void* out, float* lse, void* stream);
+
+/*
+ * splitkv_noalloc_read_stats -- splitkv_read_stats for the decodes of
+ * splitkv_decode_noalloc, whose status word and per-CTA log live in the
+ * library's scratch array rather than a caller workspace.  It synchronises
+ * `stream` and copies the log and status of the last splitkv_decode_noalloc
+ * call on the current device (which should be a call with this plan: the
+ * array holds whatever the last call left).  Arguments and fields as
+ * splitkv_read_stats.  No counterpart on the pages.
+ * EINVAL for a NULL plan or a too-small capacity; EWORKSPACE for a plan larger
+ * than the array (it can never have run there).
+ */
+splitkv_status splitkv_noalloc_read_stats(const splitkv_plan_t* plan, int32_t* cta_log_host,
+                                          int32_t capacity, int32_t* status_host, void* stream);
 
 /*
  * splitkv_combine -- the log-sum-exp merge on its own, over caller buffers.
@@ -392,11 +408,16 @@ enum {
 
 /*
  * splitkv_debug_gather -- copies keys [0, n_keys) of sequence b, KV head h_kv
- * through the block table into dst_host-shaped device memory `dst`
- * ([n_keys][row_bytes / element size] raw elements), using the same TMA
- * tensor-map loads and swizzled shared-memory reads as the decode kernel.
- * `pages` is k_pages or v_pages in desc->kv_layout, `row_elems` its last
- * dimension.  For checking the paged gather bit for bit.
+ * through the block table into device memory `dst` ([n_keys][row_elems] raw
+ * elements), using the same TMA tensor-map loads and swizzled shared-memory
+ * reads as the decode kernel.  For checking the paged gather bit for bit.
+ *   GQA:  `pages` is k_pages or v_pages in desc->kv_layout; row_elems = 128.
+ *   MLA:  `pages` is the latent cache (row_elems = qk_dim = 576) or, with
+ *         v_shares_k = 0, the separate V tensor (row_elems = v_dim = 512);
+ *         h_kv = 0; rows come in the decode kernel's 64-key blocks of 64-column
+ *         boxes (one box per page for pages of 16 or 32 keys).
+ * Page ids outside [0, num_pages_total) are read as page 0, as the decode
+ * kernels do.  EINVAL for other row widths, ranges or misaligned buffers.
  */
 splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* pages,
                                     int32_t row_elems, const int32_t* block_table,

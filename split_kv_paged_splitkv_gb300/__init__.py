@@ -64,6 +64,7 @@ _SIGNATURES = {
     "splitkv_decode_kv_scales": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _vp, _vp, _vp,
                                         _vp, _vp]),
     "splitkv_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp, _vp]),
+    "splitkv_noalloc_read_stats": (_i32, [_vp, _vp, _i32, _vp, _vp]),
     "splitkv_decode_partials": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _f32, _vp, _vp,
                                        _vp]),
     "splitkv_combine_workspace": (_i32, [_vp, _vp, _vp, _vp, _vp]),
@@ -272,6 +273,17 @@ def splitkv_read_stats(plan: Plan, workspace, stream=None):
     st = np.zeros(1, dtype=np.int32)
     _check(_lib.splitkv_read_stats(plan.handle, _ptr(workspace), log.ctypes.data, log.shape[0],
                                    st.ctypes.data, _stream(stream)))
+    return log[:n], int(st[0])
+
+
+def splitkv_noalloc_read_stats(plan: Plan, stream=None):
+    """(cta_log [n_ctas][4] int32, status int) of the last splitkv_decode_noalloc
+    call on the current device (synchronises the stream)."""
+    n = splitkv_plan_num_ctas(plan)
+    log = np.zeros((max(n, 1), 4), dtype=np.int32)
+    st = np.zeros(1, dtype=np.int32)
+    _check(_lib.splitkv_noalloc_read_stats(plan.handle, log.ctypes.data, log.shape[0],
+                                           st.ctypes.data, _stream(stream)))
     return log[:n], int(st[0])
 
 

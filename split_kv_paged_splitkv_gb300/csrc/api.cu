@@ -547,12 +547,27 @@ splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* page
   splitkv_status st = validate_desc(desc);
   if (st != SPLITKV_OK) return st;
   if (!pages || !block_table || !dst) return fail(SPLITKV_EINVAL, "NULL pointer");
-  if (row_elems != 128) return fail(SPLITKV_EUNSUPPORTED, "debug gather supports 128-wide rows");
   if (b < 0 || b >= desc->batch || h_kv < 0 || h_kv >= desc->num_kv_heads)
     return fail(SPLITKV_EINVAL, "b or h_kv out of range");
   if (n_keys < 0 || int64_t(n_keys) > int64_t(desc->max_pages_per_seq) * desc->page_size)
     return fail(SPLITKV_EINVAL, "n_keys out of range");
   if (!aligned16(pages) || !aligned16(dst)) return fail(SPLITKV_EINVAL, "misaligned buffers");
+  if (family_of(*desc) == Family::kMla) {
+    // the latent key rows (qk_dim wide) or a separate V tensor (v_dim wide)
+    if (row_elems != desc->qk_dim && !(row_elems == desc->v_dim && !desc->v_shares_k))
+      return fail(SPLITKV_EINVAL, "row_elems (%d) must be qk_dim, or v_dim for a separate V tensor",
+                  row_elems);
+    TmaDesc t;
+    const int64_t rows_total = int64_t(desc->num_pages_total) * desc->page_size;
+    st = make_bf16_map(&t, pages, row_elems, rows_total, desc->page_size < 64 ? desc->page_size : 64);
+    if (st != SPLITKV_OK) return st;
+    cudaError_t e = launch_mla_debug_gather(t, block_table + size_t(b) * desc->max_pages_per_seq,
+                                            desc->page_size, desc->num_pages_total, row_elems,
+                                            n_keys, dst, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the gather kernel");
+    return SPLITKV_OK;
+  }
+  if (row_elems != 128) return fail(SPLITKV_EINVAL, "GQA rows are 128 wide");
   const bool fp8 = desc->kv_dtype == SPLITKV_FP8_E4M3;
   TmaDesc t;
   st = make_gqa_map(&t, pages, fp8, desc->page_size, desc->num_kv_heads, desc->num_pages_total, 1,

@@ -444,34 +444,76 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   const int rph = a.T * a.G;           // query rows per KV head
   // scores -> log2 units: scale (and the e4m3 K scale, per KV head if given)
   const float qk_l2 = a.k_scale ? a.qk_scale_log2 * __ldg(a.k_scale + hkv) : a.qk_scale_log2;
+  // Per query row of this lane's scores (rows 2ti, 2ti + 1 of the slot's row
+  // group): qk_l2 times the inverse of the power of two the row's f16 query
+  // fragments were scaled by (e4m3 path; 1 for bf16).
+  float qk0 = qk_l2, qk1 = qk_l2;
 
   // Q^T operand fragments: query row n = 8 rg + gi of this head, dims by ti
   // (see the layout notes); rows past the head's T*G rows are zero.
   uint32_t qf[8][2];
   {
     const int n = rg * 8 + gi;
-    if (n < rph) {
-      const int t = n / a.G, g = n - t * a.G;
-      const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) +
-                                ((size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g) * 128;
+    if (!FP8) {
+      if (n < rph) {
+        const int t = n / a.G, g = n - t * a.G;
+        const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) +
+                                  ((size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g) * 128;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (!FP8) {
+        for (int ks = 0; ks < 8; ++ks) {
           qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * ti));
           qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * ti + 8));
-        } else {
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+      }
+    } else {
+      // The f16 MMA needs f16 queries, whose range (|x| < 65,520, normal from
+      // 2^-14) is far narrower than bf16's.  Each row is scaled by 2^k so that
+      // its largest component lies in [2^14, 2^15): a power of two is exact,
+      // and every component then rounds to f16 without loss unless it is
+      // below 2^-29 of the row maximum (a term 2^-29 of the largest one).  The
+      // row's score scale takes the factor 2^-k.  The four lanes ti of a row
+      // (lanes 4 gi .. 4 gi + 3) hold its 128 dims.
+      float f[8][4];
+      float amax = 0.f;
+      if (n < rph) {
+        const int t = n / a.G, g = n - t * a.G;
+        const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) +
+                                  ((size_t(b) * a.T + t) * a.Hq + size_t(hkv) * a.G + g) * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
           // k = 2ti, 2ti+1 <-> d = 16ks+4ti, +1 ; k = 2ti+8, 2ti+9 <-> d = 16ks+4ti+2, +3
           // (the byte order of the e4m3 K operand, see the QK product below)
           const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qp + ks * 16 + 4 * ti));
-          const float f0 = __uint_as_float(raw.x << 16), f1 = __uint_as_float(raw.x & 0xffff0000u);
-          const float f2 = __uint_as_float(raw.y << 16), f3 = __uint_as_float(raw.y & 0xffff0000u);
-          qf[ks][0] = pack_f16(f0, f1);
-          qf[ks][1] = pack_f16(f2, f3);
-        }
-      }
-    } else {
+          f[ks][0] = __uint_as_float(raw.x << 16);
+          f[ks][1] = __uint_as_float(raw.x & 0xffff0000u);
+          f[ks][2] = __uint_as_float(raw.y << 16);
+          f[ks][3] = __uint_as_float(raw.y & 0xffff0000u);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+          for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(f[ks][i]));
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) f[ks][0] = f[ks][1] = f[ks][2] = f[ks][3] = 0.f;
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      // k = 14 - floor(log2 amax), within [-113, 126] so that 2^k and 2^-k are
+      // normal floats (a zero row keeps k = 0)
+      int k = 0;
+      if (amax > 0.f) k = min(126, max(-113, 14 - (int((__float_as_uint(amax) >> 23) & 0xff) - 127)));
+      const float up = __uint_as_float(uint32_t(127 + k) << 23);
+      const float down = __uint_as_float(uint32_t(127 - k) << 23);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qf[ks][0] = pack_f16(f[ks][0] * up, f[ks][1] * up);
+        qf[ks][1] = pack_f16(f[ks][2] * up, f[ks][3] * up);
+      }
+      // rows 2ti and 2ti + 1 are held by lanes 8 ti and 8 ti + 4
+      qk0 = qk_l2 * __shfl_sync(kFull, down, 8 * ti);
+      qk1 = qk_l2 * __shfl_sync(kFull, down, 8 * ti + 4);
     }
   }
   // Visible-key limits of the two query rows whose scores this lane holds.
@@ -549,8 +591,8 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
     for (int r = 0; r < 4; ++r) sc[r] += sd[r];
 
     // ---- scores in log2 units, masked
-    float s0 = sc[0] * qk_l2, s1 = sc[1] * qk_l2;
-    float s2 = sc[2] * qk_l2, s3 = sc[3] * qk_l2;
+    float s0 = sc[0] * qk0, s1 = sc[1] * qk1;
+    float s2 = sc[2] * qk0, s3 = sc[3] * qk1;
     if (key0 + 15 > min_lim) {
       const int ka = key0 + gi, kb = ka + 8;
       s0 = ka <= lim0 ? s0 : -INFINITY;

@@ -137,5 +137,9 @@ cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n
                                void* stream);
 cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, const int32_t* table_row,
                                 int32_t h_kv, int32_t P, int32_t n_keys, void* dst, void* stream);
+// The MLA family's gather (2-D latent or separate-V map, row_elems 576 or 512).
+cudaError_t launch_mla_debug_gather(const TmaDesc& t, const int32_t* table_row, int32_t P,
+                                    int32_t num_pages, int32_t row_elems, int32_t n_keys, void* dst,
+                                    void* stream);
 
 }  // namespace splitkv

@@ -661,6 +661,61 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
   }
 }
 
+// Copies keys [0, n_keys) of one sequence's latent (or separate V) rows
+// through the block table with the decode kernel's tensor map, boxes and
+// 128-byte-swizzled shared-memory addressing: per 64-key block and 64-column
+// chunk, one box of 64 rows at the block's row offset (pages of 64 keys or a
+// multiple of 64), or one box of P rows per page written P * 128 bytes apart
+// (pages of 16 or 32 keys).  One CTA of 128 threads; one chunk at a time.
+// Page ids outside [0, num_pages) are read as page 0, as in the decode kernel.
+__global__ void __launch_bounds__(128) mla_gather_debug_kernel(const __grid_constant__ CUtensorMap tm,
+                                                               const int32_t* table_row, int P,
+                                                               int num_pages, int row_elems,
+                                                               int n_keys, uint8_t* dst) {
+  __shared__ __align__(1024) uint8_t chunk[Mla::K_CH];
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int small = P < Mla::BK;
+  const int br = small ? P : Mla::BK;  // rows per box
+  const int n_pages = (n_keys + P - 1) / P;
+  const int n_chunks = row_elems / 64;
+  int phase = 0;
+  for (int key0 = 0; key0 < n_keys; key0 += Mla::BK) {
+    for (int c = 0; c < n_chunks; ++c, ++phase) {
+      if (threadIdx.x == 0) {
+        const int nb = small ? min(Mla::BK / P, n_pages - key0 / P) : 1;
+        mbar_arrive_expect_tx(smem_u32(&bar), uint32_t(nb * br * 128));
+        for (int r = 0; r < nb; ++r) {
+          const int page = small ? key0 / P + r : key0 / P;
+          const int off = small ? 0 : key0 - page * P;
+          int ph = table_row[page];
+          if (ph < 0 || ph >= num_pages) ph = 0;
+          tma_load_2d_warp_lane(smem_u32(chunk + r * br * 128), &tm, smem_u32(&bar), c * 64,
+                                ph * P + off);
+        }
+      }
+      if (!__syncthreads_and(mbar_wait(smem_u32(&bar), phase & 1))) {
+        // one more bounded wait so the copy is not left writing into freed smem
+        if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), phase & 1);
+        __syncthreads();
+        return;
+      }
+      const int rows = min(Mla::BK, n_keys - key0);
+      for (int x = threadIdx.x; x < rows * 8; x += blockDim.x) {
+        const int i = x >> 3, seg = x & 7;
+        const uint32_t off = uint32_t(i * 128 + ((seg ^ (i & 7)) << 4));
+        *reinterpret_cast<uint4*>(dst + (size_t(key0 + i) * row_elems + c * 64 + seg * 8) * 2) =
+            *reinterpret_cast<const uint4*>(chunk + off);
+      }
+      __syncthreads();
+    }
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -697,6 +752,15 @@ cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv
     return small ? launch_mla_t<true, true>(a, mk, mv, s) : launch_mla_t<true, false>(a, mk, mv, s);
   }
   return small ? launch_mla_t<false, true>(a, mk, mk, s) : launch_mla_t<false, false>(a, mk, mk, s);
+}
+
+cudaError_t launch_mla_debug_gather(const TmaDesc& t, const int32_t* table_row, int32_t P,
+                                    int32_t num_pages, int32_t row_elems, int32_t n_keys, void* dst,
+                                    void* stream) {
+  const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(&t);
+  mla_gather_debug_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      m, table_row, P, num_pages, row_elems, n_keys, static_cast<uint8_t*>(dst));
+  return cudaGetLastError();
 }
 
 }  // namespace splitkv

@@ -80,3 +80,21 @@ extern "C" splitkv_status splitkv_decode_noalloc(const splitkv_plan_t* plan, con
   return splitkv_decode(plan, scratch, q, k_pages, v_pages, block_table, seq_lens, num_splits,
                         scale, kv_scale, out, lse, stream);
 }
+
+// The status word and per-CTA log of the last splitkv_decode_noalloc call on
+// the current device live in the scratch array, whose address callers never
+// see: this reads them the way splitkv_read_stats reads a caller workspace.
+extern "C" splitkv_status splitkv_noalloc_read_stats(const splitkv_plan_t* plan,
+                                                     int32_t* cta_log_host, int32_t capacity,
+                                                     int32_t* status_host, void* stream) {
+  if (!plan) return fail(SPLITKV_EINVAL, "plan is NULL");
+  if (plan->total > kNoAllocScratchBytes)
+    return fail(SPLITKV_EWORKSPACE,
+                "this plan needs %zu bytes of scratch, more than splitkv_decode_noalloc holds "
+                "(%zu bytes), so it never ran there",
+                plan->total, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  splitkv_status st = scratch_for_current_device(&scratch);
+  if (st != SPLITKV_OK) return st;
+  return splitkv_read_stats(plan, scratch, cta_log_host, capacity, status_host, stream);
+}

@@ -160,6 +160,16 @@ __device__ __forceinline__ void tma_load_2d_warp(uint32_t dst, const CUtensorMap
 }
 
 
+// The same 2-D tiled load issued by a single thread (no elect.sync).
+__device__ __forceinline__ void tma_load_2d_warp_lane(uint32_t dst, const CUtensorMap* m,
+                                                      uint32_t bar, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d_warp(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                                  int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
   asm volatile(

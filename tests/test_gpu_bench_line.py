@@ -3,7 +3,8 @@
 A short run of the default workload (few steps, short CPU-baseline sample):
 the metric and config, the roofline object (bound, achieved, peak, frac,
 traffic), the CPU baseline, the end-to-end leg with host-copy byte counts,
-the clock record and the launch count, each with a sane value.
+the clock record and the launch count, each with a sane value; the
+per-workload entries of every configuration of the suite.
 """
 import json
 import os
@@ -39,6 +40,15 @@ def test_bench_line_has_every_key():
     assert roof["traffic"] is None or roof["traffic"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    pc = d["per_config"]
+    for name in ("tiny_gqa_ctx260", "gqa_ctx5900", "fp8_batch8_ctx32k", "mla_t6_ctx64k",
+                 "mixed_batch32_bf16", "mixed_batch32_fp8"):
+        e = pc[name]
+        assert e["us_per_call"] > 0 and e["kernel_us"] > 0 and 0 < e["frac"] < 2, name
+        assert e["nonempty_cta_fraction"] == 1.0, name
+    assert pc["mla_t6_ctx64k"]["roofline_bound"] == "tensor"
+    assert pc["gqa_ctx5900"]["us_per_call"] == d["value"]
     e2e = d["e2e"]
     assert e2e["value"] > d["value"] and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["clocks"]["sm_max_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)

@@ -257,21 +257,109 @@ def test_fp8_batch8_ctx32k_full():
 
 
 @pytest.mark.parametrize("name", ["mixed_batch32_bf16", "mixed_batch32_fp8"])
-def test_mixed_batch32_sampled(name):
-    """Full-size run; the oracle checks every head of 5 sequences (longest,
-    shortest and three seeded picks)."""
+def test_mixed_batch32_full(name):
+    """Full-size run (32 sequences of 256 to 131,072 keys, planner splits),
+    every output row of every sequence against the oracle."""
     w = W[name]
     x = workloads.make_inputs(w, device="cuda")
     s = session(x, 0)
     out, lse = s.run()
     log, status = s.stats()
     assert status == 0 and (log[:, 2] > 0).all()
-    lens = x.seq_lens_host
-    rng = np.random.default_rng(5)
-    picks = sorted({int(np.argmax(lens)), int(np.argmin(lens)), *rng.choice(w.batch, 3, replace=False).tolist()})
-    rows = [(b, 0, h) for b in picks for h in range(w.num_q_heads)]
-    ref_o, ref_l = oracle_direct(x, rows=rows)
-    compare(out, lse, ref_o, ref_l, rows=rows, what=name)
+    ref_o, ref_l = oracle_direct(x)
+    compare(out, lse, ref_o, ref_l, what=name)
+
+
+# ------------------------------------------------------------------ query magnitudes (e4m3)
+
+@pytest.mark.parametrize("T,G", [(1, 8), (2, 8), (1, 4)])
+def test_e4m3_queries_of_any_bf16_magnitude(T, G):
+    """The e4m3 path multiplies bf16 queries with f16 tensor-core products;
+    each query row is scaled by a power of two into f16's range first.  Rows
+    drawn at |q| ~ 1e5 (beyond f16's largest value), ~1e-6 (below its
+    normal range), ~1 and with components spread over 2^-20 .. 2^16 in one
+    row must match the oracle; K carries per-head scales that keep every
+    row's scores of order one, so the softmax is not trivially flat."""
+    lens = [T + 2, 300, 1000, 16 * 7]
+    w = _custom(lens, G=G, Hkv=2, T=T, fp8=True, seed=80 + T + G)
+    x = workloads.make_inputs(w, device="cuda")
+    c = float(x.kv_scale)
+    rng = np.random.default_rng(T * 10 + G)
+    for mag in (1e5, 1e-6, "spread"):
+        q = x.q.float().clone()
+        if mag == "spread":
+            # per component 2^e, e uniform in [-20, 16], random sign: row maxima
+            # around 2^16 (> 65,504) with tiny components alongside
+            e = torch.from_numpy(rng.uniform(-20, 16, size=tuple(q.shape))).float().to(q.device)
+            q = torch.sign(q) * torch.exp2(e)
+            kscale = c / 2.0 ** 16
+        else:
+            q = q * mag
+            kscale = c / mag
+        q = q.to(torch.bfloat16)
+        ks = np.full(2, kscale, np.float32)
+        vs = np.full(2, c, np.float32)
+        ref_o, ref_l = oracle.attention_direct(
+            workloads.bits(q), workloads.bits(x.k_pages), workloads.bits(x.v_pages),
+            x.block_table.cpu().numpy(), x.seq_lens_host, scale=x.scale, kv_dtype="fp8_e4m3",
+            k_scale=ks.astype(np.float64), v_scale=vs.astype(np.float64))
+        kt = torch.tensor(ks, device="cuda")
+        vt = torch.tensor(vs, device="cuda")
+        for S in (1, 3):
+            sess = DecodeSession(q, x.k_pages, x.v_pages, x.block_table, x.seq_lens,
+                                 x.seq_lens_host, scale=x.scale, num_splits=S, k_scale=kt,
+                                 v_scale=vt)
+            out, lse = sess.run()
+            compare(out, lse, ref_o, ref_l, what=f"|q| {mag} T={T} G={G} S={S}")
+            assert sess.stats()[1] == 0
+        # the per-tensor scale path with the same magnitudes: K and V share
+        # kv_scale, so the outputs scale with it; compare relative to the
+        # output's own size
+        if mag != "spread":
+            ref_o2, ref_l2 = oracle.attention_direct(
+                workloads.bits(q), workloads.bits(x.k_pages), workloads.bits(x.v_pages),
+                x.block_table.cpu().numpy(), x.seq_lens_host, scale=x.scale, kv_dtype="fp8_e4m3",
+                kv_scale=float(np.float32(kscale)))
+            sess = DecodeSession(q, x.k_pages, x.v_pages, x.block_table, x.seq_lens,
+                                 x.seq_lens_host, scale=x.scale, kv_scale=kscale, num_splits=3)
+            out, lse = sess.run()
+            o = out.float().cpu().numpy()
+            assert np.isfinite(o).all()
+            peak = np.abs(ref_o2).max()
+            assert np.abs(o - ref_o2).max() <= 1e-2 * peak, mag
+            assert np.abs(lse.cpu().numpy() - ref_l2).max() <= LSE_TOL, mag
+
+
+# ------------------------------------------------------------------ out-of-range page ids
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("S", [1, 3, 0])
+def test_out_of_range_page_ids_are_flagged(fp8, S):
+    """A block-table entry >= num_pages and a negative one: the kernel reads
+    page 0 in their place (never outside the pool), sets
+    SPLITKV_DEVERR_PAGE in the status word, keeps the output finite, and the
+    sequences whose tables are intact still match the oracle."""
+    # lengths are whole pages, so no page (page 0 included) holds the poisoned
+    # tail slots a partly filled last page carries
+    w = _custom([304, 704, 1008, 208], G=8, Hkv=4, fp8=fp8, seed=95 + fp8)
+    x = workloads.make_inputs(w, device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    bad = x.block_table.clone()
+    bad[1, 5] = x.num_pages + 7
+    bad[3, 2] = -4
+    s = session(x, S)
+    out, lse = s.run(tensors=(x.q, x.k_pages, x.v_pages, bad, x.seq_lens))
+    log, status = s.stats()
+    assert status & skv.SPLITKV_DEVERR_PAGE
+    assert not status & skv.SPLITKV_DEVERR_TIMEOUT
+    assert torch.isfinite(out.float()).all()
+    rows = [(b, 0, h) for b in (0, 2) for h in range(w.num_q_heads)]
+    compare(out, lse, ref_o, ref_l, rows=rows, what=f"intact sequences fp8={fp8} S={S}")
+    # the status word is sticky until the next upload; a clean call after a
+    # fresh upload reports nothing
+    s2 = session(x, S)
+    s2.run()
+    assert s2.stats()[1] == 0
 
 
 # ------------------------------------------------------------------ combine

@@ -41,11 +41,50 @@ def test_mla_small_ragged(T, sepv):
         compare(out, lse, ref_o, ref_l, what=f"T={T} S={S}")
         log, status = s.stats()
         assert status == 0, status
-        items = skv.splitkv_plan_get_items(s.plan)
-        # 2*T CTAs per item, in item order; every CTA scored its item's keys
-        nonempty = np.repeat(items[:, 5] > items[:, 4], 2 * T)
-        assert (log[nonempty, 2] > 0).all()
-        assert (log[:, 3] == 0).all()
+        _check_cta_ranges(s, x, T)
+
+
+def _check_cta_ranges(s, x, T):
+    """The per-CTA log equals the plan exactly: 2*T CTAs per work item (token
+    t, V half h), each iterating its item's page range [p0, p1) and scoring
+    the keys min(p1 * P, L) - p0 * P of it, with no abort record."""
+    items = skv.splitkv_plan_get_items(s.plan)
+    log, _ = s.stats()
+    assert len(log) == 2 * T * len(items)
+    P = x.w.page_size
+    L = x.seq_lens_host[items[:, 0]].astype(np.int64)
+    keys = np.maximum(0, np.minimum(items[:, 5].astype(np.int64) * P, L) - items[:, 4] * P)
+    assert np.array_equal(log[:, 0], np.repeat(items[:, 4], 2 * T))
+    assert np.array_equal(log[:, 1], np.repeat(items[:, 5], 2 * T))
+    assert np.array_equal(log[:, 2], np.repeat(keys, 2 * T))
+    assert (log[:, 3] == 0).all()
+    # and the planner's ranges equal the oracle's split table
+    ref = oracle.plan_items(list(x.seq_lens_host), P, 1, s.num_splits,
+                            torch.cuda.get_device_properties(0).multi_processor_count,
+                            ctas_per_item=2 * T, ctas_per_sm=1)
+    assert np.array_equal(items[:, :6], np.array(ref, np.int32).reshape(-1, 6))
+
+
+@pytest.mark.parametrize("P", [16, 32, 64, 128])
+@pytest.mark.parametrize("sepv", [False, True])
+def test_mla_paged_gather_is_bit_exact(P, sepv):
+    """The latent rows (576 wide) and, with a separate V tensor, the V rows
+    (512 wide), read through the block table with the decode kernel's tensor
+    maps and swizzled addressing, equal the CPU gather bit for bit."""
+    lens = [3, P + 7, 777, 64 * 3]
+    x = workloads.make_inputs(_mla(lens, 2, seed=70 + P + sepv, v_shares_k=not sepv, P=P),
+                              device="cuda")
+    desc = skv.make_desc(len(lens), 2, 128, 1, 576, 512, P, x.max_pages, x.num_pages,
+                         skv.SPLITKV_BF16, int(not sepv))
+    tables = x.block_table.cpu().numpy()
+    for b, L in enumerate(x.seq_lens_host):
+        L = int(L)
+        for pages, width in ((x.k_pages, 576),) + (((x.v_pages, 512),) if sepv else ()):
+            dst = torch.zeros((L, width), dtype=torch.bfloat16, device="cuda")
+            skv.splitkv_debug_gather(desc, pages, width, x.block_table, b, 0, L, dst)
+            torch.cuda.synchronize()
+            ref = oracle.gather_keys(workloads.bits(pages), tables[b], L, 0)
+            assert np.array_equal(workloads.bits(dst), ref), (b, width)
 
 
 @pytest.mark.parametrize("name", ["mla_t6_ctx64k", "mla_sepv_t6_ctx64k"])
@@ -78,4 +117,29 @@ def test_mla_page_sizes(P, sepv):
         compare(out, lse, ref_o, ref_l, what=f"P={P} sepv={sepv} S={S}")
         log, status = s.stats()
         assert status == 0, status
-        assert (log[:, 3] == 0).all()
+        _check_cta_ranges(s, x, T)
+
+
+@pytest.mark.parametrize("P", [16, 64])
+@pytest.mark.parametrize("sepv", [False, True])
+def test_mla_out_of_range_page_ids_are_flagged(P, sepv):
+    """As for GQA: an entry >= num_pages and a negative one are read as page
+    0, SPLITKV_DEVERR_PAGE is set, the output stays finite, and the intact
+    sequences match the oracle."""
+    T = 2
+    lens = [640, 1024, 320]  # whole pages: no poisoned tail slots in page 0
+    x = workloads.make_inputs(_mla(lens, T, seed=90 + P + sepv, v_shares_k=not sepv, P=P),
+                              device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    bad = x.block_table.clone()
+    bad[1, 2] = x.num_pages + 3
+    bad[2, 0] = -1
+    for S in (1, 3):
+        s = session(x, S)
+        out, lse = s.run(tensors=(x.q, x.k_pages, x.v_pages, bad, x.seq_lens))
+        log, status = s.stats()
+        assert status & skv.SPLITKV_DEVERR_PAGE, status
+        assert not status & skv.SPLITKV_DEVERR_TIMEOUT
+        assert torch.isfinite(out.float()).all()
+        rows = [(0, t, h) for t in range(T) for h in range(128)]
+        compare(out, lse, ref_o, ref_l, rows=rows, what=f"P={P} sepv={sepv} S={S}")

@@ -1,0 +1,113 @@
+"""Performance regression tests: correct output can hide a slow split-KV path.
+
+"vLLM 0.30.0 FA4 SplitKV Bug: H100 Decode Can Be 48% Slower" (sections "Why
+the result is still correct" and "The kernel-only sweep makes the bug
+obvious"): when the requested split count never reached the kernel, every
+extra split CTA got an empty KV range, the outputs stayed right, and only a
+kernel-only sweep over num_splits showed the decode getting no faster.  The
+same sweep guards this library: the 5,900-key single-sequence decode must get
+faster at every step from 1 to 64 splits, and at 64 splits at least 8x faster
+than unsplit.  A bandwidth floor guards the long FP8 batch: its split kernel
+alone must move its algorithmic bytes at >= 0.70 of the measured HBM copy
+bandwidth.
+
+Timing: CUDA-graph replay of back-to-back calls rotating over copies of the
+KV pool whose total exceeds four times the L2 size, CUDA events on the
+launching stream, after warm-up replays.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _support import need_gpu, session
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _pools(x):
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 << 20))
+    nbytes = x.k_pages.numel() * x.k_pages.element_size() + (
+        0 if x.v_pages is None else x.v_pages.numel() * x.v_pages.element_size())
+    R = max(2, math.ceil(4 * l2 / nbytes))
+    pools = [(x.k_pages, x.v_pages)]
+    pools += [(x.k_pages.clone(), None if x.v_pages is None else x.v_pages.clone())
+              for _ in range(R - 1)]
+    return pools
+
+
+def _us_per_call(sess, x, pools, partials=False, reps=20):
+    def step(i):
+        k, v = pools[i % len(pools)]
+        t = (x.q, k, v, x.block_table, x.seq_lens)
+        if partials:
+            sess.run_partials(tensors=t)
+        else:
+            sess.run(tensors=t)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(len(pools)):
+            step(i)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    assert sess.stats()[1] == 0
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(pools))
+
+
+def test_split_sweep_gets_faster():
+    x = workloads.make_inputs(workloads.WORKLOADS["gqa_ctx5900"], device="cuda")
+    pools = _pools(x)
+    t = {}
+    for S in (1, 4, 16, 64):
+        sess = session(x, S)
+        t[S] = _us_per_call(sess, x, pools)
+        # every launched split CTA owned keys (the page's bug gave them none)
+        log, status = sess.stats()
+        assert status == 0 and (log[:, 2] > 0).all() and len(log) == 2 * S
+    msg = ", ".join(f"S={S}: {v:.2f} us" for S, v in t.items())
+    for a, b in ((1, 4), (4, 16), (16, 64)):
+        assert t[b] < 0.95 * t[a], f"more splits did not speed the decode up ({msg})"
+    assert t[1] >= 8 * t[64], f"64 splits less than 8x faster than 1 ({msg})"
+
+
+def _hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["hbm_gbs"])
+    return 6800.0  # one earlier measured copy bandwidth of this part
+
+
+def test_fp8_batch8_ctx32k_bandwidth_floor():
+    w = workloads.WORKLOADS["fp8_batch8_ctx32k"]
+    x = workloads.make_inputs(w, device="cuda")
+    pools = _pools(x)
+    sess = session(x, 0)
+    us = _us_per_call(sess, x, pools, partials=True, reps=10)
+    lens = x.seq_lens_host.astype(np.int64)
+    nbytes = int(lens.sum()) * w.num_kv_heads * 2 * w.qk_dim + w.batch * w.num_q_heads * w.qk_dim * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak = _hbm_peak()
+    assert gbs >= 0.70 * peak, f"{gbs:.0f} GB/s is below 0.70 of {peak:.0f} GB/s ({us:.1f} us)"
