@@ -71,4 +71,4 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "us"
     assert d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
     # exactly --steps timed oracle calls (the tiny call fits the CPU budget) after --warmup
-    assert d["steps"] == 2 and d["warmup"] == 1 and "repeated 2 times" in d["cpu_baseline"]["sample"]
+    assert d["steps"] == 2 and d["warmup"] == 1 and "2 calls in all" in d["cpu_baseline"]["sample"]
