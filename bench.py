@@ -541,7 +541,7 @@ def measure(w, dev, *, splits=0, fixed=False, mode=None, layout="hnd", pool="sin
 
 
 PER_CONFIG = ("tiny_gqa_ctx260", "gqa_ctx5900", "fp8_batch8_ctx32k", "mla_t6_ctx64k",
-              "mla_sepv_t6_ctx64k", "mixed_batch32_bf16", "mixed_batch32_fp8")
+              "mla_sepv_t6_ctx64k", "mla_fp8_t6_ctx64k", "mixed_batch32_bf16", "mixed_batch32_fp8")
 
 
 def per_config(dev, args, headline):

@@ -92,6 +92,24 @@ splitkv_status make_bf16_map(TmaDesc* out, const void* base, int dim, int64_t ro
   return SPLITKV_OK;
 }
 
+// 2-D uint8 map over [rows][dim] e4m3 codes with unswizzled boxes of 64
+// columns x box_rows rows (64-byte rows, the MLA kernel's FP8 staging).
+splitkv_status make_u8_map(TmaDesc* out, const void* base, int dim, int64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap m;
+  cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
+  cuuint64_t gstride[1] = {cuuint64_t(dim)};
+  cuuint32_t box[2] = {64u, cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPLITKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  std::memcpy(out, &m, sizeof(m));
+  return SPLITKV_OK;
+}
+
 splitkv_status cuda_fail(cudaError_t e, const char* what) {
   return fail(SPLITKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -122,8 +140,9 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
   if (family_of(*d) == Family::kNone)
     return fail(SPLITKV_EUNSUPPORTED,
                 "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
-                "(GQA: qk_dim=v_dim=128, T*G<=16; MLA: 128 q heads, 1 bf16 latent head, "
-                "qk_dim=576, v_dim=512, page_size 16, 32 or a multiple of 64, T<=16)",
+                "(GQA: qk_dim=v_dim=128, T*G<=16; MLA: 128 q heads, 1 latent head, "
+                "qk_dim=576, v_dim=512, page_size 16, 32 or a multiple of 64, T<=16, "
+                "e4m3 only with V in the latent rows)",
                 d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
                 d->v_shares_k);
   return SPLITKV_OK;
@@ -145,8 +164,10 @@ Family family_of(const splitkv_desc_t& d) {
   // V either shares the latent rows (their first 512 columns) or is its own
   // tensor.  Keys stream in 64-key blocks: pages of 16 or 32 keys fill a block
   // with 4 or 2 boxes, larger pages (multiples of 64) hold whole blocks.
-  if (d.qk_dim == 576 && d.v_dim == 512 && d.num_kv_heads == 1 &&
-      d.num_q_heads == 128 && d.kv_dtype == SPLITKV_BF16 && d.q_tokens <= 16 &&
+  // An e4m3 latent cache holds V in its rows (a separate e4m3 V tensor is
+  // not served).
+  if (d.qk_dim == 576 && d.v_dim == 512 && d.num_kv_heads == 1 && d.num_q_heads == 128 &&
+      (d.kv_dtype == SPLITKV_BF16 || d.v_shares_k) && d.q_tokens <= 16 &&
       (64 % d.page_size == 0 || d.page_size % 64 == 0))
     return Family::kMla;
   return Family::kNone;
@@ -414,14 +435,15 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
     // combine kernel.
     TmaDesc tk, tv;
     const int box_rows = d.page_size < 64 ? d.page_size : 64;
-    splitkv_status st = make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, box_rows);
+    splitkv_status st = fp8 ? make_u8_map(&tk, k_pages, d.qk_dim, rows_total, box_rows)
+                            : make_bf16_map(&tk, k_pages, d.qk_dim, rows_total, box_rows);
     if (st != SPLITKV_OK) return st;
     if (!d.v_shares_k) {
       st = make_bf16_map(&tv, v_pages, d.v_dim, rows_total, box_rows);
       if (st != SPLITKV_OK) return st;
     }
     a.fused = 0;
-    cudaError_t e = launch_mla(a, tk, d.v_shares_k ? nullptr : &tv, stream);
+    cudaError_t e = launch_mla(a, tk, d.v_shares_k ? nullptr : &tv, fp8, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the MLA split-KV kernel");
     if (merge) {
       e = launch_combine(a, true, stream);
@@ -559,9 +581,12 @@ splitkv_status splitkv_debug_gather(const splitkv_desc_t* desc, const void* page
                   row_elems);
     TmaDesc t;
     const int64_t rows_total = int64_t(desc->num_pages_total) * desc->page_size;
-    st = make_bf16_map(&t, pages, row_elems, rows_total, desc->page_size < 64 ? desc->page_size : 64);
+    const bool fp8 = desc->kv_dtype == SPLITKV_FP8_E4M3;
+    const int box_rows = desc->page_size < 64 ? desc->page_size : 64;
+    st = fp8 ? make_u8_map(&t, pages, row_elems, rows_total, box_rows)
+             : make_bf16_map(&t, pages, row_elems, rows_total, box_rows);
     if (st != SPLITKV_OK) return st;
-    cudaError_t e = launch_mla_debug_gather(t, block_table + size_t(b) * desc->max_pages_per_seq,
+    cudaError_t e = launch_mla_debug_gather(t, fp8, block_table + size_t(b) * desc->max_pages_per_seq,
                                             desc->page_size, desc->num_pages_total, row_elems,
                                             n_keys, dst, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the gather kernel");

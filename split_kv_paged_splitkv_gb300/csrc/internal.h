@@ -126,7 +126,9 @@ cudaError_t launch_gqa(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc& tv
                        void* stream);
 // tv: the V map of a cache with separate V rows, or null when V is the first
 // columns of the key rows
-cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, void* stream);
+// fp8: tk is an unswizzled uint8 map over e4m3 latent rows (tv must be null)
+cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, bool fp8,
+                       void* stream);
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream);
 // The FixedShape of a capacity plan over device lengths `seq_lens`.
 FixedShape fixed_shape(const splitkv_plan_s& p, const int32_t* seq_lens);
@@ -138,7 +140,7 @@ cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n
 cudaError_t launch_debug_gather(const TmaDesc& t, bool fp8, const int32_t* table_row,
                                 int32_t h_kv, int32_t P, int32_t n_keys, void* dst, void* stream);
 // The MLA family's gather (2-D latent or separate-V map, row_elems 576 or 512).
-cudaError_t launch_mla_debug_gather(const TmaDesc& t, const int32_t* table_row, int32_t P,
+cudaError_t launch_mla_debug_gather(const TmaDesc& t, bool fp8, const int32_t* table_row, int32_t P,
                                     int32_t num_pages, int32_t row_elems, int32_t n_keys, void* dst,
                                     void* stream);
 

@@ -42,6 +42,15 @@
 // warps 2-5 load Q, then softmax and epilogue (thread = query head = TMEM
 // lane), warp 6 V-ring producer.
 //
+// FP8 (an e4m3 latent cache with a per-tensor scale, V in its first 512
+// columns): TMA lands each block's e4m3 rows in the upper half of the ring
+// slot, four converter warps turn them into f16 over the whole slot (the
+// hardware e4m3 -> f16 pair conversion is exact), and the MMAs run on f16:
+// the query rows are scaled by a power of two each into f16's range (exact;
+// the row's score scale takes the inverse), P is packed as f16, and the
+// cache scale multiplies the scores and the output once.  "Xqa decode
+// kernels", section "Purpose": an FP8 KV cache read with 16-bit queries.
+//
 // Separate V (SEPV: a cache whose V rows are their own 512-wide tensor, not
 // the first columns of the key rows): the V-ring slot of block j first holds
 // the five key chunks as above; once the score MMAs of block j have read
@@ -76,7 +85,9 @@ struct Mla {
   static constexpr int OFF_V = OFF_N + NST * N_SLOT;    // V ring
   static constexpr int OFF_BAR = OFF_V + NST * V_SLOT;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr int THREADS = 224;       // 256 with separate V (warp 7 loads V)
+  static constexpr int THREADS = 224;       // 256 with separate V (warp 7 loads V),
+                                            // 352 with FP8 (warps 7-10 convert)
+  static constexpr int CONV_WARP0 = 7;      // FP8: first converter warp
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL = 0, Q_COL = 128, O_COL = 256;  // S_b at S_COL + 64 b
   static constexpr float RESCALE_LOG2 = 8.f;  // lazy maximum: rescale when it grows by > 2^8
@@ -114,13 +125,44 @@ enum {
   B_XKDONE,                         // [NST] separate V: the score MMAs have read the
                                     // key chunks of V slot s
   B_VDATA = B_XKDONE + Mla::NST,    // [NST] separate V: V rows landed in V slot s
-  B_COUNT = B_VDATA + Mla::NST
+  B_NCONV = B_VDATA + Mla::NST,     // [NST] FP8: N slot s converted to f16 (4 warps)
+  B_VCONV = B_NCONV + Mla::NST,     // [NST] FP8: V slot s converted to f16 (4 warps)
+  B_COUNT = B_VCONV + Mla::NST
 };
-static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+static_assert(B_COUNT * 8 + 12 <= 256, "barrier area (then the TMEM slot and two flags)");
 
 // Column chunk (of the nine) in N-ring slot chunk i / V-ring slot chunk k of half h.
 __device__ __forceinline__ int n_chunk(int h, int i) { return h == 0 ? 4 + i : i; }
 __device__ __forceinline__ int v_chunk(int h, int k) { return k < 4 ? 4 * h + k : 8; }
+
+// FP8: converts the e4m3 rows TMA left in the upper half of a ring slot
+// (NCH chunks of [64 rows][64 B], one byte per element) into the f16 chunks
+// the MMAs read ([64 rows][128 B] each, 128-byte swizzle) over the whole slot.
+// Run by the 128 converter threads (ct = 0..127): each first reads all its
+// staged 16-byte segments, the converters then meet at named barrier 2 (the
+// f16 rows of the first chunks overwrite the staging area of later ones), and
+// each writes its segments as f16, 16 elements -> two 16-byte pieces.
+template <int NCH>
+__device__ __forceinline__ void convert_slot(uint8_t* slot, int ct) {
+  constexpr int PER = NCH * 64 * 4 / 128;  // 16-byte staged segments per thread
+  const uint8_t* stage = slot + NCH * Mla::K_CH / 2;
+  uint4 x[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) x[i] = *reinterpret_cast<const uint4*>(stage + (i * 128 + ct) * 16);
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int g = i * 128 + ct;  // segment: chunk g / 256, row (g / 4) % 64, columns 16 (g % 4) ..
+    const int k = g >> 8, r = (g >> 2) & 63, c4 = g & 3;
+    uint8_t* row = slot + k * Mla::K_CH + r * 128;
+    const uint4 lo = make_uint4(e4m3x2_lo(x[i].x), e4m3x2_hi(x[i].x), e4m3x2_lo(x[i].y),
+                                e4m3x2_hi(x[i].y));
+    const uint4 hi = make_uint4(e4m3x2_lo(x[i].z), e4m3x2_hi(x[i].z), e4m3x2_lo(x[i].w),
+                                e4m3x2_hi(x[i].w));
+    *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = hi;
+  }
+}
 
 // Page walk of a producer warp over its split's 64-key blocks.  Pages of
 // 64 keys or a multiple of 64 hold whole blocks: a block is one box at row
@@ -172,10 +214,11 @@ struct PageWalk {
   }
 };
 
-template <bool SEPV, bool SMALLP>
-__global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
+template <bool SEPV, bool SMALLP, bool FP8>
+__global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : (FP8 ? Mla::THREADS + 128 : Mla::THREADS), 1)
     mla_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
+  static_assert(!(SEPV && FP8), "FP8 latent caches hold V in the key rows");
   using C = Mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -183,6 +226,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B_COUNT);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* conv_abort = abort_flag + 1;  // FP8: a converter warp gave up
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -243,7 +287,14 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
         mbar_init(bar(B_VDATA + s), 1);
       }
     }
+    if (FP8) {
+      for (int s = 0; s < C::NST; ++s) {
+        mbar_init(bar(B_NCONV + s), 4);
+        mbar_init(bar(B_VCONV + s), 4);
+      }
+    }
     *abort_flag = 0;
+    *conv_abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -292,13 +343,18 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
       const int st = j % C::NST;
       if (j >= C::NST) ok = __all_sync(kFull, mbar_wait(bar(empty0 + st), ((j / C::NST) - 1) & 1));
       if (!ok) break;
-      mbar_arrive_expect_tx_warp(bar(full0 + st), slot_bytes);
+      // bf16: the chunks straight into the slot; FP8: the e4m3 rows (64 bytes
+      // each) into its upper half, for the converter warps
+      mbar_arrive_expect_tx_warp(bar(full0 + st), FP8 ? slot_bytes / 2 : slot_bytes);
 #pragma unroll
       for (int r = 0; r < PageWalk<SMALLP>::NB; ++r) {
         if (r * br >= C::BK) break;
-        for (int k = 0; k < nchk; ++k)
-          tma_load_2d_warp(smem_u32(ring + st * slot_bytes + k * C::K_CH + r * br * 128), &tk,
-                           bar(full0 + st), (vring ? v_chunk(h, k) : n_chunk(h, k)) * 64, yr[r]);
+        for (int k = 0; k < nchk; ++k) {
+          uint8_t* dst = FP8 ? ring + st * slot_bytes + slot_bytes / 2 + k * (C::K_CH / 2) + r * br * 64
+                             : ring + st * slot_bytes + k * C::K_CH + r * br * 128;
+          tma_load_2d_warp(smem_u32(dst), &tk, bar(full0 + st),
+                           (vring ? v_chunk(h, k) : n_chunk(h, k)) * 64, yr[r]);
+        }
       }
       if (!vring) {
         // The V-ring slot of block j is refilled only once PV(j - 2) is done,
@@ -370,8 +426,10 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     // next half of QK(jq) into S_{jq % 2}: the
     // N-ring chunks once their slot landed and PV(jq - 2) has read the P
     // that shares that S buffer, then the V-ring chunks once their slot landed.
-    const uint32_t idesc_qk = umma_idesc_bf16(128, 64, 0, 0);
-    const uint32_t idesc_pv = umma_idesc_bf16(128, 256, 0, 1);
+    const uint32_t idesc_qk = FP8 ? umma_idesc_f16(128, 64, 0, 0) : umma_idesc_bf16(128, 64, 0, 0);
+    const uint32_t idesc_pv = FP8 ? umma_idesc_f16(128, 256, 0, 1) : umma_idesc_bf16(128, 256, 0, 1);
+    // FP8: a slot is ready for the MMAs once converted, not when its TMA lands
+    const uint32_t nready0 = FP8 ? B_NCONV : B_NFULL, vready0 = FP8 ? B_VCONV : B_VFULL;
     bool ok = __all_sync(kFull, mbar_wait(bar(B_QFULL), 0));
     int jq = 0, jp = 0;
     bool qk_half = false;  // the N-ring half of QK(jq) has been issued
@@ -415,7 +473,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
       if (jq < nblk && !qk_half) {  // N-ring chunks of QK(jq), Q from TMEM
         const bool rdy = __shfl_sync(
             kFull,
-            mbar_test(bar(B_NFULL + qs), (jq / C::NST) & 1) &&
+            mbar_test(bar(nready0 + qs), (jq / C::NST) & 1) &&
                 (jq < 2 || mbar_test(bar(B_PFREE + (jq & 1)), ((jq - 2) >> 1) & 1)),
             0);
         if (rdy) {
@@ -435,7 +493,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
           continue;
         }
       } else if (jq < nblk) {  // V-ring chunks of QK(jq), Q from shared memory
-        if (__shfl_sync(kFull, mbar_test(bar(B_VFULL + qs), (jq / C::NST) & 1), 0)) {
+        if (__shfl_sync(kFull, mbar_test(bar(vready0 + qs), (jq / C::NST) & 1), 0)) {
           tc_fence_after();
           const uint32_t vst = smem_u32(sm + C::OFF_V + qs * C::V_SLOT);
 #pragma unroll
@@ -465,6 +523,41 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     umma_commit_warp(bar(B_DONE));
     __syncwarp();
     mbar_wait(bar(B_DONE), 0);
+  } else if (FP8 && warp >= C::CONV_WARP0) {
+    // ----------------------------------------------------- converters (FP8)
+    // Per block j: N slot j % NST, then V slot j % NST, each once its e4m3
+    // rows have landed.  A warp whose wait timed out raises conv_abort before
+    // the next named barrier, after which all four warps leave together (a
+    // named barrier has no timeout, so no warp may skip one alone).
+    const int ct = threadIdx.x - C::CONV_WARP0 * 32;
+    int done = 0;
+    bool aborted = false;
+    for (int j = 0; j < nblk && !aborted; ++j) {
+      const int st = j % C::NST;
+      for (int rg = 0; rg < 2; ++rg) {
+        const bool ok = __all_sync(kFull, mbar_wait(bar((rg ? B_VFULL : B_NFULL) + st), (j / C::NST) & 1));
+        if (!ok && lane == 0) *conv_abort = 1;
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (*conv_abort) {
+          aborted = true;
+          break;
+        }
+        if (rg == 0)
+          convert_slot<C::NN>(sm + C::OFF_N + st * C::N_SLOT, ct);
+        else
+          convert_slot<C::NX>(sm + C::OFF_V + st * C::V_SLOT, ct);
+        // order the f16 writes before the tensor cores' reads (and the slot's
+        // next TMA refill)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar((rg ? B_VCONV : B_NCONV) + st));
+      }
+      done = j + 1;
+    }
+    if (aborted && ct == 0) {
+      atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+      note_abort(abort_flag, (7 << 24) | (done & 0xfff));
+    }
   } else {
     // -------------------------------------------------------------- softmax warps
     const int g = warp & 3;          // TMEM lane group of this warp
@@ -474,9 +567,38 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     // Q row r: its N-ring chunks -> TMEM (32-bit column c of a chunk holds
     // dims 2c, 2c + 1, the even one in the low half: the A-from-TMEM layout);
     // its V-ring chunks -> shared memory, 128-byte swizzled K-major rows
+    // scores -> log2 units for this row (FP8: times the inverse of the
+    // power of two the row's f16 query was scaled by)
+    float sl2 = a.qk_scale_log2;
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                          ((size_t(b) * a.T + t) * a.Hq + r) * C::DK);
+      // FP8: the f16 products need f16 queries, whose range is far narrower
+      // than bf16's; the row is scaled by 2^k so that its largest component
+      // lies in [2^14, 2^15) (exact, and every component rounds to f16
+      // without loss unless it is below 2^-29 of the row maximum)
+      float up = 1.f;
+      if (FP8) {
+        float amax = 0.f;
+#pragma unroll 4
+        for (int v = 0; v < C::DK / 8; ++v) {
+          const uint4 x = __ldg(qrow + v);
+          const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[e] << 16)),
+                                     fabsf(__uint_as_float(wv[e] & 0xffff0000u))));
+        }
+        int k = 0;
+        if (amax > 0.f) k = min(126, max(-113, 14 - (int((__float_as_uint(amax) >> 23) & 0xff) - 127)));
+        up = __uint_as_float(uint32_t(127 + k) << 23);
+        sl2 *= __uint_as_float(uint32_t(127 - k) << 23);
+      }
+      // bf16 pair -> f16 pair times `up` (FP8), or the bf16 pair itself
+      auto cvt = [&](uint32_t w) -> uint32_t {
+        if (!FP8) return w;
+        return pack_f16(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
+      };
 #pragma unroll 1
       for (int i = 0; i < C::NN; ++i) {
         const uint4* src = qrow + n_chunk(h, i) * 8;
@@ -484,10 +606,10 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = __ldg(src + v);
-          w[4 * v] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
+          w[4 * v] = cvt(x.x);
+          w[4 * v + 1] = cvt(x.y);
+          w[4 * v + 2] = cvt(x.z);
+          w[4 * v + 3] = cvt(x.w);
         }
         tmem_st32u(lane_base + C::Q_COL + uint32_t(i * 32), w);
       }
@@ -496,8 +618,11 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
         const uint4* src = qrow + v_chunk(h, k) * 8;
         uint8_t* dst = sm + C::OFF_Q + k * C::Q_CH + r * 128;
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<uint4*>(dst + ((v ^ (r & 7)) << 4)) = __ldg(src + v);
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = __ldg(src + v);
+          *reinterpret_cast<uint4*>(dst + ((v ^ (r & 7)) << 4)) =
+              make_uint4(cvt(x.x), cvt(x.y), cvt(x.z), cvt(x.w));
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tmem_wait_st();
@@ -543,7 +668,6 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
       for (int k = 16; k < 64; k += 8)
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[k + i]);
-      const float sl2 = a.qk_scale_log2;
       const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
       float alpha = 1.f;
@@ -563,7 +687,8 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
         for (int i = 0; i < 8; ++i) pv[i] = ex2(fmaf(s[8 * c + i], sl2, nms));
         l += ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) pk[4 * c + i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+        for (int i = 0; i < 4; ++i)
+          pk[4 * c + i] = FP8 ? pack_f16(pv[2 * i], pv[2 * i + 1]) : pack_bf16(pv[2 * i], pv[2 * i + 1]);
       }
       // O may only be rescaled once PV(j-1) has finished accumulating into it
       if (__any_sync(kFull, rescale_o)) {
@@ -597,7 +722,7 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
     const int row_n = t * C::ROWS + r;  // row of the item's partial block
     float lse_n = -INFINITY;
     if (l > 0.f) lse_n = (m_ref + lg2(l)) * kLn2m;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? a.o_scale / l : 0.f;  // o_scale: the FP8 cache scale, else 1
     bool have_o = ok && nblk > 0;
     // PV(nblk - 1) complete (its commit covers every earlier MMA, PV(nblk - 2) too)
     if (have_o && !__all_sync(kFull, mbar_wait(bar(B_PFREE + ((nblk - 1) & 1)),
@@ -668,10 +793,12 @@ __global__ void __launch_bounds__(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1)
 // multiple of 64), or one box of P rows per page written P * 128 bytes apart
 // (pages of 16 or 32 keys).  One CTA of 128 threads; one chunk at a time.
 // Page ids outside [0, num_pages) are read as page 0, as in the decode kernel.
+template <bool FP8>
 __global__ void __launch_bounds__(128) mla_gather_debug_kernel(const __grid_constant__ CUtensorMap tm,
                                                                const int32_t* table_row, int P,
                                                                int num_pages, int row_elems,
                                                                int n_keys, uint8_t* dst) {
+  constexpr int RB = FP8 ? 64 : 128;  // bytes of one 64-column row of a box
   __shared__ __align__(1024) uint8_t chunk[Mla::K_CH];
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
@@ -688,13 +815,13 @@ __global__ void __launch_bounds__(128) mla_gather_debug_kernel(const __grid_cons
     for (int c = 0; c < n_chunks; ++c, ++phase) {
       if (threadIdx.x == 0) {
         const int nb = small ? min(Mla::BK / P, n_pages - key0 / P) : 1;
-        mbar_arrive_expect_tx(smem_u32(&bar), uint32_t(nb * br * 128));
+        mbar_arrive_expect_tx(smem_u32(&bar), uint32_t(nb * br * RB));
         for (int r = 0; r < nb; ++r) {
           const int page = small ? key0 / P + r : key0 / P;
           const int off = small ? 0 : key0 - page * P;
           int ph = table_row[page];
           if (ph < 0 || ph >= num_pages) ph = 0;
-          tma_load_2d_warp_lane(smem_u32(chunk + r * br * 128), &tm, smem_u32(&bar), c * 64,
+          tma_load_2d_warp_lane(smem_u32(chunk + r * br * RB), &tm, smem_u32(&bar), c * 64,
                                 ph * P + off);
         }
       }
@@ -705,10 +832,14 @@ __global__ void __launch_bounds__(128) mla_gather_debug_kernel(const __grid_cons
         return;
       }
       const int rows = min(Mla::BK, n_keys - key0);
-      for (int x = threadIdx.x; x < rows * 8; x += blockDim.x) {
-        const int i = x >> 3, seg = x & 7;
-        const uint32_t off = uint32_t(i * 128 + ((seg ^ (i & 7)) << 4));
-        *reinterpret_cast<uint4*>(dst + (size_t(key0 + i) * row_elems + c * 64 + seg * 8) * 2) =
+      constexpr int SEGS = RB / 16;  // 16-byte segments of a row
+      for (int x = threadIdx.x; x < rows * SEGS; x += blockDim.x) {
+        const int i = x / SEGS, seg = x % SEGS;
+        // bf16: the 128-byte swizzle of the decode kernel's boxes; e4m3: the
+        // unswizzled rows its converter warps read
+        const uint32_t off = FP8 ? uint32_t(i * 64 + seg * 16) : uint32_t(i * 128 + ((seg ^ (i & 7)) << 4));
+        *reinterpret_cast<uint4*>(dst + size_t(key0 + i) * row_elems * (FP8 ? 1 : 2) +
+                                  (c * 64) * (FP8 ? 1 : 2) + seg * 16) =
             *reinterpret_cast<const uint4*>(chunk + off);
       }
       __syncthreads();
@@ -720,15 +851,15 @@ __global__ void __launch_bounds__(128) mla_gather_debug_kernel(const __grid_cons
 
 namespace {
 
-template <bool SEPV, bool SMALLP>
+template <bool SEPV, bool SMALLP, bool FP8 = false>
 cudaError_t launch_mla_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                          cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      mla_splitkv_kernel<SEPV, SMALLP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Mla::SMEM);
+      mla_splitkv_kernel<SEPV, SMALLP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Mla::SMEM);
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_items * a.T * 2, 1, 1);
-  cfg.blockDim = dim3(SEPV ? Mla::THREADS + 32 : Mla::THREADS, 1, 1);
+  cfg.blockDim = dim3(SEPV ? Mla::THREADS + 32 : (FP8 ? Mla::THREADS + 128 : Mla::THREADS), 1, 1);
   cfg.dynamicSmemBytes = Mla::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attrs[1];
@@ -736,17 +867,23 @@ cudaError_t launch_mla_t(const DecodeArgs& a, const CUtensorMap& mk, const CUten
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<SEPV, SMALLP>, a, mk, mv);
+  return cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<SEPV, SMALLP, FP8>, a, mk, mv);
 }
 
 }  // namespace
 
-cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, void* stream) {
+cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv, bool fp8,
+                       void* stream) {
   if (a.n_items == 0) return cudaSuccess;
   const CUtensorMap& mk = *reinterpret_cast<const CUtensorMap*>(&tk);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // pages of 16 or 32 keys: several boxes per 64-key block
   const bool small = a.P < Mla::BK;
+  if (fp8) {
+    if (tv) return cudaErrorInvalidValue;  // FP8 latent caches hold V in the key rows
+    return small ? launch_mla_t<false, true, true>(a, mk, mk, s)
+                 : launch_mla_t<false, false, true>(a, mk, mk, s);
+  }
   if (tv) {
     const CUtensorMap& mv = *reinterpret_cast<const CUtensorMap*>(tv);
     return small ? launch_mla_t<true, true>(a, mk, mv, s) : launch_mla_t<true, false>(a, mk, mv, s);
@@ -754,12 +891,17 @@ cudaError_t launch_mla(const DecodeArgs& a, const TmaDesc& tk, const TmaDesc* tv
   return small ? launch_mla_t<false, true>(a, mk, mk, s) : launch_mla_t<false, false>(a, mk, mk, s);
 }
 
-cudaError_t launch_mla_debug_gather(const TmaDesc& t, const int32_t* table_row, int32_t P,
+cudaError_t launch_mla_debug_gather(const TmaDesc& t, bool fp8, const int32_t* table_row, int32_t P,
                                     int32_t num_pages, int32_t row_elems, int32_t n_keys, void* dst,
                                     void* stream) {
   const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(&t);
-  mla_gather_debug_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-      m, table_row, P, num_pages, row_elems, n_keys, static_cast<uint8_t*>(dst));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fp8)
+    mla_gather_debug_kernel<true><<<1, 128, 0, s>>>(m, table_row, P, num_pages, row_elems, n_keys,
+                                                    static_cast<uint8_t*>(dst));
+  else
+    mla_gather_debug_kernel<false><<<1, 128, 0, s>>>(m, table_row, P, num_pages, row_elems, n_keys,
+                                                     static_cast<uint8_t*>(dst));
   return cudaGetLastError();
 }
 

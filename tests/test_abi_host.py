@@ -144,6 +144,20 @@ def test_mla_with_separate_v_is_planned():
     assert np.array_equal(items[0], items[1])
 
 
+def test_mla_e4m3_latent_cache_is_planned_and_separate_e4m3_v_is_not():
+    """An e4m3 latent cache (V in its rows) plans like the bf16 one; an e4m3
+    cache with a separate V tensor has no kernel."""
+    lens = np.array([5000], np.int32)
+    d16 = skv.make_desc(1, 6, 128, 1, 576, 512, 64, 128, 200, skv.SPLITKV_BF16, 1)
+    d8 = skv.make_desc(1, 6, 128, 1, 576, 512, 64, 128, 200, skv.SPLITKV_FP8_E4M3, 1)
+    assert np.array_equal(skv.splitkv_plan_get_items(skv.splitkv_plan(d16, lens, 4, 148)),
+                          skv.splitkv_plan_get_items(skv.splitkv_plan(d8, lens, 4, 148)))
+    d8v = skv.make_desc(1, 6, 128, 1, 576, 512, 64, 128, 200, skv.SPLITKV_FP8_E4M3, 0)
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(d8v, lens, 4, 148)
+    assert e.value.status == skv.SPLITKV_EUNSUPPORTED
+
+
 @pytest.mark.parametrize("P,ok", [(16, True), (32, True), (64, True), (128, True), (192, True),
                                   (48, False), (80, False)])
 def test_mla_page_sizes(P, ok):

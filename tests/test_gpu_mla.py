@@ -12,6 +12,7 @@ import oracle
 import workloads
 import split_kv_paged_splitkv_gb300 as skv
 from _support import compare, need_gpu, oracle_direct, session
+from split_kv_paged_splitkv_gb300.runner import DecodeSession
 
 pytestmark = pytest.mark.gpu
 
@@ -21,8 +22,9 @@ def _gpu():
     need_gpu()
 
 
-def _mla(lens, T, seed=3, v_shares_k=True, P=64):
-    return workloads.Workload("mla_custom", len(lens), T, 128, 1, 576, 512, P, "bf16",
+def _mla(lens, T, seed=3, v_shares_k=True, P=64, fp8=False):
+    return workloads.Workload("mla_custom", len(lens), T, 128, 1, 576, 512, P,
+                              "fp8_e4m3" if fp8 else "bf16",
                               "list:" + ":".join(str(int(x)) for x in lens), std=0.5,
                               v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
@@ -66,28 +68,82 @@ def _check_cta_ranges(s, x, T):
 
 
 @pytest.mark.parametrize("P", [16, 32, 64, 128])
-@pytest.mark.parametrize("sepv", [False, True])
-def test_mla_paged_gather_is_bit_exact(P, sepv):
-    """The latent rows (576 wide) and, with a separate V tensor, the V rows
-    (512 wide), read through the block table with the decode kernel's tensor
-    maps and swizzled addressing, equal the CPU gather bit for bit."""
+@pytest.mark.parametrize("sepv,fp8", [(False, False), (True, False), (False, True)])
+def test_mla_paged_gather_is_bit_exact(P, sepv, fp8):
+    """The latent rows (576 wide, bf16 or e4m3 codes) and, with a separate V
+    tensor, the V rows (512 wide), read through the block table with the
+    decode kernel's tensor maps and shared-memory addressing, equal the CPU
+    gather bit for bit."""
     lens = [3, P + 7, 777, 64 * 3]
-    x = workloads.make_inputs(_mla(lens, 2, seed=70 + P + sepv, v_shares_k=not sepv, P=P),
+    x = workloads.make_inputs(_mla(lens, 2, seed=70 + P + sepv, v_shares_k=not sepv, P=P, fp8=fp8),
                               device="cuda")
     desc = skv.make_desc(len(lens), 2, 128, 1, 576, 512, P, x.max_pages, x.num_pages,
-                         skv.SPLITKV_BF16, int(not sepv))
+                         skv.SPLITKV_FP8_E4M3 if fp8 else skv.SPLITKV_BF16, int(not sepv))
     tables = x.block_table.cpu().numpy()
     for b, L in enumerate(x.seq_lens_host):
         L = int(L)
         for pages, width in ((x.k_pages, 576),) + (((x.v_pages, 512),) if sepv else ()):
-            dst = torch.zeros((L, width), dtype=torch.bfloat16, device="cuda")
+            dst = torch.zeros((L, width), dtype=pages.dtype, device="cuda")
             skv.splitkv_debug_gather(desc, pages, width, x.block_table, b, 0, L, dst)
             torch.cuda.synchronize()
             ref = oracle.gather_keys(workloads.bits(pages), tables[b], L, 0)
             assert np.array_equal(workloads.bits(dst), ref), (b, width)
 
 
-@pytest.mark.parametrize("name", ["mla_t6_ctx64k", "mla_sepv_t6_ctx64k"])
+@pytest.mark.parametrize("T", [1, 2, 6, 16])
+def test_mla_fp8_small_ragged(T):
+    """An e4m3 latent cache (V = its first 512 columns, one per-tensor scale):
+    converted to f16 in shared memory, f16 tensor-core products."""
+    lens = [T, 64, 100, 130, 1000]
+    x = workloads.make_inputs(_mla(lens, T, seed=40 + T, fp8=True), device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in (1, 2, 3, 0):
+        s = session(x, S)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"fp8 T={T} S={S}")
+        assert s.stats()[1] == 0
+        _check_cta_ranges(s, x, T)
+
+
+@pytest.mark.parametrize("P", [16, 32, 128, 192])
+def test_mla_fp8_page_sizes(P):
+    T = 3
+    lens = [T, 40, P + 7, 3 * P, 777, 2100]
+    x = workloads.make_inputs(_mla(lens, T, seed=50 + P, P=P, fp8=True), device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in (1, 3, 7, 0):
+        s = session(x, S)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"fp8 P={P} S={S}")
+        assert s.stats()[1] == 0
+        _check_cta_ranges(s, x, T)
+
+
+@pytest.mark.parametrize("mag", [1e5, 1e-6])
+def test_mla_fp8_queries_of_any_bf16_magnitude(mag):
+    """Queries far outside f16's range (the kernel scales each row by a power
+    of two before its f16 products), with the cache scale set so that the
+    scores stay of order one; outputs compared relative to their size."""
+    T = 2
+    lens = [T + 3, 300, 1000]
+    x = workloads.make_inputs(_mla(lens, T, seed=60, fp8=True), device="cuda")
+    q = (x.q.float() * mag).to(torch.bfloat16)
+    kv_scale = float(np.float32(x.kv_scale / mag))
+    ref_o, ref_l = oracle.attention_direct(
+        workloads.bits(q), workloads.bits(x.k_pages), None, x.block_table.cpu().numpy(),
+        x.seq_lens_host, scale=x.scale, kv_dtype="fp8_e4m3", kv_scale=kv_scale, v_dim=512,
+        v_shares_k=True)
+    s = DecodeSession(q, x.k_pages, None, x.block_table, x.seq_lens, x.seq_lens_host,
+                      scale=x.scale, kv_scale=kv_scale, num_splits=3, v_dim=512, v_shares_k=True)
+    out, lse = s.run()
+    assert s.stats()[1] == 0
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all()
+    assert np.abs(o - ref_o).max() <= 1e-2 * np.abs(ref_o).max()
+    assert np.abs(lse.cpu().numpy() - ref_l).max() <= 1e-3
+
+
+@pytest.mark.parametrize("name", ["mla_t6_ctx64k", "mla_sepv_t6_ctx64k", "mla_fp8_t6_ctx64k"])
 def test_mla_ctx64k_full(name):
     w = workloads.WORKLOADS[name]
     x = workloads.make_inputs(w, device="cuda")
@@ -121,14 +177,14 @@ def test_mla_page_sizes(P, sepv):
 
 
 @pytest.mark.parametrize("P", [16, 64])
-@pytest.mark.parametrize("sepv", [False, True])
-def test_mla_out_of_range_page_ids_are_flagged(P, sepv):
+@pytest.mark.parametrize("sepv,fp8", [(False, False), (True, False), (False, True)])
+def test_mla_out_of_range_page_ids_are_flagged(P, sepv, fp8):
     """As for GQA: an entry >= num_pages and a negative one are read as page
     0, SPLITKV_DEVERR_PAGE is set, the output stays finite, and the intact
     sequences match the oracle."""
     T = 2
     lens = [640, 1024, 320]  # whole pages: no poisoned tail slots in page 0
-    x = workloads.make_inputs(_mla(lens, T, seed=90 + P + sepv, v_shares_k=not sepv, P=P),
+    x = workloads.make_inputs(_mla(lens, T, seed=90 + P + sepv, v_shares_k=not sepv, P=P, fp8=fp8),
                               device="cuda")
     ref_o, ref_l = oracle_direct(x)
     bad = x.block_table.clone()

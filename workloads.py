@@ -84,6 +84,10 @@ WORKLOADS = {
     "mla_sepv_t6_ctx64k": Workload(
         "mla_sepv_t6_ctx64k", 1, 6, 128, 1, 576, 512, 64, "bf16", "fixed:65536",
         std=0.5, v_shares_k=False, splits=(1, 4, 0), pool_slack=0.0, seed=1006),
+    # the same MLA decode over an e4m3 latent cache with a per-tensor scale
+    "mla_fp8_t6_ctx64k": Workload(
+        "mla_fp8_t6_ctx64k", 1, 6, 128, 1, 576, 512, 64, "fp8_e4m3", "fixed:65536",
+        std=0.5, v_shares_k=True, splits=(1, 4, 8, 0), pool_slack=0.0, seed=1007),
     "mixed_batch32_bf16": Workload(
         "mixed_batch32_bf16", 32, 1, 32, 8, 128, 128, 16, "bf16",
         "loguniform:256:131072", splits=(0,), pool_slack=0.02, seed=1005),
