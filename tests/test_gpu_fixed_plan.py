@@ -33,8 +33,9 @@ def _gqa(lens, G=8, Hkv=2, T=1, P=16, fp8=False, seed=3):
         "list:" + ":".join(str(int(x)) for x in lens), pool_slack=0.5, seed=seed)
 
 
-def _mla(lens, T=2, seed=5, v_shares_k=True, P=64):
-    return workloads.Workload("fixed_mla", len(lens), T, 128, 1, 576, 512, P, "bf16",
+def _mla(lens, T=2, seed=5, v_shares_k=True, P=64, fp8=False):
+    return workloads.Workload("fixed_mla", len(lens), T, 128, 1, 576, 512, P,
+                              "fp8_e4m3" if fp8 else "bf16",
                               "list:" + ":".join(str(int(x)) for x in lens), std=0.5,
                               v_shares_k=v_shares_k, pool_slack=0.5, seed=seed)
 
@@ -108,10 +109,11 @@ def test_one_graph_serves_changing_lengths(mode, T, G):
         assert s.stats()[1] == 0
 
 
-@pytest.mark.parametrize("v_shares_k,P", [(True, 64), (False, 64), (True, 16), (False, 32)])
-def test_mla_capacity_plan(v_shares_k, P):
+@pytest.mark.parametrize("v_shares_k,P,fp8", [(True, 64, False), (False, 64, False), (True, 16, False),
+                                               (False, 32, False), (True, 64, True), (True, 16, True)])
+def test_mla_capacity_plan(v_shares_k, P, fp8):
     cap = [64 * 9 + 5, 64 * 3, 2]
-    x = workloads.make_inputs(_mla(cap, v_shares_k=v_shares_k, P=P), device="cuda")
+    x = workloads.make_inputs(_mla(cap, v_shares_k=v_shares_k, P=P, fp8=fp8), device="cuda")
     lens_dev = x.seq_lens.clone()
     s = _session(x, 4, lens_dev=lens_dev)
     for lens in (cap, [64 * 2 + 1, 64 * 3, 0]):

@@ -4,7 +4,8 @@ The fixed cases elsewhere vary one option at a time; these draw them jointly:
 batch, query tokens, group size, KV heads, page size, cache type, page layout,
 per-KV-head scales, split count, combine mode and ragged lengths (empty
 sequences and exact page multiples included) for the GQA kernel, and tokens,
-page size, lengths, split count and a separate V tensor for the MLA kernel.  Sizes stay
+page size, lengths, split count, a separate V tensor or an e4m3 latent cache for the
+MLA kernel.  Sizes stay
 small enough for the oracle to finish in seconds.
 """
 import numpy as np
@@ -92,14 +93,18 @@ def test_random_mla(case):
     P = int(rng.choice([16, 32, 64, 64, 128]))
     lens = _lens(rng, B, P, T, 1500)
     sepv = bool(rng.random() < 0.5)
-    w = workloads.Workload(f"rand_mla{case}", B, T, 128, 1, 576, 512, P, "bf16",
+    fp8 = not sepv and bool(np.random.default_rng(990 + case).random() < 0.5)  # e4m3 latent cache
+    w = workloads.Workload(f"rand_mla{case}", B, T, 128, 1, 576, 512, P,
+                           "fp8_e4m3" if fp8 else "bf16",
                            "list:" + ":".join(str(x) for x in lens), std=0.5,
                            v_shares_k=not sepv, pool_slack=0.3, seed=950 + case)
     x = workloads.make_inputs(w, device="cuda")
     S = int(rng.choice([0, 1, 2, 5]))
     ref_o, ref_l = oracle_direct(x)
     s = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
-                      scale=x.scale, num_splits=S, v_dim=512, v_shares_k=not sepv)
+                      scale=x.scale, kv_scale=x.kv_scale, num_splits=S, v_dim=512,
+                      v_shares_k=not sepv)
     out, lse = s.run()
-    compare(out, lse, ref_o, ref_l, what=f"MLA T={T} B={B} P={P} sepv={sepv} S={S} lens={lens}")
+    compare(out, lse, ref_o, ref_l,
+            what=f"MLA T={T} B={B} P={P} sepv={sepv} fp8={fp8} S={S} lens={lens}")
     assert s.stats()[1] == 0

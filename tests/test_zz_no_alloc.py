@@ -4,9 +4,10 @@ plugins that may not allocate after start-up, real-time loops that must not
 stall on an allocation).  It keeps its workspace in a fixed 16 MiB device array
 inside the library instead of a caller buffer.
 
-The GPU test calls it through the C-ABI, twice in a row, on each of four
+The GPU test calls it through the C-ABI, twice in a row, on each of five
 workloads (bf16 GQA with the planner's splits, a short bf16 GQA at 4 splits,
-an e4m3 cache in NHD pages, an MLA decode with a separate V tensor): every
+an e4m3 cache in NHD pages, an MLA decode with a separate V tensor, an MLA
+decode over an e4m3 latent cache in 16-key pages): every
 call must reproduce splitkv_decode on a caller workspace bit for bit (same
 kernels, same plan, so a stale work list or ticket from the previous call
 would show), leave the device status word clear, and log the same per-CTA
@@ -47,6 +48,9 @@ _CASES = [
                         "list:500:1200:33", pool_slack=0.5, seed=61), 0, "NHD"),
     (workloads.Workload("noalloc_mla", 1, 2, 128, 1, 576, 512, 64, "bf16", "list:700",
                         std=0.5, v_shares_k=False, pool_slack=0.5, seed=62), 3, "HND"),
+    # and an MLA decode over an e4m3 latent cache
+    (workloads.Workload("noalloc_mla_e4m3", 1, 2, 128, 1, 576, 512, 16, "fp8_e4m3", "list:900",
+                        std=0.5, v_shares_k=True, pool_slack=0.5, seed=63), 4, "HND"),
 ]
 
 
