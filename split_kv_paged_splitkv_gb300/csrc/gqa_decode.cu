@@ -9,7 +9,8 @@
 // of NST stages guarded by mbarriers: two 32 KB stages, so that three CTAs
 // share an SM, or four for a grid of at most one CTA per SM, whose producer
 // also warms L2 with its first tiles before the dependency wait.  One
-// producer warp issues the copies.  The four consumer warps form slots
+// producer warp issues the copies (four, taking the tiles round-robin, in the
+// four-stage form, whose CTA has an SM to itself).  The four consumer warps form slots
 // (head slot, row group): each slot serves query rows [8 rg, 8 rg + 8) of
 // KV head h0 + hs, and a slot's warps take its tiles round-robin.
 //
@@ -69,14 +70,24 @@ struct Gqa {
   static constexpr int TPS = STAGE / TILE;                 // tiles per stage
   static constexpr int NST = NST_;                         // stages in the ring
   static constexpr int NCW = 4;                            // consumer warps
+  // Producer warps: four for the one-wave four-stage ring (tiles go to them
+  // round-robin; measured on GB300, a CTA's cold 48 KB lands about 13 %
+  // sooner when four warps issue its boxes than when one does), one for the
+  // two-stage ring, whose three CTAs per SM have no threads to spare.
+  static constexpr int NPROD = NST_ == 4 ? 4 : 1;
   // A slot is (head slot hs, row group rg) = (slot % HPI, slot / HPI): the
   // warps of a slot score query rows [8 rg, 8 rg + 8) of KV head h0 + hs.
   static constexpr int SLOTS = HPI * NRG;
   static constexpr int WPH = NCW / SLOTS;                  // warps per slot
-  static constexpr int THREADS = (NCW + 1) * 32;
+  static constexpr int THREADS = (NCW + NPROD) * 32;
+  static constexpr int MIN_CTAS = NST_ == 4 ? 1 : kGqaCtasPerSm;  // resident CTAs per SM
   static constexpr int RING = NST * STAGE;
   static constexpr int ROWS = 8 * SLOTS;                   // merge rows (8 per slot)
-  static constexpr int MERGE = NCW * 8 * D * 4 + NCW * 8 * 2 * 4;
+  // The warps' O rows in the merge area are MO_STRIDE floats apart: 4 more
+  // than D, so that the 4 rows (2 ti) a warp's lanes store at once fall on
+  // different banks (a 128-float stride put them on the same 8 banks).
+  static constexpr int MO_STRIDE = D + 4;
+  static constexpr int MERGE = NCW * 8 * MO_STRIDE * 4 + NCW * 8 * 2 * 4;
   static_assert(MERGE + 64 * ROWS * 4 <= RING, "merge area and staged LSEs alias the ring");
   // Warp w takes tiles w / HPI, w / HPI + WPH, ...: its successive visits to
   // one stage must be exactly one barrier phase apart (parity waits cannot
@@ -89,7 +100,7 @@ struct Gqa {
                 "stage/warp aliasing");
   static constexpr int BARS = 2 * NST * 8;
   static constexpr int PT_CHUNK = 1024;  // block-table entries staged at a time
-  static constexpr int SMEM = 1024 + RING + BARS + 64 + PT_CHUNK * 4;
+  static constexpr int SMEM = 1024 + RING + BARS + 64 + NPROD * PT_CHUNK * 4;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -136,7 +147,7 @@ __device__ __forceinline__ void store_row(const float (&acc)[DPT], __nv_bfloat16
 // result.  Runs on the NT = NCW * 32 consumer threads: merge row n = tid /
 // TPR (slot n / 8, i.e. head slot hs and row group rg; query row rg * 8 +
 // n % 8 of that head), DPT = 128 / TPR consecutive dims from d0.  `mo` is
-// [NCW][8][128] fp32, `mm`/`ml` [NCW][8]; m is in log2 units.  Partial rows
+// [NCW][8][MO_STRIDE] fp32, `mm`/`ml` [NCW][8]; m is in log2 units.  Partial rows
 // are numbered hs * T*G + row.
 template <bool FP8, int HPI, int NRG>
 __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, const float* mo,
@@ -161,7 +172,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
       const int w = sl + C::SLOTS * j;
       const float sc = ex2(mm[w * 8 + r8] - M);
       lsum += sc * ml[w * 8 + r8];
-      axpy<DPT>(acc, sc, mo + (w * 8 + r8) * 128 + d0);
+      axpy<DPT>(acc, sc, mo + (w * 8 + r8) * C::MO_STRIDE + d0);
     }
   }
   float lse_n = -INFINITY;
@@ -288,7 +299,7 @@ __device__ __forceinline__ void prefetch_first_tiles(const DecodeArgs& a, const 
 }
 
 template <bool FP8, int HPI, int NRG, int NST>
-__global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerSm)
+__global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, Gqa<FP8, HPI, NRG, NST>::MIN_CTAS)
     gqa_splitkv_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv) {
   using C = Gqa<FP8, HPI, NRG, NST>;
@@ -298,7 +309,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::RING);
   uint64_t* empty = full + C::NST;
   int* misc = reinterpret_cast<int*>(empty + C::NST);  // [0] merge flag, [1] keys scored
-  int* pt = misc + 16;                                 // staged block-table entries
+  int* pt = misc + 16;                                 // staged block-table entries, per producer
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A capacity plan's item is derived from the device lengths (read after the
@@ -362,17 +373,27 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   wait_prerequisites();
   if (threadIdx.x == 0 && a.seq_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
 
-  if (warp == C::NCW) {
-    // ---------------------------------------------------------------- producer
-    // The warp stages up to PT_CHUNK physical page ids of this item in shared
-    // memory (coalesced loads); then the whole warp walks the tiles, arming
-    // each stage's barrier and issuing the tile boxes from one elected lane
-    // (copies issued by a converged warp cost a fraction of the issue cycles
-    // of copies issued by a lane that branched away from its warp).
+  if (warp >= C::NCW) {
+    // --------------------------------------------------------------- producers
+    // Each producer warp stages up to PT_CHUNK physical page ids of this item
+    // in its own shared-memory array (coalesced loads; the warps read the same
+    // entries, so they never wait for one another), then walks the tiles,
+    // issuing its own (tile t goes to producer warp t % NPROD) from one elected
+    // lane of the converged warp (copies issued by a converged warp cost a
+    // fraction of the issue cycles of copies issued by a lane that branched
+    // away from its warp).  The warp owning a stage's first tile arms the
+    // stage's barrier with the stage's bytes; every warp waits for a ring slot
+    // to be released before writing into it again.
+    const int pw = warp - C::NCW;
+    int32_t* ptw = pt + pw * C::PT_CHUNK;
     const int32_t* trow = a.block_table + size_t(b) * a.max_pages;
     const int pg_end = (k_end + a.P - 1) / a.P;
     const int tiles_per_page = a.P >> 4;
-    int stages = 0, t = 0;
+    // Last stage this warp issued into (a stage holds TPS >= NPROD tiles, so
+    // every full stage holds a tile of every producer warp).
+    static_assert(C::TPS >= C::NPROD, "every full stage has a tile of every producer warp");
+    int last_j = -1;
+    int t = 0;
     bool ok = true;
     for (int pc = p0; pc < pg_end && ok; pc += C::PT_CHUNK) {
       const int cnt = min(C::PT_CHUNK, pg_end - pc);
@@ -380,30 +401,31 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
       for (int x = lane; x < cnt; x += 32) {
         int ph = __ldg(trow + pc + x);
         if (ph < 0 || ph >= a.num_pages) {
-          atomicOr(a.status, SPLITKV_DEVERR_PAGE);
+          if (pw == 0) atomicOr(a.status, SPLITKV_DEVERR_PAGE);
           ph = 0;
         }
-        pt[x] = ph;
+        ptw[x] = ph;
       }
       __syncwarp();
       const int t_end = min(n_tiles, (pc + cnt) * tiles_per_page - p0 * tiles_per_page);
       for (; t < t_end; ++t) {
+        if (C::NPROD > 1 && t % C::NPROD != pw) continue;
         const int key0 = k_begin + t * 16;
         const int page = key0 / a.P;
-        const int ph = pt[page - pc];
+        const int ph = ptw[page - pc];
         const int j = t / C::TPS, u = t - j * C::TPS, st = j % C::NST;
         const uint32_t bar = smem_u32(full + st);
-        if (u == 0) {
-          if (j >= C::NST) {
-            ok = __all_sync(kFull, mbar_wait(smem_u32(empty + st), ((j / C::NST) - 1) & 1));
-            if (!ok) {
-              if (lane == 0) atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
-              break;
-            }
+        // the first of this warp's tiles in stage j (u < NPROD) waits for the
+        // slot's release
+        if (j >= C::NST && u < C::NPROD) {
+          ok = __all_sync(kFull, mbar_wait(smem_u32(empty + st), ((j / C::NST) - 1) & 1));
+          if (!ok) {
+            if (lane == 0) atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
+            break;
           }
-          mbar_arrive_expect_tx_warp(bar, min(C::TPS, n_tiles - t) * C::TILE);
-          stages = j + 1;
         }
+        if (u == 0) mbar_arrive_expect_tx_warp(bar, min(C::TPS, n_tiles - t) * C::TILE);
+        last_j = j;
         const uint32_t dk = smem_u32(ring + st * C::STAGE + u * C::TILE);
         const uint32_t dv = dk + HPI * C::KT_BYTES;
         // The maps' coordinates are (dims, key in page, [column half,] KV
@@ -418,14 +440,22 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
         }
       }
     }
-    // Stay resident until every issued copy has landed: the CTA must not exit
-    // (and free its shared memory) with TMA writes in flight, even when a
-    // consumer gave up on a timed-out wait.  Normally these waits return at
-    // once, since the consumers have already seen the same phases complete.
+    // Stay resident until every copy this warp issued has landed: the CTA
+    // must not exit (and free its shared memory) with TMA writes in flight,
+    // even when a consumer gave up on a timed-out wait.  Each ring slot is
+    // waited on at the latest phase it reached: the item's last stage in that
+    // slot, which covers the earlier phases (and, were a warp's own last
+    // phase in a slot used instead, another warp's tile of the item's final
+    // stage could complete one more phase there, leaving the barrier at the
+    // parity the wait asks for).  A warp that gave up waits only on the
+    // phases it used itself; the stage it stopped at cannot complete, so no
+    // slot runs further.  Normally these waits return at once.
+    const int final_j = !ok ? last_j : n_tiles > 0 ? (n_tiles - 1) / C::TPS : -1;
     if (lane == 0) {
-      for (int st = 0; st < C::NST && st < stages; ++st) {
-        const int last = st + C::NST * ((stages - 1 - st) / C::NST);
-        if (!mbar_wait(smem_u32(full + st), (last / C::NST) & 1)) {
+      for (int st = 0; st < C::NST; ++st) {
+        const int j = final_j - ((final_j - st + C::NST) % C::NST);
+        if (j < 0) continue;
+        if (!mbar_wait(smem_u32(full + st), (j / C::NST) & 1)) {
           atomicOr(a.status, SPLITKV_DEVERR_TIMEOUT);
           break;
         }
@@ -673,7 +703,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   // ---- cross-warp merge through shared memory (aliases the drained ring)
   asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
   float* mo = reinterpret_cast<float*>(ring);
-  float* mm = mo + C::NCW * 8 * 128;
+  float* mm = mo + C::NCW * 8 * C::MO_STRIDE;
   float* ml = mm + C::NCW * 8;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
@@ -685,8 +715,8 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
       da = mt * 16 + 2 * gi;
       db = da + 1;
     }
-    float* w0 = mo + (warp * 8 + 2 * ti) * 128;
-    float* w1 = w0 + 128;
+    float* w0 = mo + (warp * 8 + 2 * ti) * C::MO_STRIDE;
+    float* w1 = w0 + C::MO_STRIDE;
     w0[da] = o[mt][0];
     w1[da] = o[mt][1];
     w0[db] = o[mt][2];
@@ -711,7 +741,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, kGqaCtasPerS
   int merged = 0;
   if (slot >= 0 && a.fused) {
     constexpr int kBundle = 8;
-    float* sl = reinterpret_cast<float*>(ring) + C::NCW * 8 * 128 + 2 * C::NCW * 8;
+    float* sl = reinterpret_cast<float*>(ring) + C::NCW * 8 * C::MO_STRIDE + 2 * C::NCW * 8;
     const int slot0 = slot - split;
     const bool two_level = nsplit > kBundle;
     const int bslot = slot0 + (split / kBundle) * kBundle;
