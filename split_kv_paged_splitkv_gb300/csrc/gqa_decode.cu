@@ -100,7 +100,12 @@ struct Gqa {
                 "stage/warp aliasing");
   static constexpr int BARS = 2 * NST * 8;
   static constexpr int PT_CHUNK = 1024;  // block-table entries staged at a time
-  static constexpr int SMEM = 1024 + RING + BARS + 64 + NPROD * PT_CHUNK * 4;
+  // The four-stage form has shared memory to spare: its merge area is its
+  // own, so each consumer warp stores its (m, l, O) as soon as its tiles are
+  // done (in the two-stage form the area aliases the ring, and the warps
+  // first wait for one another to drain it).
+  static constexpr bool SEP_MERGE = NST_ == 4;
+  static constexpr int SMEM = 1024 + RING + BARS + 64 + NPROD * PT_CHUNK * 4 + (SEP_MERGE ? MERGE : 0);
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -177,7 +182,9 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, co
   }
   float lse_n = -INFINITY;
   const float osc = a.v_scale ? __ldg(a.v_scale + h0 + hs) : a.o_scale;
-  const float inv = lsum > 0.f ? osc / lsum : 0.f;
+  // (lsum is a sum of at most a few million terms of at most 1: far below
+  // the 2^126 where the fast divide loses range)
+  const float inv = lsum > 0.f ? __fdividef(osc, lsum) : 0.f;
 #pragma unroll
   for (int i = 0; i < DPT; ++i) acc[i] *= inv;
   if (lsum > 0.f) lse_n = (M + lg2(lsum)) * kLn2;
@@ -700,9 +707,11 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, Gqa<FP8, HPI
   }
   if (lane == 0) atomicAdd(&misc[1], keys_scored);
 
-  // ---- cross-warp merge through shared memory (aliases the drained ring)
-  asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-  float* mo = reinterpret_cast<float*>(ring);
+  // ---- cross-warp merge through shared memory (its own area in the
+  // four-stage form, else the drained ring)
+  if (!C::SEP_MERGE) asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+  float* mo = C::SEP_MERGE ? reinterpret_cast<float*>(pt + C::NPROD * C::PT_CHUNK)
+                           : reinterpret_cast<float*>(ring);
   float* mm = mo + C::NCW * 8 * C::MO_STRIDE;
   float* ml = mm + C::NCW * 8;
 #pragma unroll
