@@ -23,6 +23,7 @@ def _gpu():
 @pytest.mark.parametrize("name,mode,calls", [
     ("mla_t6_ctx64k", skv.SPLITKV_COMBINE_SEPARATE, 600),
     ("mla_sepv_t6_ctx64k", skv.SPLITKV_COMBINE_SEPARATE, 600),
+    ("mla_fp8_t6_ctx64k", skv.SPLITKV_COMBINE_SEPARATE, 600),
     ("gqa_ctx5900", skv.SPLITKV_COMBINE_SEPARATE, 3000),
     ("gqa_ctx5900", skv.SPLITKV_COMBINE_FUSED, 3000),
     ("fp8_batch8_ctx32k", skv.SPLITKV_COMBINE_SEPARATE, 600),
