@@ -9,10 +9,11 @@
 // of NST stages guarded by mbarriers: two 32 KB stages, so that three CTAs
 // share an SM, or four for a grid of at most one CTA per SM, whose producer
 // also warms L2 with its first tiles before the dependency wait.  One
-// producer warp issues the copies (four, taking the tiles round-robin, in the
-// four-stage form, whose CTA has an SM to itself).  The four consumer warps form slots
-// (head slot, row group): each slot serves query rows [8 rg, 8 rg + 8) of
-// KV head h0 + hs, and a slot's warps take its tiles round-robin.
+// producer warp issues the copies (four, taking the tiles round-robin, in
+// the four-stage form, whose CTA has an SM to itself).  The four consumer
+// warps form slots (head slot, row group): each slot serves query rows
+// [8 rg, 8 rg + 8) of KV head h0 + hs, and a slot's warps take its tiles
+// round-robin.
 //
 // Per 16-key tile a consumer warp computes, on the warp tensor-core path:
 //   S^T[16 keys x 8 rows] = K_tile[16 x 128] . Q^T      (m16n8k16, keys on M)
