@@ -119,16 +119,23 @@ def test_mla_fp8_page_sizes(P):
         _check_cta_ranges(s, x, T)
 
 
-@pytest.mark.parametrize("mag", [1e5, 1e-6])
+@pytest.mark.parametrize("mag", [1e5, 1e-6, "spread"])
 def test_mla_fp8_queries_of_any_bf16_magnitude(mag):
     """Queries far outside f16's range (the kernel scales each row by a power
-    of two before its f16 products), with the cache scale set so that the
-    scores stay of order one; outputs compared relative to their size."""
+    of two before its f16 products), or with components spread over 2^-20 ..
+    2^16 within each row, with the cache scale set so that the scores stay of
+    order one; outputs compared relative to their size."""
     T = 2
     lens = [T + 3, 300, 1000]
     x = workloads.make_inputs(_mla(lens, T, seed=60, fp8=True), device="cuda")
-    q = (x.q.float() * mag).to(torch.bfloat16)
-    kv_scale = float(np.float32(x.kv_scale / mag))
+    if mag == "spread":
+        rng = np.random.default_rng(61)
+        e = torch.from_numpy(rng.uniform(-20, 16, size=tuple(x.q.shape))).float().cuda()
+        q = (torch.sign(x.q.float()) * torch.exp2(e)).to(torch.bfloat16)
+        kv_scale = float(np.float32(x.kv_scale / 2.0 ** 16))
+    else:
+        q = (x.q.float() * mag).to(torch.bfloat16)
+        kv_scale = float(np.float32(x.kv_scale / mag))
     ref_o, ref_l = oracle.attention_direct(
         workloads.bits(q), workloads.bits(x.k_pages), None, x.block_table.cpu().numpy(),
         x.seq_lens_host, scale=x.scale, kv_dtype="fp8_e4m3", kv_scale=kv_scale, v_dim=512,
