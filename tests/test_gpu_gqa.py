@@ -221,6 +221,24 @@ def test_both_ring_depths(T, G, Hkv, fp8):
         assert s.stats()[1] == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_items_longer_than_the_block_table_staging_chunk(fp8):
+    """One split over 1,250+ pages: every producer warp restages the item's
+    block-table entries chunk by chunk (1,024 at a time) mid-item, in the
+    one-wave four-stage form (four producer warps) and, with a plan for four
+    SMs, the two-stage form."""
+    lens = [16 * 1250 + 5, 16 * 1100, 37]
+    w = _custom(lens, G=8, Hkv=2, fp8=fp8, seed=17 + fp8)
+    x = workloads.make_inputs(w, device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S, num_sms in ((1, 0), (1, 4), (2, 0)):
+        s = session(x, S, 1, num_sms=num_sms)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"fp8={fp8} S={S} num_sms={num_sms}")
+        log, status = s.stats()
+        assert status == 0 and (log[:, 2] > 0).all()
+
+
 @pytest.mark.parametrize("T,G,Hkv,fp8,P", [(1, 8, 2, False, 16), (2, 8, 2, False, 32),
                                             (1, 4, 3, False, 64), (1, 8, 4, True, 16),
                                             (1, 2, 3, True, 32), (2, 8, 2, True, 16)])
