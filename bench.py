@@ -36,6 +36,8 @@ Protocol
   * ``per_config``: every workload of the suite, measured the same way with
     fewer steps (µs per call, the split kernel alone, roofline fraction, the
     fraction of split CTAs that scored keys).
+  * ``split_sweep``: the kernel-only num_splits sweep of the default workload
+    (1 to 64 splits: µs per call, the split kernel alone, non-empty CTAs).
   * Clocks: ``nvidia-smi`` samples every 200 ms while the same work runs
     (a >= 1 s soak immediately followed by the timed region).
 
@@ -572,6 +574,28 @@ def per_config(dev, args, headline):
     return out
 
 
+SWEEP_SPLITS = (1, 2, 4, 8, 16, 32, 64)
+
+
+def split_sweep(w, dev, args):
+    """The kernel-only num_splits sweep of "vLLM 0.30.0 FA4 SplitKV Bug: H100
+    Decode Can Be 48% Slower" (section "The kernel-only sweep makes the bug
+    obvious") on this workload: the call and its split kernel alone at each
+    requested split count, with the fraction of split CTAs that scored keys
+    (a split count that never reached the kernel would leave CTAs empty and
+    the times flat)."""
+    out = {"num_splits": [], "us_per_call": [], "kernel_us": [], "nonempty_cta_fraction": []}
+    for S in SWEEP_SPLITS:
+        r = measure(w, dev, splits=S, pool=args.pool, warmup=5)
+        out["num_splits"].append(S)
+        out["us_per_call"].append(r["us"])
+        out["kernel_us"].append(r["kernel_us"])
+        out["nonempty_cta_fraction"].append(r["nonempty"])
+        del r
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import split_kv_paged_splitkv_gb300 as skv
     from split_kv_paged_splitkv_gb300.runner import DecodeSession
@@ -650,6 +674,8 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_per_config:
         line["per_config"] = per_config(dev, args, r)
+        if not w.v_shares_k:  # GQA workloads: the pages' kernel-only sweep
+            line["split_sweep"] = split_sweep(w, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
     if rank == 0:

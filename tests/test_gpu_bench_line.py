@@ -49,6 +49,10 @@ def test_bench_line_has_every_key():
         assert e["nonempty_cta_fraction"] == 1.0, name
     assert pc["mla_t6_ctx64k"]["roofline_bound"] == "tensor"
     assert pc["gqa_ctx5900"]["us_per_call"] == d["value"]
+    sw = d["split_sweep"]
+    assert sw["num_splits"] == [1, 2, 4, 8, 16, 32, 64]
+    assert all(f == 1.0 for f in sw["nonempty_cta_fraction"])
+    assert sw["kernel_us"][-1] < sw["kernel_us"][0] / 8  # splitting pays
     e2e = d["e2e"]
     assert e2e["value"] > d["value"] and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["clocks"]["sm_max_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)
