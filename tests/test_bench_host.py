@@ -78,3 +78,25 @@ def test_algorithmic_counts():
     assert bench.algorithmic_bytes(sv, lm) == 65536 * (576 + 512) * 2 + 6 * 128 * 576 * 2
     f8 = workloads.WORKLOADS["mla_fp8_t6_ctx64k"]
     assert bench.algorithmic_bytes(f8, lm) == 65536 * 576 + 6 * 128 * 576 * 2
+
+
+def test_packed_step_buffer_round_trips():
+    """The end-to-end leg ships a step's inputs in one byte buffer: every
+    tensor at a 256-byte-aligned offset, read back bit for bit through its
+    view (e4m3 codes, bf16 with NaN poison, int32 tables)."""
+    import torch
+    x = workloads.make_inputs(workloads.WORKLOADS["fp8_batch8_ctx32k"].replace(
+        batch=2, lens="list:300:1000"), device="cpu")
+    src = [x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens]
+    offs, n = bench._packed(src)
+    assert all(o % 256 == 0 for o in offs)
+    assert n == offs[-1] + x.seq_lens.numel() * 4
+    for a, b, t in zip(offs, offs[1:], src):
+        assert a + t.numel() * t.element_size() <= b
+    buf = torch.zeros(n, dtype=torch.uint8)
+    views = bench._views(buf, src, offs)
+    for v, t in zip(views, src):
+        v.copy_(t)
+    for v, t in zip(bench._views(buf.clone(), src, offs), src):
+        assert v.dtype == t.dtype and v.shape == t.shape
+        assert torch.equal(v.reshape(-1).view(torch.uint8), t.reshape(-1).view(torch.uint8))
