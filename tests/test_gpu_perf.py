@@ -7,9 +7,12 @@ extra split CTA got an empty KV range, the outputs stayed right, and only a
 kernel-only sweep over num_splits showed the decode getting no faster.  The
 same sweep guards this library: the 5,900-key single-sequence decode must get
 faster at every step from 1 to 64 splits, and at 64 splits at least 8x faster
-than unsplit.  A bandwidth floor guards the long FP8 batch: its split kernel
-alone must move its algorithmic bytes at >= 0.70 of the measured HBM copy
-bandwidth.
+than unsplit.  Floors guard the other workloads: the long FP8 batch's split
+kernel alone must move its algorithmic bytes at >= 0.70 of the measured HBM
+copy bandwidth, the mixed-length bf16 batch of 32 at >= 0.85, the 6-token MLA
+decode's split kernel must reach >= 0.36 of the measured bf16 tensor
+throughput, and the whole 5,900-key call must stay under 7.5 us (each about
+15 % below what this build measures).
 
 Timing: CUDA-graph replay of back-to-back calls rotating over copies of the
 KV pool whose total exceeds four times the L2 size, CUDA events on the
@@ -93,11 +96,21 @@ def test_split_sweep_gets_faster():
     assert t[1] >= 8 * t[64], f"64 splits less than 8x faster than 1 ({msg})"
 
 
-def _hbm_peak():
+def _peak(key, fallback):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        return float(json.load(open(p))["hbm_gbs"])
-    return 6800.0  # one earlier measured copy bandwidth of this part
+        return float(json.load(open(p))[key])
+    return fallback  # one earlier measurement on this part
+
+
+def _hbm_peak():
+    return _peak("hbm_gbs", 6800.0)
+
+
+def _kv_bytes(w, x):
+    lens = x.seq_lens_host.astype(np.int64)
+    kv = 1 if w.kv_dtype == "fp8_e4m3" else 2
+    return int(lens.sum()) * w.num_kv_heads * 2 * w.qk_dim * kv + w.batch * w.num_q_heads * w.qk_dim * 2
 
 
 def test_fp8_batch8_ctx32k_bandwidth_floor():
@@ -106,8 +119,39 @@ def test_fp8_batch8_ctx32k_bandwidth_floor():
     pools = _pools(x)
     sess = session(x, 0)
     us = _us_per_call(sess, x, pools, partials=True, reps=10)
-    lens = x.seq_lens_host.astype(np.int64)
-    nbytes = int(lens.sum()) * w.num_kv_heads * 2 * w.qk_dim + w.batch * w.num_q_heads * w.qk_dim * 2
-    gbs = nbytes / (us * 1e-6) / 1e9
+    gbs = _kv_bytes(w, x) / (us * 1e-6) / 1e9
     peak = _hbm_peak()
     assert gbs >= 0.70 * peak, f"{gbs:.0f} GB/s is below 0.70 of {peak:.0f} GB/s ({us:.1f} us)"
+
+
+def test_mixed_batch32_bf16_bandwidth_floor():
+    w = workloads.WORKLOADS["mixed_batch32_bf16"]
+    x = workloads.make_inputs(w, device="cuda")
+    pools = _pools(x)
+    sess = session(x, 0)
+    us = _us_per_call(sess, x, pools, partials=True, reps=3)
+    gbs = _kv_bytes(w, x) / (us * 1e-6) / 1e9
+    peak = _hbm_peak()
+    assert gbs >= 0.85 * peak, f"{gbs:.0f} GB/s is below 0.85 of {peak:.0f} GB/s ({us:.1f} us)"
+
+
+def test_mla_t6_ctx64k_tensor_floor():
+    w = workloads.WORKLOADS["mla_t6_ctx64k"]
+    x = workloads.make_inputs(w, device="cuda")
+    pools = _pools(x)
+    sess = session(x, 0)
+    us = _us_per_call(sess, x, pools, partials=True, reps=5)
+    # query token t sees L - T + 1 + t keys; QK over 576 dims and PV over 512,
+    # 2 FLOP per multiply-add, 128 heads
+    L, T = int(x.seq_lens_host[0]), w.q_tokens
+    visible = sum(L - T + 1 + t for t in range(T))
+    tflops = 2.0 * w.num_q_heads * visible * (w.qk_dim + w.v_dim) / (us * 1e-6) / 1e12
+    peak = _peak("bf16_tflops", 1900.0)
+    assert tflops >= 0.36 * peak, f"{tflops:.0f} TFLOP/s is below 0.36 of {peak:.0f} ({us:.1f} us)"
+
+
+def test_gqa_ctx5900_call_latency_ceiling():
+    x = workloads.make_inputs(workloads.WORKLOADS["gqa_ctx5900"], device="cuda")
+    pools = _pools(x)
+    us = _us_per_call(session(x, 0), x, pools, reps=200)
+    assert us <= 7.5, f"the 5,900-key call takes {us:.2f} us"
