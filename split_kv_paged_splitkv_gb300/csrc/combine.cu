@@ -173,9 +173,21 @@ namespace {
 // Groups of at most kSmallGroup splits take the warp-per-row form, kSmallLoads
 // splits per pass.  Measured on the MLA merge (768 rows x 512 dims, 12
 // splits): 4.1 us with 8 loads per pass, 4.8 with 16 (162 registers), 5.8
-// with the 4-way form at 4 loads per way, 14.3 at 16 loads per way.
+// with the 4-way form at 4 loads per way, 14.3 at 16 loads per way.  Above
+// kSmallLoads splits that form needs a second dependent pass over L2, which
+// only pays when the launch has rows enough to fill the GPU: a merge of a few
+// rows (one short GQA sequence, 16 rows, 9 to 16 splits) took ~0.5 us longer
+// per call than with 8 or 17 splits, so there the 8-way form (one pass for up
+// to 64 splits) is used instead.
 constexpr int kSmallGroup = 16;
 constexpr int kSmallLoads = 8;
+constexpr long kManyRowCtas = 256;  // warp-per-row CTAs that fill the GPU
+
+bool warp_per_row(int max_splits, long groups, int rows, int dv) {
+  if (max_splits <= kSmallLoads) return true;
+  if (max_splits > kSmallGroup) return false;
+  return groups * ((rows + 3) / 4) * ((dv + 127) / 128) >= kManyRowCtas;
+}
 
 // Shared-memory carveout: the kernel's 3 KB of shared memory would otherwise
 // cap the resident CTAs below what the registers allow.  Set once per
@@ -214,7 +226,8 @@ cudaError_t launch_combine_t(const DecodeArgs& a, bool pdl, cudaStream_t s) {
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream) {
   if (a.n_groups == 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a.max_splits <= kSmallGroup) return launch_combine_t<1, kSmallLoads>(a, pdl, s);
+  if (warp_per_row(a.max_splits, a.n_groups, a.rows, a.dv))
+    return launch_combine_t<1, kSmallLoads>(a, pdl, s);
   return launch_combine_t<8, 8>(a, pdl, s);
 }
 
@@ -224,7 +237,7 @@ cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n
   if (rows == 0) return cudaSuccess;
   dim3 grid(1, rows, (dv + 127) / 128), block(kCombineThreads, 1, 1);  // (small groups)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (n_parts <= kSmallGroup) {
+  if (warp_per_row(n_parts, 1, rows, dv)) {
     cudaError_t e = combine_attrs<1, kSmallLoads>();
     if (e != cudaSuccess) return e;
     grid.y = (rows + 3) / 4;

@@ -59,7 +59,7 @@ def test_paged_gather_is_bit_exact(fp8, P, layout):
 def test_tiny_gqa_ctx260(mode):
     x = workloads.make_inputs(W["tiny_gqa_ctx260"], device="cuda")
     ref_o, ref_l = oracle_direct(x)
-    for S in (1, 4):
+    for S in (1, 4, 12):  # 12: a few rows over 9..16 splits merge in the one-pass form
         s = session(x, S, mode)
         out, lse = s.run()
         compare(out, lse, ref_o, ref_l, what=f"S={S} mode={mode}")
@@ -437,7 +437,8 @@ def test_seq_len_mismatch_is_reported():
 
 
 @pytest.mark.parametrize("S,R,D", [(200, 3, 512), (70, 2, 96), (1, 4, 128), (64, 5, 128),
-                                   (16, 6, 512), (17, 3, 128), (12, 768, 512)])
+                                   (16, 6, 512), (17, 3, 128), (12, 768, 512), (9, 2, 128),
+                                   (13, 1100, 128)])
 def test_combine_many_parts_and_widths(S, R, D):
     """More splits than one load round covers (running maximum across chunks),
     V widths that are not a multiple of 128, a single part, and -inf rows."""
