@@ -155,11 +155,11 @@ __device__ __forceinline__ void store_row(const float (&acc)[DPT], __nv_bfloat16
 // n % 8 of that head), DPT = 128 / TPR consecutive dims from d0.  `mo` is
 // [NCW][8][MO_STRIDE] fp32, `mm`/`ml` [NCW][8]; m is in log2 units.  Partial rows
 // are numbered hs * T*G + row.
-template <bool FP8, int HPI, int NRG>
+template <bool FP8, int HPI, int NRG, int NST>
 __device__ __forceinline__ void merge_and_store(const DecodeArgs& a, int tid, const float* mo,
                                                 const float* mm, const float* ml, int b, int h0,
                                                 int slot) {
-  using C = Gqa<FP8, HPI, NRG>;
+  using C = Gqa<FP8, HPI, NRG, NST>;
   constexpr int NT = C::NCW * 32, TPR = NT / C::ROWS, DPT = 128 / TPR;
   const int n = tid / TPR;           // merge row
   const int sl = n >> 3, r8 = n & 7;
@@ -739,7 +739,7 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, Gqa<FP8, HPI
     ml[warp * 8 + 2 * ti + 1] = l1;
   }
   asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
-  merge_and_store<FP8, HPI, NRG>(a, tid, mo, mm, ml, b, h0, slot);
+  merge_and_store<FP8, HPI, NRG, NST>(a, tid, mo, mm, ml, b, h0, slot);
 
   // Fused combine: last-arriver merges, no waiting.  With S <= kBundle splits
   // the CTA that finishes last merges the group's S partials into the output.
