@@ -425,7 +425,17 @@ splitkv_status decode_impl(const splitkv_plan_t* plan, void* workspace, const vo
   a.hpi = heads_per_item(d);
   if (plan->fixed) a.fx = fixed_shape(*plan, seq_lens);
   a.fused = merge && d.combine_mode == SPLITKV_COMBINE_FUSED;
-  a.deep_ring = plan->n_items <= plan->num_sms ? 1 : 0;
+  // A grid of at most one CTA per SM takes the four-stage ring.  A capacity
+  // plan is made without a device, so its decode reads the SM count of the
+  // device it runs on.
+  int sms = plan->num_sms;
+  if (sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+  }
+  a.deep_ring = plan->n_items <= sms ? 1 : 0;
 
   const int64_t rows_total = int64_t(d.num_pages_total) * d.num_kv_heads * d.page_size;
   if (family_of(d) == Family::kMla) {

@@ -15,14 +15,21 @@
 
 namespace splitkv {
 
-// The length served for sequence b: seq_lens[b] when the plan can serve it
+// The length served for a sequence of length L: L when the plan can serve it
 // (0 <= L <= cap, and L >= T unless L == 0), else 0 -- an empty sequence,
 // with `bad` set.
-__device__ __forceinline__ int fixed_len(const FixedShape& f, int b, bool* bad) {
-  const int L = f.seq_lens[b];
+__device__ __forceinline__ int fixed_len_of(const FixedShape& f, int L, bool* bad) {
   *bad = L < 0 || int64_t(L) > f.cap || (L > 0 && L < f.T);
   return *bad ? 0 : L;
 }
+
+// The length served for sequence b (seq_lens[b], validated as above).
+__device__ __forceinline__ int fixed_len(const FixedShape& f, int b, bool* bad) {
+  return fixed_len_of(f, f.seq_lens[b], bad);
+}
+
+// The sequence of item i.
+__device__ __forceinline__ int fixed_seq(const FixedShape& f, int i) { return i / (f.S * f.U); }
 
 // Splits of sequence b for length L (1 for an empty sequence).
 __device__ __forceinline__ int fixed_splits(const FixedShape& f, int L) {
@@ -30,13 +37,14 @@ __device__ __forceinline__ int fixed_splits(const FixedShape& f, int L) {
   return n > 0 ? min(f.S, n) : 1;
 }
 
-// Work-list fields of item i (SPLITKV_ITEM_* order); *L receives the length
-// served and *bad whether seq_lens[b] was replaced by 0.
-__device__ __forceinline__ void fixed_item(const FixedShape& f, int i,
-                                           int32_t (&it)[SPLITKV_ITEM_FIELDS], int* L,
-                                           bool* bad) {
-  const int s = i % f.S, u = (i / f.S) % f.U, b = i / (f.S * f.U);
-  *L = fixed_len(f, b, bad);
+// Work-list fields of item i (SPLITKV_ITEM_* order) when its sequence has
+// length L_raw; *L receives the length served and *bad whether L_raw was
+// replaced by 0.
+__device__ __forceinline__ void fixed_item_at(const FixedShape& f, int i, int L_raw,
+                                              int32_t (&it)[SPLITKV_ITEM_FIELDS], int* L,
+                                              bool* bad) {
+  const int s = i % f.S, u = (i / f.S) % f.U, b = fixed_seq(f, i);
+  *L = fixed_len_of(f, L_raw, bad);
   const int n = (*L + f.P - 1) / f.P;
   const int Sb = fixed_splits(f, *L);
   const int g = b * f.U + u;
@@ -49,6 +57,13 @@ __device__ __forceinline__ void fixed_item(const FixedShape& f, int i,
   it[SPLITKV_ITEM_PAGE1] = s < Sb && n > 0 ? int32_t((int64_t(s + 1) * n) / Sb) : 0;
   it[SPLITKV_ITEM_SLOT] = s < Sb && split ? g * f.S + s : -1;
   it[SPLITKV_ITEM_GROUP] = s < Sb && split ? g : -1;
+}
+
+// The same from the current device length seq_lens[b].
+__device__ __forceinline__ void fixed_item(const FixedShape& f, int i,
+                                           int32_t (&it)[SPLITKV_ITEM_FIELDS], int* L,
+                                           bool* bad) {
+  fixed_item_at(f, i, f.seq_lens[fixed_seq(f, i)], it, L, bad);
 }
 
 // Combine group g = b * U + u: (b, first KV head, splits to merge -- 0 when

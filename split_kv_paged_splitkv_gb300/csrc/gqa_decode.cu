@@ -320,33 +320,16 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, Gqa<FP8, HPI
   int* pt = misc + 16;                                 // staged block-table entries, per producer
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // A capacity plan's item is derived from the device lengths (read after the
-  // dependency wait); a host plan's comes from the uploaded work list.
+  // A host plan's item comes from the uploaded work list, with the plan's
+  // copy of the sequence length (read first, so that these loads overlap the
+  // rest of the prologue).
   int32_t it[SPLITKV_ITEM_FIELDS];
-  int L_fixed = 0;
-  if (a.fixed) {
-    wait_prerequisites();
-    bool bad;
-    fixed_item(a.fx, blockIdx.x, it, &L_fixed, &bad);
-    if (threadIdx.x == 0) fixed_write_group(a.fx, const_cast<int32_t*>(a.groups), it);
-  } else {
+  int L = 0;
+  if (!a.fixed) {
     const int32_t* src = a.items + size_t(blockIdx.x) * SPLITKV_ITEM_FIELDS;
 #pragma unroll
     for (int k = 0; k < SPLITKV_ITEM_FIELDS; ++k) it[k] = src[k];
-  }
-  const int b = it[SPLITKV_ITEM_B], h0 = it[SPLITKV_ITEM_HKV];  // heads h0 .. h0+HPI-1
-  const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
-  const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
-  const int slot = it[SPLITKV_ITEM_SLOT], group = it[SPLITKV_ITEM_GROUP];
-  if (nsplit == 0) {  // a capacity item the current sequence lengths leave unused
-    if (threadIdx.x == 0) {
-      int32_t* lg = a.cta_log + size_t(blockIdx.x) * kLogFields;
-      lg[0] = p0;
-      lg[1] = p1;
-      lg[2] = 0;
-      lg[3] = 0;
-    }
-    return;
+    L = a.plan_lens[it[SPLITKV_ITEM_B]];
   }
 
   // Prologue: only shared memory, the tensor maps and the uploaded work list,
@@ -367,18 +350,57 @@ __global__ void __launch_bounds__(Gqa<FP8, HPI, NRG, NST>::THREADS, Gqa<FP8, HPI
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
   }
-  // The plan's copy of the sequence length (uploaded with the work list, never
-  // written by a kernel) is read before the wait; the caller's device copy is
-  // only checked against it, off the critical path.
-  const int L = a.fixed ? L_fixed : a.plan_lens[b];
+  __syncthreads();  // barriers initialised before any thread uses them
+  launch_dependents();
+  // The plan's copy of the length is never written by a kernel; the caller's
+  // device copy is only checked against it, after the wait and off the
+  // critical path.  A capacity plan's item is derived from the device length
+  // after the wait; before it, a relaxed read of that length (which the
+  // previous kernel may still be writing) gives a speculative item whose
+  // first tiles are only prefetched into L2, so a stale value costs nothing
+  // but the prefetch.  Only the first producer warp issues the prefetches:
+  // the other warps go straight to the dependency wait.
+  if (a.fixed) {
+    if (a.deep_ring && warp == C::NCW) {
+      int Ls;
+      bool bad_s;
+      fixed_item_at(a.fx, blockIdx.x, ld_relaxed_gpu(a.fx.seq_lens + fixed_seq(a.fx, blockIdx.x)),
+                    it, &Ls, &bad_s);
+      if (it[SPLITKV_ITEM_NSPLIT] > 0) {
+        const int kb = it[SPLITKV_ITEM_PAGE0] * a.P, ke = min(it[SPLITKV_ITEM_PAGE1] * a.P, Ls);
+        prefetch_first_tiles<C, FP8>(a, &tk, &tv, it[SPLITKV_ITEM_B], it[SPLITKV_ITEM_HKV], kb,
+                                     ke > kb ? (ke - kb + 15) >> 4 : 0, lane);
+      }
+    }
+    wait_prerequisites();
+    bool bad;
+    fixed_item(a.fx, blockIdx.x, it, &L, &bad);
+    if (threadIdx.x == 0) fixed_write_group(a.fx, const_cast<int32_t*>(a.groups), it);
+  } else {
+    if (a.deep_ring && warp == C::NCW) {
+      const int kb = it[SPLITKV_ITEM_PAGE0] * a.P, ke = min(it[SPLITKV_ITEM_PAGE1] * a.P, L);
+      prefetch_first_tiles<C, FP8>(a, &tk, &tv, it[SPLITKV_ITEM_B], it[SPLITKV_ITEM_HKV], kb,
+                                   ke > kb ? (ke - kb + 15) >> 4 : 0, lane);
+    }
+    wait_prerequisites();
+  }
+  const int b = it[SPLITKV_ITEM_B], h0 = it[SPLITKV_ITEM_HKV];  // heads h0 .. h0+HPI-1
+  const int split = it[SPLITKV_ITEM_SPLIT], nsplit = it[SPLITKV_ITEM_NSPLIT];
+  const int p0 = it[SPLITKV_ITEM_PAGE0], p1 = it[SPLITKV_ITEM_PAGE1];
+  const int slot = it[SPLITKV_ITEM_SLOT], group = it[SPLITKV_ITEM_GROUP];
+  if (nsplit == 0) {  // a capacity item the current sequence lengths leave unused
+    if (threadIdx.x == 0) {
+      int32_t* lg = a.cta_log + size_t(blockIdx.x) * kLogFields;
+      lg[0] = p0;
+      lg[1] = p1;
+      lg[2] = 0;
+      lg[3] = 0;
+    }
+    return;
+  }
   const int k_begin = p0 * a.P;
   const int k_end = min(p1 * a.P, L);
   const int n_tiles = k_end > k_begin ? (k_end - k_begin + 15) >> 4 : 0;
-  if (a.deep_ring && !a.fixed && warp == C::NCW)
-    prefetch_first_tiles<C, FP8>(a, &tk, &tv, b, h0, k_begin, n_tiles, lane);
-  __syncthreads();
-  launch_dependents();
-  wait_prerequisites();
   if (threadIdx.x == 0 && a.seq_lens[b] != L) atomicOr(a.status, SPLITKV_DEVERR_SEQLEN);
 
   if (warp >= C::NCW) {
