@@ -8,7 +8,9 @@
 // the ldmatrix reads below are bank-conflict free.  The boxes land in a ring
 // of NST stages guarded by mbarriers: two 32 KB stages, so that three CTAs
 // share an SM, or four for a grid of at most one CTA per SM, whose producer
-// also warms L2 with its first tiles before the dependency wait.  One
+// also warms L2 with its first tiles before the dependency wait (a capacity
+// plan's CTA picks those tiles from a speculative read of the device length;
+// its real item comes from the length read after the wait).  One
 // producer warp issues the copies (four, taking the tiles round-robin, in
 // the four-stage form, whose CTA has an SM to itself).  The four consumer
 // warps form slots (head slot, row group): each slot serves query rows
