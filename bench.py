@@ -574,6 +574,25 @@ def per_config(dev, args, headline):
     return out
 
 
+CAPACITY_SPLITS = 64
+
+
+def capacity_plan(w, dev, args):
+    """The same workload through a capacity plan (splitkv_plan_fixed) of
+    CAPACITY_SPLITS splits: the form one captured CUDA graph serves any
+    lengths with, its kernels deriving their items from the device lengths
+    each call.  About 50 ms of timed calls, like the other entries."""
+    r = measure(w, dev, splits=CAPACITY_SPLITS, fixed=True, pool=args.pool, warmup=5)
+    roof = r["roof"]
+    out = {"num_splits": CAPACITY_SPLITS, "us_per_call": r["us"], "kernel_us": roof["kernel_us"],
+           "achieved": roof["achieved"], "unit": roof["unit"], "frac": roof["frac"],
+           "nonempty_cta_fraction": r["nonempty"], "planned_items": int(len(r["items"])),
+           "steps": r["steps"]}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
 SWEEP_SPLITS = (1, 2, 4, 8, 16, 32, 64)
 
 
@@ -676,6 +695,7 @@ def run_ours(args, rank, world, local):
         line["per_config"] = per_config(dev, args, r)
         if not w.v_shares_k:  # GQA workloads: the pages' kernel-only sweep
             line["split_sweep"] = split_sweep(w, dev, args)
+            line["capacity_plan"] = capacity_plan(w, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
     if rank == 0:

@@ -53,6 +53,9 @@ def test_bench_line_has_every_key():
     assert sw["num_splits"] == [1, 2, 4, 8, 16, 32, 64]
     assert all(f == 1.0 for f in sw["nonempty_cta_fraction"])
     assert sw["kernel_us"][-1] < sw["kernel_us"][0] / 8  # splitting pays
+    cp = d["capacity_plan"]
+    assert cp["num_splits"] == 64 and cp["planned_items"] == 2 * 64
+    assert cp["us_per_call"] > 0 and cp["kernel_us"] > 0 and cp["nonempty_cta_fraction"] == 1.0
     e2e = d["e2e"]
     assert e2e["value"] > d["value"] and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["clocks"]["sm_max_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)
