@@ -234,7 +234,8 @@ import oracle
 d = pickle.load(open({path!r}, 'rb'))
 def call():
     oracle.attention_direct(d['q'], d['k'], d['v'], d['table'], d['lens'], scale=d['scale'],
-        kv_dtype=d['kv_dtype'], kv_scale=d['kv_scale'], v_dim=d['v_dim'], v_shares_k=d['v_shares_k'])
+        kv_dtype=d['kv_dtype'], kv_scale=d['kv_scale'], v_dim=d['v_dim'], v_shares_k=d['v_shares_k'],
+        layout=d['layout'])
 for _ in range(d['warmup']):
     call()
 # start together with the other processes of the same sample
@@ -267,7 +268,8 @@ def time_oracle(w, x, seconds, calls=0, warmup=0, procs=1):
                    v=None if x.v_pages is None else workloads.bits(x.v_pages),
                    table=x.block_table.cpu().numpy(), lens=x.seq_lens_host, scale=x.scale,
                    kv_dtype=w.kv_dtype, kv_scale=x.kv_scale, v_dim=w.v_dim,
-                   v_shares_k=w.v_shares_k, seconds=seconds, calls=calls, warmup=warmup)
+                   v_shares_k=w.v_shares_k, layout=x.layout, seconds=seconds, calls=calls,
+                   warmup=warmup)
     with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
         pickle.dump(payload, f)
         path = f.name
@@ -320,13 +322,21 @@ def cpu_baseline(w, x, seconds):
 
 # ----------------------------------------------------------------- reference arm
 
+def workload_config(w, args):
+    """The keys naming the workload, shared by both arms' JSON lines."""
+    return {"workload": w.name, "batch": w.batch, "q_tokens": w.q_tokens,
+            "heads_q_kv": [w.num_q_heads, w.num_kv_heads], "head_dim": w.qk_dim,
+            "context": w.lens, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+            "kv_layout": args.layout.upper()}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
     w = workloads.WORKLOADS[args.workload]
     if args.page_size:
         w = dataclasses.replace(w, page_size=args.page_size)
-    x = workloads.make_inputs(w, device="cpu")
+    x = workloads.make_inputs(w, device="cpu", layout=args.layout.upper())
     # Each step is one full oracle call; the run is bounded by --cpu-seconds
     # (so at most --steps calls, at least one).
     per_call, _ = time_oracle(w, x, 0.0)
@@ -337,7 +347,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
         "steps": n, "warmup": warm, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "page_size": w.page_size},
+        "config": workload_config(w, args),
         "cpu_baseline": {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": oracle_sample_desc(w, n, 1)},
         "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -674,10 +684,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "f16",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "q_tokens": w.q_tokens,
-                   "heads_q_kv": [w.num_q_heads, w.num_kv_heads], "head_dim": w.qk_dim,
-                   "context": w.lens, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
-                   "kv_layout": args.layout.upper(),
+        "config": {**workload_config(w, args),
                    "num_splits": args.splits, "planned_items": int(len(items)),
                    "plan": "capacity plan, items derived from the device lengths each step" if args.fixed else "host",
                    "combine": args.combine, "parallelism": f"replicas{world}",
