@@ -410,38 +410,97 @@ def capture(run_step, n, first=0):
 
 class Replayer:
     """Back-to-back calls of `run_step(i)` (i cycling over R steps of
-    distinct pages) as CUDA graphs: the R-step cycle, and on demand a graph
-    of the K mod R steps left over (all K when K < R).  Every graph is
-    replayed before it is timed, and the steps just before a timed region
-    are always the cycle's, so the first timed step's pages were last read
-    R - 1 steps earlier."""
+    distinct pages) as CUDA graphs: the R-step cycle, and on demand the
+    graphs that open and close a timed region.
+    Every graph is replayed before it is timed, and the steps just before a
+    timed step are always the cycle's, so each timed step's pages were last
+    read R - 1 steps earlier."""
 
     def __init__(self, run_step, R):
         self.run_step, self.R = run_step, R
         self.cycle = capture(run_step, R)
-        self.tails = {}
+        self.bracketed, self.tails = {}, {}
 
     def warm(self, reps=1):
         for _ in range(max(1, reps)):
             self.cycle.replay()
 
+    def _graph(self, n, lead, end):
+        """Graph of steps 0 .. n-1 with events inside it: with `lead`, one
+        untimed lead-in call (the cycle's last step) and then the start
+        event before them; with `end`, the end event after them."""
+        key = (n, lead, end)
+        if key not in self.bracketed:
+            e0 = torch.cuda.Event(enable_timing=True, external=True) if lead else None
+            e1 = torch.cuda.Event(enable_timing=True, external=True) if end else None
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                if lead:
+                    self.run_step(self.R - 1)
+                    e0.record()
+                for i in range(n):
+                    self.run_step(i)
+                if end:
+                    e1.record()
+            self.bracketed[key] = (g, e0, e1)
+        return self.bracketed[key]
+
     def time(self, K, stream, warm_reps=1):
-        """µs per step over exactly K timed steps (CUDA events on `stream`)."""
+        """µs per step over exactly K timed steps (CUDA events on `stream`).
+
+        Both events are recorded inside graphs: the start event after an
+        untimed lead-in call, so the first timed call overlaps its
+        predecessor's tail (programmatic dependent launch) as every later
+        call does, and the end event right after the last timed call, so
+        neither graph launch nor graph completion falls inside the region.
+        Where the torch build cannot record an event inside a graph, the
+        events are recorded on the stream around the graphs."""
+        try:
+            return self._time_in_graph(K, stream, warm_reps)
+        except (TypeError, RuntimeError):
+            return self._time_on_stream(K, stream, warm_reps)
+
+    def _time_in_graph(self, K, stream, warm_reps):
+        # K = q R + r with 1 <= r <= R: the first graph opens the region, q - 1
+        # plain cycles follow, and the last graph (r steps) closes it.
+        q, r = divmod(K - 1, self.R)
+        r += 1
+        if q == 0:
+            g, e0, e1 = self._graph(r, True, True)
+            graphs = [g]
+        else:
+            head, e0, _ = self._graph(self.R, True, False)
+            last, _, e1 = self._graph(r, False, True)
+            graphs = [head] + [self.cycle] * (q - 1) + [last]
+        for g in set(graphs):
+            g.replay()  # first replays (graph upload) stay untimed
+        self.warm(warm_reps)
+        torch.cuda.synchronize()
+        # A short device-side spin keeps the GPU busy while the host
+        # enqueues the graph launches.
+        torch.cuda._sleep(100000)
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / K
+        if not us > 0:
+            raise RuntimeError("no usable events inside the graphs")
+        return us
+
+    def _tail(self, n):
+        if n not in self.tails:
+            self.tails[n] = capture(self.run_step, n)
+        return self.tails[n]
+
+    def _time_on_stream(self, K, stream, warm_reps):
         reps, rem = divmod(K, self.R)
-        tail = None
-        if rem:
-            if rem not in self.tails:
-                self.tails[rem] = capture(self.run_step, rem)
-            tail = self.tails[rem]
-            tail.replay()  # its first replay (graph upload) stays untimed
+        tail = self._tail(rem) if rem else None
+        if tail is not None:
+            tail.replay()
         self.warm(warm_reps)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        # A short device-side spin (outside the timed region) keeps the GPU
-        # busy while the host enqueues the start event and the first graph
-        # launch, so the host's launch latency does not land between the
-        # start event and the first call.
         torch.cuda._sleep(100000)
         e0.record(stream)
         for _ in range(reps):
@@ -690,7 +749,9 @@ def run_ours(args, rank, world, local):
                    "combine": args.combine, "parallelism": f"replicas{world}",
                    "l2": pool_desc,
                    "timing": "CUDA-graph replay of back-to-back calls (every graph replayed "
-                             "before timing), CUDA events on the launching stream"},
+                             "before timing; the start event recorded inside the first graph, "
+                             "after one untimed lead-in call), CUDA events on the launching "
+                             "stream"},
         "roofline": roof,
         "nonempty_cta_fraction": r["nonempty"],
         "cold_us_per_call": cold_us,
