@@ -85,7 +85,7 @@ typedef enum splitkv_kv_layout {
 typedef struct splitkv_desc {
   int32_t batch;              /* B, >= 1                                        */
   int32_t q_tokens;           /* T query tokens per sequence, causal among them;
-                                 GQA: T * (Hq / Hkv) <= 16; MLA: T <= 16       */
+                                 GQA: T * (Hq / Hkv) <= 32; MLA: T <= 16       */
   int32_t num_q_heads;        /* Hq                                             */
   int32_t num_kv_heads;       /* Hkv, divides Hq                                */
   int32_t qk_dim;             /* Dk: 128 (GQA) or 576 (MLA latent + rope)       */

@@ -140,7 +140,7 @@ splitkv_status validate_desc(const splitkv_desc_t* d) {
   if (family_of(*d) == Family::kNone)
     return fail(SPLITKV_EUNSUPPORTED,
                 "no kernel for qk_dim=%d v_dim=%d T=%d G=%d kv_dtype=%d v_shares_k=%d "
-                "(GQA: qk_dim=v_dim=128, T*G<=16; MLA: 128 q heads, 1 latent head, "
+                "(GQA: qk_dim=v_dim=128, T*G<=32; MLA: 128 q heads, 1 latent head, "
                 "qk_dim=576, v_dim=512, page_size 16, 32 or a multiple of 64, T<=16, "
                 "e4m3 only with V in the latent rows)",
                 d->qk_dim, d->v_dim, d->q_tokens, d->num_q_heads / d->num_kv_heads, d->kv_dtype,
@@ -160,7 +160,7 @@ splitkv_status fail(splitkv_status s, const char* fmt, ...) {
 
 Family family_of(const splitkv_desc_t& d) {
   const int G = d.num_q_heads / d.num_kv_heads;
-  if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 16) return Family::kGqa;
+  if (d.qk_dim == 128 && d.v_dim == 128 && !d.v_shares_k && d.q_tokens * G <= 32) return Family::kGqa;
   // V either shares the latent rows (their first 512 columns) or is its own
   // tensor.  Keys stream in 64-key blocks: pages of 16 or 32 keys fill a block
   // with 4 or 2 boxes, larger pages (multiples of 64) hold whole blocks.

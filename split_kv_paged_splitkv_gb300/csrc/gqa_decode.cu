@@ -23,7 +23,8 @@
 //   O^T[128 x 8 rows]   += V_tile^T[128 x 16] . P^T     (m16n8k16, dims on M)
 // so a row group of up to 8 query rows fills the MMA's N side (9 to 16 rows
 // per KV head -- speculative decode -- take two row groups over the same
-// tiles) and the 16-key tile fills M with no padding.  P^T is turned from
+// tiles, 17 to 32 four, one warp each) and the 16-key tile fills M with no
+// padding.  P^T is turned from
 // accumulator layout into operand layout in registers with movmatrix.  FP8
 // e4m3 tiles are converted to f16 in registers (exact, ptx::e4m3x2_*) and
 // use the f16 MMA; BF16 tiles go straight to the bf16 MMA.
@@ -64,7 +65,7 @@ using namespace ptx;
 template <bool FP8, int HPI, int NRG = 1, int NST_ = 2>
 struct Gqa {
   static_assert(HPI == 1 || (FP8 && (HPI == 2 || HPI == 4)), "heads per item");
-  static_assert(NRG == 1 || (NRG == 2 && HPI == 1), "row groups per head");
+  static_assert(NRG == 1 || ((NRG == 2 || NRG == 4) && HPI == 1), "row groups per head");
   static constexpr int D = 128;
   static constexpr int TK = 16;                            // keys per tile
   static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one head's K (or V) rows
@@ -897,6 +898,11 @@ constexpr int kDeepStages = 4;
 template <int NST>
 cudaError_t launch_gqa_nst(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                            bool fp8, cudaStream_t s) {
+  if (a.T * a.G > 16) {  // 17..32 query rows per KV head: four row groups
+    if (a.hpi != 1) return cudaErrorInvalidValue;
+    return fp8 ? launch_gqa_t<true, 1, 4, NST>(a, mk, mv, s)
+               : launch_gqa_t<false, 1, 4, NST>(a, mk, mv, s);
+  }
   if (a.T * a.G > 8) {  // 9..16 query rows per KV head: two row groups
     if (a.hpi != 1) return cudaErrorInvalidValue;
     return fp8 ? launch_gqa_t<true, 1, 2, NST>(a, mk, mv, s)

@@ -124,7 +124,7 @@ def test_plan_slots_and_groups_are_consistent():
     (dict(P=8), skv.SPLITKV_EINVAL),
     (dict(Hq=15), skv.SPLITKV_EINVAL),
     (dict(D=96, Dv=96), skv.SPLITKV_EUNSUPPORTED),
-    (dict(T=3, Hq=16, Hkv=2), skv.SPLITKV_EUNSUPPORTED),  # 3 * 8 query rows per KV head > 16
+    (dict(T=5, Hq=16, Hkv=2), skv.SPLITKV_EUNSUPPORTED),  # 5 * 8 query rows per KV head > 32
     (dict(N=0), skv.SPLITKV_EINVAL),
 ])
 def test_plan_rejects_bad_descriptors(bad, code):

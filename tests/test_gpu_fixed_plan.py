@@ -88,7 +88,7 @@ def test_refreshed_work_list_equals_the_planner(fp8, Hkv, G):
 
 
 @pytest.mark.parametrize("mode", [skv.SPLITKV_COMBINE_SEPARATE, skv.SPLITKV_COMBINE_FUSED])
-@pytest.mark.parametrize("T,G", [(1, 8), (2, 8)])
+@pytest.mark.parametrize("T,G", [(1, 8), (2, 8), (4, 8)])
 def test_one_graph_serves_changing_lengths(mode, T, G):
     """Capture the decode once; change the device lengths; replay."""
     cap = [16 * 30 + 3, 16 * 61, 16 * 9 + 7]

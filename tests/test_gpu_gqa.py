@@ -141,11 +141,13 @@ def test_ragged_lengths(fp8, G, Hkv, P):
 
 
 @pytest.mark.parametrize("T,G", [(2, 4), (8, 1), (4, 2), (3, 2),
-                                 (2, 8), (4, 4), (3, 5), (16, 1), (5, 2)])
+                                 (2, 8), (4, 4), (3, 5), (16, 1), (5, 2),
+                                 (3, 8), (4, 8), (6, 4), (16, 2), (5, 6)])
 @pytest.mark.parametrize("fp8", [False, True])
 def test_multi_token_causal(T, G, fp8):
     """Speculative decode: T query tokens, causal among themselves; T*G > 8
-    takes the two-row-group kernel (query rows 8..15 of a KV head)."""
+    takes the two-row-group kernel (query rows 8..15 of a KV head), T*G > 16
+    the four-row-group one (up to 32 rows)."""
     lens = [T, T + 1, 37, 300, 16 * 5]
     w = _custom(lens, G=G, Hkv=2, T=T, fp8=fp8, seed=T * 7 + G)
     x = workloads.make_inputs(w, device="cuda")
@@ -185,6 +187,20 @@ def test_per_head_kv_scales(T, G, Hkv):
             out, lse = s.run()
             compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} Hkv={Hkv} S={S}")
             assert s.stats()[1] == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_thirty_two_rows_per_head_long_context(fp8):
+    """T*G = 32 (four tokens of a G = 8 group) over a long context with the
+    planner's splits, one-wave and multi-wave grids."""
+    for lens, Hkv in (([2048 + 9, 700, 16], 4), ([4000, 3000, 2500, 1800, 1200, 900, 600, 33], 8)):
+        w = _custom(lens, G=8, Hkv=Hkv, T=4, fp8=fp8, seed=93 + Hkv)
+        x = workloads.make_inputs(w, device="cuda")
+        ref_o, ref_l = oracle_direct(x)
+        s = session(x, 0)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"T=4 G=8 Hkv={Hkv} planner")
+        assert s.stats()[1] == 0
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -290,7 +306,7 @@ def test_mixed_batch32_full(name):
 
 # ------------------------------------------------------------------ query magnitudes (e4m3)
 
-@pytest.mark.parametrize("T,G", [(1, 8), (2, 8), (1, 4)])
+@pytest.mark.parametrize("T,G", [(1, 8), (2, 8), (1, 4), (4, 8)])
 def test_e4m3_queries_of_any_bf16_magnitude(T, G):
     """The e4m3 path multiplies bf16 queries with f16 tensor-core products;
     each query row is scaled by a power of two into f16's range first.  Rows

@@ -43,7 +43,7 @@ def _lens(rng, B, P, T, max_len):
 def test_random_gqa(case):
     rng = np.random.default_rng(500 + case)
     T = int(rng.choice([1, 1, 2, 3, 4]))
-    G = int(rng.choice([g for g in (1, 2, 4, 5, 8) if T * g <= 16]))
+    G = int(rng.choice([g for g in (1, 2, 4, 5, 8) if T * g <= 32]))
     Hkv = int(rng.choice([1, 2, 3, 4]))
     P = int(rng.choice([16, 32, 64]))
     B = int(rng.integers(1, 5))
