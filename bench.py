@@ -621,8 +621,9 @@ def measure(w, dev, *, splits=0, fixed=False, mode=None, layout="hnd", pool="sin
             "nonempty": nonempty, "roof": roof, "clocks": clocks, "steps": steps}
 
 
-PER_CONFIG = ("tiny_gqa_ctx260", "gqa_ctx5900", "fp8_batch8_ctx32k", "mla_t6_ctx64k",
-              "mla_sepv_t6_ctx64k", "mla_fp8_t6_ctx64k", "mixed_batch32_bf16", "mixed_batch32_fp8")
+PER_CONFIG = ("tiny_gqa_ctx260", "gqa_ctx5900", "spec_t4_gqa_ctx5900", "fp8_batch8_ctx32k",
+              "mla_t6_ctx64k", "mla_sepv_t6_ctx64k", "mla_fp8_t6_ctx64k", "mixed_batch32_bf16",
+              "mixed_batch32_fp8")
 
 
 def per_config(dev, args, headline):

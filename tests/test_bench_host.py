@@ -76,6 +76,9 @@ def test_algorithmic_counts():
     assert bench.is_tensor_bound(m) and not bench.is_tensor_bound(w)
     sv = workloads.WORKLOADS["mla_sepv_t6_ctx64k"]
     assert bench.algorithmic_bytes(sv, lm) == 65536 * (576 + 512) * 2 + 6 * 128 * 576 * 2
+    sp = workloads.WORKLOADS["spec_t4_gqa_ctx5900"]
+    # the four tokens share the keys: KV counted once, Q for every token
+    assert bench.algorithmic_bytes(sp, lens) == 5900 * 2 * 2 * 128 * 2 + 4 * 16 * 128 * 2
     f8 = workloads.WORKLOADS["mla_fp8_t6_ctx64k"]
     assert bench.algorithmic_bytes(f8, lm) == 65536 * 576 + 6 * 128 * 576 * 2
 

@@ -84,6 +84,21 @@ def test_gqa_ctx5900_split_sweep(mode):
         assert np.abs(o - outs[0]).max() <= OUT_TOL
 
 
+@pytest.mark.parametrize("mode", [skv.SPLITKV_COMBINE_FUSED, skv.SPLITKV_COMBINE_SEPARATE])
+def test_spec_t4_gqa_ctx5900(mode):
+    """Four speculative tokens of each G = 8 group over the 5.9k context (32
+    query rows per KV head): every split count of the workload against the
+    oracle, and the splits agree with one another."""
+    x = workloads.make_inputs(W["spec_t4_gqa_ctx5900"], device="cuda")
+    ref_o, ref_l = oracle_direct(x)
+    for S in W["spec_t4_gqa_ctx5900"].splits:
+        s = session(x, S, mode)
+        out, lse = s.run()
+        compare(out, lse, ref_o, ref_l, what=f"T=4 S={S} mode={mode}")
+        log, status = s.stats()
+        assert status == 0 and (log[:, 2] > 0).all()
+
+
 def test_split_ranges_and_nonempty_ctas():
     """Every launched CTA iterated exactly its planned page range and scored keys."""
     x = workloads.make_inputs(W["gqa_ctx5900"], device="cuda")

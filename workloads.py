@@ -66,7 +66,7 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads, each with its own seed (1000 + index).
+# The workloads, each with its own seed.
 WORKLOADS = {
     "tiny_gqa_ctx260": Workload(
         "tiny_gqa_ctx260", 1, 1, 16, 2, 128, 128, 16, "bf16", "fixed:260",
@@ -88,6 +88,11 @@ WORKLOADS = {
     "mla_fp8_t6_ctx64k": Workload(
         "mla_fp8_t6_ctx64k", 1, 6, 128, 1, 576, 512, 64, "fp8_e4m3", "fixed:65536",
         std=0.5, v_shares_k=True, splits=(1, 4, 8, 0), pool_slack=0.0, seed=1007),
+    # speculative decode: four query tokens of each G = 8 group (32 rows per
+    # KV head, causal among themselves) over the 5.9k context
+    "spec_t4_gqa_ctx5900": Workload(
+        "spec_t4_gqa_ctx5900", 1, 4, 16, 2, 128, 128, 16, "bf16", "fixed:5900",
+        splits=(1, 8, 0), pool_slack=0.39, seed=1008),
     "mixed_batch32_bf16": Workload(
         "mixed_batch32_bf16", 32, 1, 32, 8, 128, 128, 16, "bf16",
         "loguniform:256:131072", splits=(0,), pool_slack=0.02, seed=1005),
