@@ -23,8 +23,7 @@
 //   O^T[128 x 8 rows]   += V_tile^T[128 x 16] . P^T     (m16n8k16, dims on M)
 // so a row group of up to 8 query rows fills the MMA's N side (9 to 16 rows
 // per KV head -- speculative decode -- take two row groups over the same
-// tiles, 17 to 32 four, one warp each) and the 16-key tile fills M with no
-// padding.  P^T is turned from
+// tiles, 17 to 32 four) and the 16-key tile fills M with no padding.  P^T is turned from
 // accumulator layout into operand layout in registers with movmatrix.  FP8
 // e4m3 tiles are converted to f16 in registers (exact, ptx::e4m3x2_*) and
 // use the f16 MMA; BF16 tiles go straight to the bf16 MMA.
@@ -73,7 +72,11 @@ struct Gqa {
   static constexpr int STAGE = 32768;
   static constexpr int TPS = STAGE / TILE;                 // tiles per stage
   static constexpr int NST = NST_;                         // stages in the ring
-  static constexpr int NCW = 4;                            // consumer warps
+  // Consumer warps: eight when two or four row groups share a one-wave CTA
+  // (more warps per row group shorten the chain of tiles each scores: on the
+  // 5.9k shape two tokens of a G = 8 group took 7.35 -> 7.11 us per call,
+  // four 8.82 -> 8.41), else four.
+  static constexpr int NCW = NST_ == 4 && NRG >= 2 ? 8 : 4;
   // Producer warps: four for the one-wave four-stage ring (tiles go to them
   // round-robin; measured on GB300, a CTA's cold 48 KB lands about 13 %
   // sooner when four warps issue its boxes than when one does), one for the
