@@ -221,9 +221,9 @@ int32_t splitkv_plan_num_items(const splitkv_plan_t* plan);
 int32_t splitkv_plan_num_ctas(const splitkv_plan_t* plan);
 
 /* KV heads one work item covers: 2 when Hkv is even for the e4m3 GQA path
- * with at most 8 query rows (T * G) per KV head, where one TMA box then
- * brings a 16-key tile of both; 1 otherwise.  Partial-result rows of an item are numbered
- * head_slot * T * G + t * G + g. */
+ * with at most 16 query rows (T * G) per KV head, where one TMA box then
+ * brings a 16-key tile of both; 1 otherwise.  Partial-result rows of an item
+ * are numbered head_slot * T * G + t * G + g. */
 int32_t splitkv_plan_heads_per_item(const splitkv_plan_t* plan);
 
 /* Kernel launches one splitkv_decode of this plan makes (1 or 2: the split

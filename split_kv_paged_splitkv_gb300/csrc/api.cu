@@ -183,9 +183,12 @@ int ctas_per_sm(const splitkv_desc_t& d) {
 
 int heads_per_item(const splitkv_desc_t& d) {
   const int rows_per_head = d.q_tokens * (d.num_q_heads / d.num_kv_heads);
-  if (family_of(d) != Family::kGqa || d.kv_dtype != SPLITKV_FP8_E4M3 || rows_per_head > 8) return 1;
+  if (family_of(d) != Family::kGqa || d.kv_dtype != SPLITKV_FP8_E4M3 || rows_per_head > 16) return 1;
   // Two heads per item measured best on GB300 (e4m3, 32 query / 4 KV heads,
-  // 28k-33k keys: 47.1 us per call against 50.1 with four and 54.9 with one).
+  // 28k-33k keys: 47.1 us per call against 50.1 with four and 54.9 with one;
+  // with two query tokens, 16 rows per head, 60.3 against 69.4 with one).
+  // Past 16 rows the two heads' four row groups would need more warps than
+  // the two-stage kernel form has threads and registers for.
   return d.num_kv_heads % 2 == 0 ? 2 : 1;
 }
 

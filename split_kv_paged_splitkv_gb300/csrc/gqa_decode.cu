@@ -64,7 +64,8 @@ using namespace ptx;
 template <bool FP8, int HPI, int NRG = 1, int NST_ = 2>
 struct Gqa {
   static_assert(HPI == 1 || (FP8 && (HPI == 2 || HPI == 4)), "heads per item");
-  static_assert(NRG == 1 || ((NRG == 2 || NRG == 4) && HPI == 1), "row groups per head");
+  static_assert(NRG == 1 || ((NRG == 2 || NRG == 4) && HPI == 1) || (NRG == 2 && HPI == 2),
+                "row groups per head");
   static constexpr int D = 128;
   static constexpr int TK = 16;                            // keys per tile
   static constexpr int KT_BYTES = TK * D * (FP8 ? 1 : 2);  // one head's K (or V) rows
@@ -907,6 +908,7 @@ cudaError_t launch_gqa_nst(const DecodeArgs& a, const CUtensorMap& mk, const CUt
                : launch_gqa_t<false, 1, 4, NST>(a, mk, mv, s);
   }
   if (a.T * a.G > 8) {  // 9..16 query rows per KV head: two row groups
+    if (fp8 && a.hpi == 2) return launch_gqa_t<true, 2, 2, NST>(a, mk, mv, s);
     if (a.hpi != 1) return cudaErrorInvalidValue;
     return fp8 ? launch_gqa_t<true, 1, 2, NST>(a, mk, mv, s)
                : launch_gqa_t<false, 1, 2, NST>(a, mk, mv, s);

@@ -38,7 +38,7 @@ GQA_CTAS_PER_SM = 3
 
 
 def _expected_hpi(Hkv, fp8, rows_per_head=8):
-    if not fp8 or rows_per_head > 8:
+    if not fp8 or rows_per_head > 16:
         return 1
     return 2 if Hkv % 2 == 0 else 1
 
@@ -239,8 +239,8 @@ def test_decode_validates_before_any_cuda_call():
         assert skv.splitkv_last_error()
 
 
-def test_heads_per_item_is_one_above_eight_rows_per_head():
-    for T, G, want in ((1, 8, 2), (2, 8, 1), (3, 4, 1), (2, 4, 2)):
+def test_heads_per_item_is_one_above_sixteen_rows_per_head():
+    for T, G, want in ((1, 8, 2), (2, 8, 2), (3, 4, 2), (2, 4, 2), (3, 8, 1), (4, 8, 1)):
         d = _desc(T=T, Hq=8 * G, Hkv=8, fp8=True)
         plan = skv.splitkv_plan(d, np.array([300], np.int32), 0, 148)
         assert skv.splitkv_plan_heads_per_item(plan) == _expected_hpi(8, True, T * G) == want

@@ -167,10 +167,15 @@ def test_multi_token_causal(T, G, fp8):
     w = _custom(lens, G=G, Hkv=2, T=T, fp8=fp8, seed=T * 7 + G)
     x = workloads.make_inputs(w, device="cuda")
     ref_o, ref_l = oracle_direct(x)
-    for S in (1, 2, 5):
-        for mode in ((1, 0) if S == 5 else (1,)):
-            out, lse = session(x, S, mode).run()
-            compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} S={S} mode={mode}")
+    # num_sms = 1 makes every plan of more than one item take the two-stage
+    # (several CTAs per SM) kernel form; 0 plans for the device (one wave here)
+    for sms in (0, 1):
+        for S in (1, 2, 5):
+            for mode in ((1, 0) if S == 5 else (1,)):
+                s = session(x, S, mode, num_sms=sms)
+                out, lse = s.run()
+                compare(out, lse, ref_o, ref_l, what=f"T={T} G={G} S={S} mode={mode} sms={sms}")
+                assert s.stats()[1] == 0
 
 
 @pytest.mark.parametrize("T,G,Hkv", [(1, 8, 4), (1, 4, 8), (2, 8, 2), (1, 2, 3)])
