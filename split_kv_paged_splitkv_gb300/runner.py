@@ -10,7 +10,7 @@ import torch
 from . import (SPLITKV_BF16, SPLITKV_COMBINE_SEPARATE, SPLITKV_FP8_E4M3, SPLITKV_LAYOUT_HND,
                SPLITKV_LAYOUT_NHD, make_desc, splitkv_combine_workspace, splitkv_decode,
                splitkv_decode_partials,
-               splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_fixed, splitkv_plan_refresh,
+               splitkv_decode_kv_scales, splitkv_plan, splitkv_plan_fixed,
                splitkv_plan_upload, splitkv_read_stats)
 
 

@@ -8,7 +8,7 @@ import torch
 
 import workloads
 import split_kv_paged_splitkv_gb300 as skv
-from _support import compare, need_gpu, oracle_direct, session
+from _support import compare, need_gpu, oracle_direct
 from split_kv_paged_splitkv_gb300.runner import DecodeSession
 
 pytestmark = pytest.mark.gpu
