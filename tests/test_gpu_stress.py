@@ -27,6 +27,8 @@ def _gpu():
     ("gqa_ctx5900", skv.SPLITKV_COMBINE_SEPARATE, 3000),
     ("gqa_ctx5900", skv.SPLITKV_COMBINE_FUSED, 3000),
     ("fp8_batch8_ctx32k", skv.SPLITKV_COMBINE_SEPARATE, 600),
+    ("spec_t4_gqa_ctx5900", skv.SPLITKV_COMBINE_SEPARATE, 3000),
+    ("spec_t4_gqa_ctx5900", skv.SPLITKV_COMBINE_FUSED, 3000),
 ])
 def test_back_to_back_calls(name, mode, calls):
     w = workloads.WORKLOADS[name]
