@@ -29,9 +29,14 @@ def _gpu():
     ("fp8_batch8_ctx32k", skv.SPLITKV_COMBINE_SEPARATE, 600),
     ("spec_t4_gqa_ctx5900", skv.SPLITKV_COMBINE_SEPARATE, 3000),
     ("spec_t4_gqa_ctx5900", skv.SPLITKV_COMBINE_FUSED, 3000),
+    # two query tokens over the e4m3 batch: two KV heads and two row groups
+    # per item in a multi-wave grid
+    ("fp8_batch8_ctx32k@2", skv.SPLITKV_COMBINE_SEPARATE, 300),
 ])
 def test_back_to_back_calls(name, mode, calls):
-    w = workloads.WORKLOADS[name]
+    w = workloads.WORKLOADS[name.split("@")[0]]
+    if "@" in name:
+        w = w.replace(q_tokens=int(name.split("@")[1]))
     x = workloads.make_inputs(w, device="cuda")
     s = DecodeSession(x.q, x.k_pages, x.v_pages, x.block_table, x.seq_lens, x.seq_lens_host,
                       scale=x.scale, kv_scale=x.kv_scale, num_splits=0, v_dim=w.v_dim,
