@@ -9,6 +9,7 @@
 // is still correct" (empty splits contribute zero weight).
 #include <cuda_runtime.h>
 
+#include "fixed_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,20 +41,25 @@ constexpr int kCombineThreads = 128;
 // shared memory.  WAYS = 1 (small groups; PER_WAY splits per pass): each warp
 // (DL = 32) merges a row of its own over all the splits, 4 rows per CTA,
 // with no shared memory and no CTA barrier.
-template <int WAYS, int PER_WAY>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+template <int WAYS, int PER_WAY, bool CAP>
+__device__ __forceinline__ void combine_body(
     const float* __restrict__ o_part, const float* __restrict__ lse_part,
     const int32_t* __restrict__ groups, int n_parts, int rows, int dv, int T, int Hq, int G,
-    void* out_bf16, float* out_f32, float* lse_out, int pdl, int fixed) {
+    void* out_bf16, float* out_f32, float* lse_out, int pdl, int fixed, const FixedShape& fx) {
   __shared__ float4 red[kCombineThreads];
   __shared__ float red_w[kCombineThreads], red_m[kCombineThreads];
   launch_dependents();
   // The group table of a host plan is uploaded with the plan and never
   // written by a kernel: it is read before waiting for the split kernel, off
-  // the critical path.  A capacity plan's table is written by the split
-  // kernel (the first item of each group), and a group with S = 0 has
-  // nothing to merge.
-  if (fixed && pdl) wait_prerequisites();
+  // the critical path.  A capacity plan's group g = b * U + u has its slots
+  // [g S, g S + S) fixed, but its split count follows the device length of
+  // sequence b: after the wait that length is read together with the
+  // partials of every slot of the group, and the splits past the count are
+  // dropped by select (those slots may hold anything).  A group with no
+  // splits to merge (S_b <= 1) leaves the output the split kernel wrote.
+  // Without the lengths (the standalone merge of a capacity plan's
+  // workspace) the group table the split kernel wrote is read after the wait.
+  if (!CAP && fixed && pdl) wait_prerequisites();
   static_assert(WAYS == 1 || WAYS == 8, "ways");
   constexpr int DL = WAYS == 1 ? 32 : kCombineThreads / WAYS;  // dim lanes of a way
   constexpr int RPC = WAYS == 1 ? kCombineThreads / 32 : 1;    // rows per CTA
@@ -61,18 +67,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   if (WAYS == 1 && n >= rows) return;
   int S = n_parts, slot0 = 0;
   size_t orow = n;
-  if (groups) {
-    const int32_t* g = groups + size_t(blockIdx.x) * kGroupFields;
-    const int b = g[0], hkv = g[1];
-    S = g[2];
-    slot0 = g[3];
-    // rows are numbered hs * T*G + t * G + gg over the group's heads hkv + hs
+  // CAP: the groups of a capacity plan (groups != nullptr)
+  constexpr bool cap = CAP;
+  int S_load = n_parts;  // CAP: the slots loaded, every slot of the group
+  int bcap = 0;  // CAP: the group's sequence
+  if constexpr (CAP) {
+    const int b = blockIdx.x / fx.U, hkv = (blockIdx.x % fx.U) * fx.hpi;
+    bcap = b;
+    slot0 = blockIdx.x * fx.S;
+    S_load = fx.S;
     const int hs = n / (T * G), r = n - hs * (T * G);
     const int t = r / G, gg = r - t * G;
     orow = (size_t(b) * T + t) * Hq + size_t(hkv + hs) * G + gg;
-    if (S == 0) return;
+    if (pdl) wait_prerequisites();
+  } else {
+    if (groups) {
+      const int32_t* g = groups + size_t(blockIdx.x) * kGroupFields;
+      const int b = g[0], hkv = g[1];
+      S = g[2];
+      slot0 = g[3];
+      // rows are numbered hs * T*G + t * G + gg over the group's heads hkv + hs
+      const int hs = n / (T * G), r = n - hs * (T * G);
+      const int t = r / G, gg = r - t * G;
+      orow = (size_t(b) * T + t) * Hq + size_t(hkv + hs) * G + gg;
+      if (S == 0) return;
+    }
+    if (pdl) wait_prerequisites();
   }
-  if (pdl) wait_prerequisites();
   const int tid = threadIdx.x, dl = tid % DL, way = WAYS == 1 ? 0 : tid / DL;
   const int d = blockIdx.z * (DL * 4) + dl * 4;
   const bool dim_ok = d < dv;
@@ -82,7 +103,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 
   float m_run = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = way; s0 < S; s0 += WAYS * PER_WAY) {
+  bool have_S = !cap;  // (a compile-time true without CAP)
+  const int S_end = CAP ? S_load : S;
+  for (int s0 = way; s0 < S_end; s0 += WAYS * PER_WAY) {
     float lv[PER_WAY];
     float4 x[PER_WAY];
 #pragma unroll
@@ -90,10 +113,26 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
       const int s = s0 + u * WAYS;
       lv[u] = -INFINITY;
       x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (s < S) {
+      if (s < S_end) {
         lv[u] = lp[size_t(s) * rows];
         if (dim_ok) x[u] = *reinterpret_cast<const float4*>(op + size_t(s) * ostride);
       }
+    }
+    if (!have_S) {
+      // the group's device length, read after the partials' loads are
+      // issued (read before them it measured 0.25 us slower per 5.9k call)
+      bool bad;
+      const int Sb = fixed_splits(fx, fixed_len_of(fx, fx.seq_lens[bcap], &bad));
+      S = Sb > 1 ? Sb : 0;
+      have_S = true;
+    }
+    if constexpr (CAP) {
+#pragma unroll
+      for (int u = 0; u < PER_WAY; ++u)
+        if (s0 + u * WAYS >= S) {  // past the group's splits: a slot of no split
+          lv[u] = -INFINITY;
+          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     float m_new = m_run;
 #pragma unroll
@@ -110,6 +149,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     }
     m_run = m_new;
   }
+  if (!have_S) {  // a way with no slot of the group (S_load <= way)
+    bool bad;
+    const int Sb = fixed_splits(fx, fixed_len_of(fx, fx.seq_lens[bcap], &bad));
+    S = Sb > 1 ? Sb : 0;
+  }
+  if (cap && S == 0) return;  // the same for the whole CTA (one group)
   float M = m_run, wtot = wsum;
   float4 tot = acc;
   if constexpr (WAYS > 1) {
@@ -166,6 +211,26 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   if (dl == 0 && blockIdx.z == 0 && lse_out) lse_out[orow] = lse_n;
 }
 
+// Host plans and the standalone merge: the group table (or one raw group).
+template <int WAYS, int PER_WAY>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const float* __restrict__ o_part, const float* __restrict__ lse_part,
+    const int32_t* __restrict__ groups, int n_parts, int rows, int dv, int T, int Hq, int G,
+    void* out_bf16, float* out_f32, float* lse_out, int pdl, int fixed) {
+  combine_body<WAYS, PER_WAY, false>(o_part, lse_part, groups, n_parts, rows, dv, T, Hq, G,
+                                     out_bf16, out_f32, lse_out, pdl, fixed, FixedShape{});
+}
+
+// Capacity plans: each group's split count from the device lengths.
+template <int WAYS, int PER_WAY>
+__global__ void __launch_bounds__(kCombineThreads) combine_cap_kernel(
+    const float* __restrict__ o_part, const float* __restrict__ lse_part,
+    const int32_t* __restrict__ groups, int n_parts, int rows, int dv, int T, int Hq, int G,
+    void* out_bf16, float* out_f32, float* lse_out, int pdl, const FixedShape fx) {
+  combine_body<WAYS, PER_WAY, true>(o_part, lse_part, groups, n_parts, rows, dv, T, Hq, G,
+                                    out_bf16, out_f32, lse_out, pdl, 1, fx);
+}
+
 }  // namespace
 
 namespace {
@@ -192,16 +257,19 @@ bool warp_per_row(int max_splits, long groups, int rows, int dv) {
 // Shared-memory carveout: the kernel's 3 KB of shared memory would otherwise
 // cap the resident CTAs below what the registers allow.  Set once per
 // instantiation.
-template <int WAYS, int PER_WAY>
+template <int WAYS, int PER_WAY, bool CAP>
 cudaError_t combine_attrs() {
-  static cudaError_t e = cudaFuncSetAttribute(
-      combine_kernel<WAYS, PER_WAY>, cudaFuncAttributePreferredSharedMemoryCarveout, 50);
+  static cudaError_t e =
+      CAP ? cudaFuncSetAttribute(combine_cap_kernel<WAYS, PER_WAY>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, 50)
+          : cudaFuncSetAttribute(combine_kernel<WAYS, PER_WAY>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, 50);
   return e;
 }
 
-template <int WAYS, int PER_WAY>
+template <int WAYS, int PER_WAY, bool CAP>
 cudaError_t launch_combine_t(const DecodeArgs& a, bool pdl, cudaStream_t s) {
-  cudaError_t e = combine_attrs<WAYS, PER_WAY>();
+  cudaError_t e = combine_attrs<WAYS, PER_WAY, CAP>();
   if (e != cudaSuccess) return e;
   constexpr int RPC = WAYS == 1 ? kCombineThreads / 32 : 1;
   constexpr int DIMS = WAYS == 1 ? 128 : 4 * kCombineThreads / WAYS;  // dims per CTA
@@ -215,10 +283,16 @@ cudaError_t launch_combine_t(const DecodeArgs& a, bool pdl, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<WAYS, PER_WAY>, static_cast<const float*>(a.o_part),
-                            static_cast<const float*>(a.lse_part), a.groups, 0, a.rows, a.dv, a.T,
-                            a.Hq, a.G, a.out, static_cast<float*>(nullptr), a.lse, pdl ? 1 : 0,
-                            a.fixed);
+  if constexpr (CAP)
+    return cudaLaunchKernelEx(&cfg, combine_cap_kernel<WAYS, PER_WAY>,
+                              static_cast<const float*>(a.o_part), static_cast<const float*>(a.lse_part),
+                              a.groups, 0, a.rows, a.dv, a.T, a.Hq, a.G, a.out,
+                              static_cast<float*>(nullptr), a.lse, pdl ? 1 : 0, a.fx);
+  else
+    return cudaLaunchKernelEx(&cfg, combine_kernel<WAYS, PER_WAY>,
+                              static_cast<const float*>(a.o_part), static_cast<const float*>(a.lse_part),
+                              a.groups, 0, a.rows, a.dv, a.T, a.Hq, a.G, a.out,
+                              static_cast<float*>(nullptr), a.lse, pdl ? 1 : 0, a.fixed);
 }
 
 }  // namespace
@@ -226,9 +300,13 @@ cudaError_t launch_combine_t(const DecodeArgs& a, bool pdl, cudaStream_t s) {
 cudaError_t launch_combine(const DecodeArgs& a, bool pdl, void* stream) {
   if (a.n_groups == 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // A capacity plan's decode passes its lengths (a.fx); the standalone merge
+  // of its workspace does not, and reads the group table instead.
+  const bool cap = a.fixed && a.fx.seq_lens != nullptr && a.fx.U > 0 && a.fx.S > 0;
   if (warp_per_row(a.max_splits, a.n_groups, a.rows, a.dv))
-    return launch_combine_t<1, kSmallLoads>(a, pdl, s);
-  return launch_combine_t<8, 8>(a, pdl, s);
+    return cap ? launch_combine_t<1, kSmallLoads, true>(a, pdl, s)
+               : launch_combine_t<1, kSmallLoads, false>(a, pdl, s);
+  return cap ? launch_combine_t<8, 8, true>(a, pdl, s) : launch_combine_t<8, 8, false>(a, pdl, s);
 }
 
 cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n_parts, int rows,
@@ -238,14 +316,14 @@ cudaError_t launch_combine_raw(const float* o_part, const float* lse_part, int n
   dim3 grid(1, rows, (dv + 127) / 128), block(kCombineThreads, 1, 1);  // (small groups)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (warp_per_row(n_parts, 1, rows, dv)) {
-    cudaError_t e = combine_attrs<1, kSmallLoads>();
+    cudaError_t e = combine_attrs<1, kSmallLoads, false>();
     if (e != cudaSuccess) return e;
     grid.y = (rows + 3) / 4;
     combine_kernel<1, kSmallLoads><<<grid, block, 0, s>>>(o_part, lse_part, nullptr, n_parts, rows,
                                                           dv, 1, 1, 1, out_bf16, out_f32, lse_out,
                                                           0, 0);
   } else {
-    cudaError_t e = combine_attrs<8, 8>();
+    cudaError_t e = combine_attrs<8, 8, false>();
     if (e != cudaSuccess) return e;
     grid.z = (dv + 63) / 64;
     combine_kernel<8, 8><<<grid, block, 0, s>>>(o_part, lse_part, nullptr, n_parts, rows, dv, 1, 1,
